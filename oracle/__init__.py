@@ -1,0 +1,167 @@
+"""Float64 CPU oracle for the speculative-decoding verify step.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference legs of ``bench.py`` may import this package; the
+product library never loads it and there is no CPU fallback through it.
+
+The arithmetic lives in ``specdec_oracle.c`` (plain C, IEEE double, OpenMP over
+independent requests); this module only builds it with gcc and marshals numpy
+arrays through ctypes.  It shares no code with the CUDA library.
+
+Parity pins: every function here is pinned in ``tests/test_oracle_pins.py``
+against what the method description fixes (exact enumeration of the output
+law, Lemma 1, the expected-accepted-count sums, a worked exercise, the
+greedy limit, library softmax/argmax, boundary probes of the compare
+conventions); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "specdec_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libspecdec_oracle.so")
+_lib = None
+
+DT_F32 = 0
+DT_BF16 = 1
+ROW_BAD_TOKEN = 1
+ROW_BAD_Q = 2
+ROW_NONFINITE = 4
+ROW_BAD_TEMP = 8
+ROW_BAD_TREE = 16
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (seconds).  Returns the library path."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-shared", "-fPIC", "-Wall",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        p = ctypes.c_void_p
+        i = ctypes.c_int
+        lib.specdec_oracle_verify_linear.argtypes = [p, p, i, p, p, p, i, i, i,
+                                                     p, p, p, p, p, p, p, p, p]
+        lib.specdec_oracle_verify_linear.restype = i
+        lib.specdec_oracle_verify_tree.argtypes = [p, p, i, p, p, p, p, i, i, i, i,
+                                                   p, p, p, p, p, p, p, p, p]
+        lib.specdec_oracle_verify_tree.restype = i
+        lib.specdec_oracle_num_threads.argtypes = []
+        lib.specdec_oracle_num_threads.restype = i
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle's parallel loops use."""
+    return int(_load().specdec_oracle_num_threads())
+
+
+def _dtype_code(dtype: str) -> int:
+    return {"f32": DT_F32, "bf16": DT_BF16}[dtype]
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _storage(a: np.ndarray, dtype: str) -> np.ndarray:
+    want = np.float32 if dtype == "f32" else np.uint16
+    return np.ascontiguousarray(a, dtype=want)
+
+
+def verify_linear(logits, q, dtype, draft_tokens, temperature, uniforms,
+                  diagnostics: bool = True) -> dict:
+    """Run the oracle on host arrays shaped [B, gamma+1, V] / [B, gamma, V] / ...
+
+    Returns numpy arrays: n_accepted, out_tokens, final_token, is_bonus,
+    row_status and, with ``diagnostics``, p_draft, ratio, final_margin,
+    row_diag ([B, gamma, 2]: sum min(p,q), sum max(0, p-q)).
+    """
+    lib = _load()
+    logits = _storage(logits, dtype)
+    q = _storage(q, dtype)
+    B, R, V = logits.shape
+    gamma = R - 1
+    if q.shape != (B, gamma, V):
+        raise ValueError("q must be [B, gamma, V]")
+    toks = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, gamma)
+    temp = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
+    uni = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, R)
+    out = dict(
+        n_accepted=np.empty(B, np.int32), out_tokens=np.empty((B, R), np.int32),
+        final_token=np.empty(B, np.int32), is_bonus=np.empty(B, np.uint8),
+        row_status=np.empty(B, np.int32))
+    if diagnostics:
+        out.update(p_draft=np.empty((B, gamma)), ratio=np.empty((B, gamma)),
+                   final_margin=np.empty(B), row_diag=np.empty((B, gamma, 2)))
+    rc = lib.specdec_oracle_verify_linear(
+        _ptr(logits), _ptr(q), _dtype_code(dtype), _ptr(toks), _ptr(temp), _ptr(uni),
+        B, gamma, V, _ptr(out["n_accepted"]), _ptr(out["out_tokens"]),
+        _ptr(out["final_token"]), _ptr(out["is_bonus"]), _ptr(out["row_status"]),
+        _ptr(out.get("p_draft")), _ptr(out.get("ratio")), _ptr(out.get("final_margin")),
+        _ptr(out.get("row_diag")))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def verify_tree(logits, q, dtype, node_tokens, parent, temperature, uniforms,
+                max_depth: int, diagnostics: bool = True) -> dict:
+    """Run the tree oracle on host arrays [B, N, V] / [B, N] / [B]."""
+    lib = _load()
+    logits = _storage(logits, dtype)
+    q = _storage(q, dtype)
+    B, N, V = logits.shape
+    if q.shape != (B, N, V):
+        raise ValueError("q must be [B, N, V]")
+    toks = np.ascontiguousarray(node_tokens, dtype=np.int32).reshape(B, N)
+    par = np.ascontiguousarray(parent, dtype=np.int32).reshape(B, N)
+    temp = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
+    uni = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, N)
+    D1 = max_depth + 1
+    out = dict(
+        n_accepted=np.empty(B, np.int32), path_nodes=np.empty((B, D1), np.int32),
+        out_tokens=np.empty((B, D1), np.int32), final_token=np.empty(B, np.int32),
+        is_bonus=np.empty(B, np.uint8), row_status=np.empty(B, np.int32))
+    if diagnostics:
+        out.update(p_node=np.empty((B, N)), test_margin=np.empty(B),
+                   final_margin=np.empty(B))
+    rc = lib.specdec_oracle_verify_tree(
+        _ptr(logits), _ptr(q), _dtype_code(dtype), _ptr(toks), _ptr(par), _ptr(temp),
+        _ptr(uni), B, N, V, max_depth, _ptr(out["n_accepted"]), _ptr(out["path_nodes"]),
+        _ptr(out["out_tokens"]), _ptr(out["final_token"]), _ptr(out["is_bonus"]),
+        _ptr(out["row_status"]), _ptr(out.get("p_node")), _ptr(out.get("test_margin")),
+        _ptr(out.get("final_margin")))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def verify_linear_workload(w, diagnostics: bool = True) -> dict:
+    """Oracle on a ``workloads.LinearWorkload``."""
+    return verify_linear(w.logits, w.q, w.dtype, w.draft_tokens, w.temperature,
+                         w.uniforms, diagnostics=diagnostics)
+
+
+def verify_tree_workload(w, diagnostics: bool = True) -> dict:
+    """Oracle on a ``workloads.TreeWorkload``."""
+    return verify_tree(w.logits, w.q, w.dtype, w.node_tokens, w.parent, w.temperature,
+                       w.uniforms, w.max_depth, diagnostics=diagnostics)

@@ -1,0 +1,643 @@
+"""Pins of the float64 oracle against what the method description fixes.
+
+Source: "Chapter 15: Decoding acceleration" of the LLM edge inference notes
+(zsc.github.io llm_edge_inference/chapter15):
+  * section 15.1.2, speculative sampling steps 2-4, the theorem that the
+    output law equals p, Lemma 1 (probability conservation), the law of the
+    accepted count N and its expectation (i.i.d. and exponential decay);
+  * section 15.1.3, the constant-acceptance expectation a(1-a^g)/(1-a);
+  * the exercises (basic exercise 2: p = [0.5, 0.3, 0.2], q = [0.6, 0.3, 0.1]).
+
+Each pin is chosen so that a plausible slip in the oracle (wrong row index,
+wrong sign or missing clamp in the residual, reversed or strict accept
+compare, bonus from the wrong row, non-strict CDF compare, wrong tie rule,
+dropped temperature) fails at least one test.  No expected value here comes
+from the CUDA path.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import special, stats
+
+from speculative_decoding_verification_64_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------
+# helpers (input construction only)
+# ----------------------------------------------------------------------------
+
+def dyadic_rows(rng, rows, V, denom=1024, floor=16):
+    """Probability rows that are exact in float32 and sum to exactly 1."""
+    out = np.empty((rows, V))
+    for r in range(rows):
+        extra = rng.multinomial(denom - floor * V, rng.dirichlet(np.ones(V)))
+        out[r] = (floor + extra) / denom
+    return out
+
+
+def target_rows(logits_f32, T):
+    """Target distributions the oracle must see: softmax(l/T) of the stored
+    float32 logits, by scipy (an independent routine)."""
+    return special.softmax(logits_f32.astype(np.float64) / T, axis=-1)
+
+
+def tile(a, n):
+    return np.ascontiguousarray(np.broadcast_to(a, (n,) + a.shape))
+
+
+# ----------------------------------------------------------------------------
+# worked exercise
+# ----------------------------------------------------------------------------
+
+def test_exercise2_worked_example(oracle_lib):
+    g = json.load(open(os.path.join(GOLDEN, "exercise2_pq.json")))
+    p = np.array(g["p"])
+    q = np.array(g["q"], dtype=np.float32)
+    d = g["derived"]
+    logits = np.stack([np.log(p), np.log(p)]).astype(np.float32)   # rows 0 and 1
+    p_seen = target_rows(logits, 1.0)
+    qf = q.astype(np.float64)
+    # every draft token, accepted (u small) and rejected (u large)
+    cases = []
+    for tok in range(3):
+        for u0 in (1e-3, 0.5, 0.999):
+            for U in (0.01, 0.5, 0.99):
+                cases.append((tok, u0, U))
+    B = len(cases)
+    out = oracle_lib.verify_linear(
+        tile(logits, B), tile(q[None, :], B), "f32",
+        np.array([[c[0]] for c in cases], np.int32), np.ones(B, np.float32),
+        np.array([[c[1], c[2]] for c in cases], np.float32))
+    ratio = out["ratio"][:, 0]
+    for i, (tok, u0, U) in enumerate(cases):
+        want_r = d["accept_prob_per_draft_token"][tok]
+        assert abs(ratio[i] - want_r) < 1e-6
+        assert abs(out["row_diag"][i, 0, 0] - d["sum_min_pq"]) < 1e-6
+        assert abs(out["row_diag"][i, 0, 1] - d["sum_residual"]) < 1e-6
+        # exact reference with the stored (rounded) values
+        r_exact = min(1.0, p_seen[0, tok] / qf[tok])
+        assert abs(ratio[i] - r_exact) < 1e-15
+        if u0 <= r_exact:
+            assert out["n_accepted"][i] == 1 and out["is_bonus"][i] == 1
+        else:
+            assert out["n_accepted"][i] == 0 and out["is_bonus"][i] == 0
+            assert out["final_token"][i] == d["corrected_token_after_any_rejection"]
+    # the residual is concentrated on token 2 with mass 0.1
+    res = np.maximum(p_seen[0] - qf, 0)
+    assert np.allclose(res, d["residual"], atol=1e-6)
+
+
+# ----------------------------------------------------------------------------
+# exact enumeration of the output law (the theorem of section 15.1.2)
+# ----------------------------------------------------------------------------
+
+def _linear_cells(p, q, gamma, V):
+    """All decision cells of the verify step for a fixed set of rows.
+
+    For every draft tuple (weight prod q_i(x_i)) and every stopping point j,
+    and every token v of the final draw, returns the probability of that cell
+    (accept test passes with probability min(1, p/q); final draw law = w/Z)
+    and a uniform vector strictly inside it."""
+    cells = []
+    for x in itertools.product(range(V), repeat=gamma):
+        wt = np.prod([q[i][x[i]] for i in range(gamma)])
+        if wt == 0:
+            continue
+        r = [min(1.0, p[i][x[i]] / q[i][x[i]]) for i in range(gamma)]
+        for j in range(gamma + 1):
+            pj = wt * np.prod(r[:j]) * ((1.0 - r[j]) if j < gamma else 1.0)
+            if pj <= 0:
+                continue
+            w = np.maximum(p[j] - q[j], 0.0) if j < gamma else p[gamma].copy()
+            if w.sum() <= 0:
+                w = p[j].copy()
+            Z = w.sum()
+            C = np.cumsum(w)
+            for v in range(V):
+                if w[v] <= 0:
+                    continue
+                U = (C[v] - w[v] / 2) / Z
+                u = [r[i] / 2 for i in range(j)]
+                if j < gamma:
+                    u.append((1.0 + r[j]) / 2)
+                u += [0.5] * (gamma - len(u))
+                u.append(U)
+                checkable = (w[v] / Z > 1e-6) and (j == gamma or 1.0 - r[j] > 1e-6)
+                cells.append(dict(x=x, j=j, v=v, prob=pj * w[v] / Z, u=u,
+                                  checkable=checkable))
+    return cells
+
+
+@pytest.mark.parametrize("V,gamma,T,seed", [(3, 2, 1.0, 0), (4, 3, 0.7, 1), (4, 2, 1.6, 2)])
+def test_enumerated_output_law_is_p(oracle_lib, V, gamma, T, seed):
+    rng = np.random.default_rng(seed)
+    logits = rng.normal(0, 1.5, size=(gamma + 1, V)).astype(np.float32)
+    p = target_rows(logits, T)
+    q = dyadic_rows(rng, gamma, V)
+    cells = _linear_cells(p, q, gamma, V)
+    B = len(cells)
+    out = oracle_lib.verify_linear(
+        tile(logits, B), tile(q.astype(np.float32), B), "f32",
+        np.array([c["x"] for c in cells], np.int32), np.full(B, T, np.float32),
+        np.array([c["u"] for c in cells], np.float32))
+    assert (out["row_status"] == 0).all()
+    checked = 0
+    for i, c in enumerate(cells):
+        if not c["checkable"]:
+            continue
+        checked += 1
+        assert out["n_accepted"][i] == c["j"], c
+        assert out["final_token"][i] == c["v"], c
+        assert out["is_bonus"][i] == (c["j"] == gamma)
+        want = list(c["x"][:c["j"]]) + [c["v"]] + [-1] * (gamma - c["j"])
+        assert list(out["out_tokens"][i]) == want
+    assert checked >= 0.95 * B
+    probs = np.array([c["prob"] for c in cells])
+    assert abs(probs.sum() - 1.0) < 1e-12
+    # law of the first emitted token is p_0
+    first = np.array([c["x"][0] if c["j"] > 0 else c["v"] for c in cells])
+    law = np.bincount(first, weights=probs, minlength=V)
+    assert np.max(np.abs(law - p[0])) < 1e-12
+    # given the first j drafts were accepted, the next emitted token ~ p_j
+    for jc in range(1, gamma + 1):
+        sel = [k for k, c in enumerate(cells) if c["j"] >= jc]
+        tokj = np.array([cells[k]["x"][jc] if cells[k]["j"] > jc else cells[k]["v"]
+                         for k in sel])
+        lw = np.bincount(tokj, weights=probs[sel], minlength=V)
+        assert np.max(np.abs(lw / probs[sel].sum() - p[jc])) < 1e-12
+
+
+def test_boundary_conventions(oracle_lib):
+    """u == min(1,p/q) accepts (the chapter's "u <= alpha"); the CDF draw is
+    strict (first C_v > U Z); ties of the greedy argmax go to the lowest index."""
+    V = 4
+    logits = np.zeros((2, V), np.float32)           # p = 1/4 each, exactly
+    q = np.array([[0.5, 0.5, 0.0, 0.0]], np.float32)  # r(token 0) = 0.5 exactly
+    cases = [  # (u0, U, expected n_acc, expected final)
+        (0.5, 0.5, 1, 2),          # u == r accepts; bonus U*Z = 0.5 = C_1 -> v = 2
+        (0.5000001, 0.25, 0, 2),   # just above r rejects; residual (p-q)+ = [0,0,.25,.25]
+        (0.5000001, 0.5, 0, 3),    # residual C = [0,0,.25,.5]; U*Z = .25 = C_2 -> v = 3
+        (0.25, 0.25, 1, 1),        # bonus: U*Z = .25 = C_0 -> v = 1
+        (0.25, 0.2499999, 1, 0),
+    ]
+    B = len(cases)
+    out = oracle_lib.verify_linear(
+        tile(logits, B), tile(q, B), "f32", np.zeros((B, 1), np.int32),
+        np.ones(B, np.float32), np.array([[c[0], c[1]] for c in cases], np.float32))
+    for i, c in enumerate(cases):
+        assert out["n_accepted"][i] == c[2], (i, c)
+        assert out["final_token"][i] == c[3], (i, c)
+
+
+# ----------------------------------------------------------------------------
+# Monte Carlo with the Philox uniform buffer (the oracle's u-driven path)
+# ----------------------------------------------------------------------------
+
+def _mc_linear(oracle_lib, p_logits, q, T, n, seed):
+    gamma = q.shape[0]
+    V = q.shape[1]
+    rng = np.random.default_rng(seed + 100)
+    toks = np.stack([rng.choice(V, size=n, p=q[i] / q[i].sum()) for i in range(gamma)],
+                    axis=1).astype(np.int32)
+    uni = W.philox_uniforms(seed, (n, gamma + 1))
+    out = oracle_lib.verify_linear(tile(p_logits, n), tile(q.astype(np.float32), n), "f32",
+                                   toks, np.full(n, T, np.float32), uni, diagnostics=False)
+    assert (out["row_status"] == 0).all()
+    return out
+
+
+def _assert_freq(samples, p, V, z=5.0):
+    n = samples.size
+    f = np.bincount(samples, minlength=V) / n
+    sd = np.sqrt(np.maximum(p * (1 - p), 1e-12) / n)
+    assert np.all(np.abs(f - p) <= z * sd + 1e-12), (f, p)
+
+
+def test_mc_output_law_and_count_law(oracle_lib):
+    V, gamma, n, T = 4, 3, 400_000, 0.9
+    rng = np.random.default_rng(11)
+    logits = rng.normal(0, 1.2, size=(gamma + 1, V)).astype(np.float32)
+    p = target_rows(logits, T)
+    q = dyadic_rows(rng, gamma, V)
+    out = _mc_linear(oracle_lib, logits, q, T, n, seed=21)
+    _assert_freq(out["out_tokens"][:, 0], p[0], V)
+    for j in range(1, gamma + 1):
+        m = out["n_accepted"] >= j
+        _assert_freq(out["out_tokens"][m, j], p[j], V)
+    # law of N: P(N=k) = prod_{i<k} a_i (1 - a_k), a_i = sum_x min(p_i, q_i)
+    a = np.minimum(p[:gamma], q).sum(axis=1)
+    pk = np.array([np.prod(a[:k]) * (1 - a[k]) for k in range(gamma)] + [np.prod(a)])
+    obs = np.bincount(out["n_accepted"], minlength=gamma + 1)
+    chi = stats.chisquare(obs, pk * n)
+    assert chi.pvalue > 1e-4
+
+
+def _iid_rows(alphas):
+    """V = 2 rows with p_i = (a_i, 1 - a_i) and q_i = (1, 0): the drafted token
+    is always 0 and min(1, p/q) = a_i exactly as the rows fix it."""
+    gamma = len(alphas)
+    p = np.array([[a, 1 - a] for a in alphas] + [[0.5, 0.5]])
+    logits = np.log(p).astype(np.float32)
+    q = np.tile(np.array([1.0, 0.0]), (gamma, 1))
+    return logits, q
+
+
+@pytest.mark.parametrize("alpha,gamma", [(0.8, 4), (0.6, 8), (0.9, 1)])
+def test_expected_accepted_iid(oracle_lib, alpha, gamma):
+    n = 500_000
+    logits, q = _iid_rows([alpha] * gamma)
+    a = target_rows(logits, 1.0)[0, 0]                 # the alpha the rows realise
+    out = _mc_linear(oracle_lib, logits, q, 1.0, n, seed=31 + gamma)
+    N = out["n_accepted"].astype(np.float64)
+    se = N.std() / math.sqrt(n)
+    # section 15.1.2: E[N] = sum_{k<g} k a^k (1-a) + g a^g ; section 15.1.3: a(1-a^g)/(1-a)
+    by_sum = sum(k * a ** k * (1 - a) for k in range(gamma)) + gamma * a ** gamma
+    closed = a * (1 - a ** gamma) / (1 - a)
+    assert abs(by_sum - closed) < 1e-12
+    assert abs(N.mean() - closed) < 4 * se
+    # the law of N itself (section 15.1.2, "distribution of accepted tokens")
+    pk = np.array([a ** k * (1 - a) for k in range(gamma)] + [a ** gamma])
+    obs = np.bincount(out["n_accepted"], minlength=gamma + 1)
+    assert stats.chisquare(obs, pk * n).pvalue > 1e-4
+    # the generating-function closed form printed in section 15.1.2,
+    # a[1 - (g+1)a^g + g a^(g+1)] / (1-a)^2, is sum_{k=0}^{g} k a^k: it equals
+    # E[N] only for g = 1.  The oracle follows the defining sum.
+    printed = a * (1 - (gamma + 1) * a ** gamma + gamma * a ** (gamma + 1)) / (1 - a) ** 2
+    assert abs(printed - sum(k * a ** k for k in range(gamma + 1))) < 1e-12
+    if gamma == 1:
+        assert abs(printed - closed) < 1e-12
+    else:
+        assert abs(N.mean() - printed) > 20 * se
+    # second moment: E[N^2] = sum_k (2k-1) P(N >= k) = sum_{k=1}^{g} (2k-1) a^k
+    m2 = sum((2 * k - 1) * a ** k for k in range(1, gamma + 1))
+    se2 = (N ** 2).std() / math.sqrt(n)
+    assert abs((N ** 2).mean() - m2) < 4 * se2
+
+
+def test_printed_second_moment_is_garbled():
+    """The closed form for E[N^2] printed in section 15.1.2 goes negative
+    (a = 0.8, g = 2 gives -88.8); the defining sum it starts from does not."""
+    a, g = 0.8, 2
+    printed = a * (1 + a - (g * g + 2 * g + 1) * a ** g + (g * g + g) * a ** (g + 1)) / (1 - a) ** 3
+    assert printed < 0
+    by_def = sum(k * k * a ** k * (1 - a) for k in range(g)) + g * g * a ** g
+    assert abs(by_def - sum((2 * k - 1) * a ** k for k in range(1, g + 1))) < 1e-12
+
+
+@pytest.mark.parametrize("alpha,beta,gamma", [(0.9, 0.92, 8), (0.85, 0.95, 6)])
+def test_expected_accepted_exponential_decay(oracle_lib, alpha, beta, gamma):
+    n = 500_000
+    al = [alpha * beta ** i for i in range(gamma)]
+    logits, q = _iid_rows(al)
+    a = target_rows(logits, 1.0)[:gamma, 0]
+    out = _mc_linear(oracle_lib, logits, q, 1.0, n, seed=41 + gamma)
+    N = out["n_accepted"].astype(np.float64)
+    # section 15.1.2 exponential decay: E[N] = sum_{k=1}^{g} a^k b^(k(k-1)/2)
+    closed = sum(alpha ** k * beta ** (k * (k - 1) / 2) for k in range(1, gamma + 1))
+    exact = sum(np.prod(a[:k]) for k in range(1, gamma + 1))
+    assert abs(closed - exact) < 1e-6
+    assert abs(N.mean() - exact) < 4 * N.std() / math.sqrt(n)
+    pk = np.array([np.prod(a[:k]) * (1 - a[k]) for k in range(gamma)] + [np.prod(a)])
+    obs = np.bincount(out["n_accepted"], minlength=gamma + 1)
+    assert stats.chisquare(obs, pk * n).pvalue > 1e-4
+
+
+# ----------------------------------------------------------------------------
+# Lemma 1, softmax, greedy limit
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["linear_b64_g5_v32000_bf16", "linear_b256_g8_v128256_bf16",
+                                  "mixed_b512_g4_v152064_bf16"])
+def test_lemma1_on_workload_rows(oracle_lib, name):
+    w = W.make_workload(name, B=6, V=3000)
+    out = oracle_lib.verify_linear_workload(w)
+    ok = out["row_status"] == 0
+    s = out["row_diag"][ok].sum(axis=-1)
+    assert np.max(np.abs(s - 1.0)) < 1e-12
+
+
+@pytest.mark.parametrize("T", [0.3, 1.0, 1.7])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_target_probability_matches_library_softmax(oracle_lib, T, dtype):
+    B, gamma, V = 8, 3, 1000
+    rng = np.random.default_rng(5)
+    l64 = rng.normal(0, 3, size=(B, gamma + 1, V))
+    logits = W.encode(l64, dtype)
+    seen = W.decode(logits, dtype)
+    q = np.full((B, gamma, V), 1.0 / V)
+    toks = rng.integers(0, V, size=(B, gamma)).astype(np.int32)
+    out = oracle_lib.verify_linear(logits, W.encode(q, dtype), dtype, toks,
+                                   np.full(B, T, np.float32), W.philox_uniforms(9, (B, gamma + 1)))
+    Tf = float(np.float32(T))
+    p = special.softmax(seen / Tf, axis=-1)
+    want = np.take_along_axis(p[:, :gamma], toks[..., None].astype(np.int64), axis=-1)[..., 0]
+    assert np.max(np.abs(out["p_draft"] / want - 1)) < 1e-12
+
+
+def test_greedy_rows_follow_first_argmax(oracle_lib):
+    B, gamma, V = 400, 4, 40
+    rng = np.random.default_rng(3)
+    logits = rng.integers(-3, 4, size=(B, gamma + 1, V)).astype(np.float32)   # many ties
+    amax = logits.argmax(axis=-1)                        # numpy: first occurrence
+    toks = np.where(rng.random((B, gamma)) < 0.7, amax[:, :gamma],
+                    rng.integers(0, V, size=(B, gamma))).astype(np.int32)
+    q = np.full((B, gamma, V), 1.0 / V, np.float32)
+    out = oracle_lib.verify_linear(logits, q, "f32", toks, np.zeros(B, np.float32),
+                                   W.philox_uniforms(4, (B, gamma + 1)))
+    for b in range(B):
+        k = gamma
+        for i in range(gamma):
+            if toks[b, i] != amax[b, i]:
+                k = i
+                break
+        assert out["n_accepted"][b] == k
+        assert out["final_token"][b] == amax[b, k]
+        assert out["is_bonus"][b] == (k == gamma)
+        r = out["ratio"][b]
+        for i in range(gamma):
+            assert r[i] == (1.0 if toks[b, i] == amax[b, i] else 0.0)
+
+
+def test_small_temperature_tends_to_greedy(oracle_lib):
+    B, gamma, V = 200, 3, 64
+    rng = np.random.default_rng(8)
+    # distinct logits spaced >= 0.25 apart: at T = 1e-3 the softmax is one-hot to e^-250
+    base = np.arange(V, dtype=np.float64) * 0.25
+    logits = np.stack([np.stack([rng.permutation(base) for _ in range(gamma + 1)])
+                       for _ in range(B)]).astype(np.float32)
+    amax = logits.argmax(axis=-1)
+    toks = np.where(rng.random((B, gamma)) < 0.6, amax[:, :gamma],
+                    rng.integers(0, V, size=(B, gamma))).astype(np.int32)
+    q = np.full((B, gamma, V), 1.0 / V, np.float32)
+    uni = W.philox_uniforms(12, (B, gamma + 1))
+    g = oracle_lib.verify_linear(logits, q, "f32", toks, np.zeros(B, np.float32), uni)
+    s = oracle_lib.verify_linear(logits, q, "f32", toks, np.full(B, 1e-3, np.float32), uni)
+    for key in ("n_accepted", "final_token", "out_tokens", "is_bonus"):
+        assert np.array_equal(g[key], s[key]), key
+
+
+# ----------------------------------------------------------------------------
+# malformed requests
+# ----------------------------------------------------------------------------
+
+def test_status_bits_and_sentinels(oracle_lib):
+    B, gamma, V = 8, 2, 16
+    rng = np.random.default_rng(1)
+    logits = rng.normal(size=(B, gamma + 1, V)).astype(np.float32)
+    q = np.full((B, gamma, V), 1.0 / V, np.float32)
+    toks = rng.integers(0, V, size=(B, gamma)).astype(np.int32)
+    temp = np.ones(B, np.float32)
+    logits[1, 2, 5] = np.nan
+    logits[2, 0, 3] = np.inf
+    logits[3, 1, :] = -np.inf
+    toks[4, 1] = V
+    q[5, 0, toks[5, 0]] = 0.0
+    temp[6] = -1.0
+    logits[7, 0, :4] = -np.inf                        # partial -inf is a valid row
+    out = oracle_lib.verify_linear(logits, q, "f32", toks, temp,
+                                   W.philox_uniforms(2, (B, gamma + 1)))
+    st = out["row_status"]
+    assert list(st) == [0, oracle_lib.ROW_NONFINITE, oracle_lib.ROW_NONFINITE,
+                        oracle_lib.ROW_NONFINITE, oracle_lib.ROW_BAD_TOKEN,
+                        oracle_lib.ROW_BAD_Q, oracle_lib.ROW_BAD_TEMP, 0]
+    bad = st != 0
+    assert (out["n_accepted"][bad] == 0).all() and (out["final_token"][bad] == -1).all()
+    assert (out["out_tokens"][bad] == -1).all() and (out["is_bonus"][bad] == 0).all()
+    assert out["final_token"][7] >= 4                 # -inf logits have zero mass
+
+
+# ----------------------------------------------------------------------------
+# token tree
+# ----------------------------------------------------------------------------
+
+def _chain_from_linear(w):
+    """The linear workload as a chain tree: node n <-> row n, node n's token
+    is draft n-1, tree slot n <-> linear slot n-1, tree slot 0 <-> slot gamma."""
+    B, g, V = w.B, w.gamma, w.V
+    N = g + 1
+    q = np.zeros((B, N, V), dtype=w.q.dtype)
+    q[:, :g] = w.q
+    q[:, g] = w.q[:, g - 1]                           # leaf row: never read
+    toks = np.zeros((B, N), np.int32)
+    toks[:, 1:] = w.draft_tokens
+    parent = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
+    uni = np.empty((B, N), np.float32)
+    uni[:, 1:] = w.uniforms[:, :g]
+    uni[:, 0] = w.uniforms[:, g]
+    return q, toks, parent, uni
+
+
+@pytest.mark.parametrize("dtype,T", [("f32", 0.8), ("bf16", 1.0), ("bf16", 0.0)])
+def test_chain_tree_equals_linear(oracle_lib, dtype, T):
+    w = W.make_linear("normal2_tq08", B=3000, gamma=5, V=50, dtype=dtype, seed=13)
+    w.temperature[:] = T
+    lin = oracle_lib.verify_linear_workload(w)
+    q, toks, parent, uni = _chain_from_linear(w)
+    tr = oracle_lib.verify_tree(w.logits, q, dtype, toks, parent, w.temperature, uni,
+                                max_depth=w.gamma)
+    for key in ("n_accepted", "final_token", "is_bonus", "row_status", "out_tokens"):
+        assert np.array_equal(lin[key], tr[key]), key
+    D1 = w.gamma + 1
+    for b in range(w.B):
+        k = lin["n_accepted"][b]
+        assert list(tr["path_nodes"][b]) == list(range(k + 1)) + [-1] * (D1 - k - 1)
+    assert 0 < lin["n_accepted"].mean() < w.gamma
+
+
+def _tree_cells_star(p_root, p_child, q, K, V):
+    """Exact cells of a star tree: root with K leaf children whose tokens are
+    i.i.d. from q.  Sibling s is tested against the current P (p_root, then
+    max(0, P - q)/sum after each rejection); an accepted leaf c draws its bonus
+    from p_child[c]; if all are rejected the final token is drawn from P."""
+    cells = []
+    for t in itertools.product(range(V), repeat=K):
+        wt = np.prod([q[x] for x in t])
+        if wt == 0:
+            continue
+        P = p_root.copy()
+        reach = wt
+        rej_u = []
+        for s in range(K):
+            r = min(1.0, P[t[s]] / q[t[s]])
+            if r > 0:
+                pa = reach * r
+                w = p_child[s]
+                C = np.cumsum(w)
+                for v in range(V):
+                    if w[v] <= 0:
+                        continue
+                    u = [0.0] * (K + 1)
+                    u[0] = (C[v] - w[v] / 2) / w.sum()
+                    for s2, uu in enumerate(rej_u):
+                        u[1 + s2] = uu
+                    u[1 + s] = r / 2
+                    for s2 in range(s + 1, K):
+                        u[1 + s2] = 0.5
+                    ok = w[v] / w.sum() > 1e-6 and all(x < 1 - 1e-7 for x in rej_u)
+                    cells.append(dict(t=t, acc=s + 1, v=v, prob=pa * w[v] / w.sum(),
+                                      u=u, checkable=ok, first=t[s]))
+            if r >= 1:
+                reach = 0
+                break
+            rej_u.append((1.0 + r) / 2)
+            reach *= (1 - r)
+            nxt = np.maximum(P - q, 0)
+            if nxt.sum() > 0:
+                P = nxt / nxt.sum()
+        if reach > 0:
+            C = np.cumsum(P)
+            for v in range(V):
+                if P[v] <= 0:
+                    continue
+                u = [0.0] * (K + 1)
+                u[0] = (C[v] - P[v] / 2) / P.sum()
+                for s2, uu in enumerate(rej_u):
+                    u[1 + s2] = uu
+                ok = P[v] / P.sum() > 1e-6 and all(x < 1 - 1e-7 for x in rej_u)
+                cells.append(dict(t=t, acc=None, v=v, prob=reach * P[v] / P.sum(), u=u,
+                                  checkable=ok, first=v))
+    return cells
+
+
+@pytest.mark.parametrize("V,K,seed", [(3, 2, 0), (4, 3, 1), (3, 3, 2)])
+def test_tree_enumerated_law_is_p(oracle_lib, V, K, seed):
+    rng = np.random.default_rng(seed + 50)
+    N = K + 1
+    logits = rng.normal(0, 1.3, size=(N, V)).astype(np.float32)
+    p = target_rows(logits, 1.0)
+    q_root = dyadic_rows(rng, 1, V)[0]
+    cells = _tree_cells_star(p[0], p[1:], q_root, K, V)
+    B = len(cells)
+    qrows = np.tile(q_root.astype(np.float32), (N, 1))
+    toks = np.array([[0] + list(c["t"]) for c in cells], np.int32)
+    parent = np.tile(np.array([-1] + [0] * K, np.int32), (B, 1))
+    out = oracle_lib.verify_tree(tile(logits, B), tile(qrows, B), "f32", toks, parent,
+                                 np.ones(B, np.float32), np.array([c["u"] for c in cells],
+                                                                  np.float32), max_depth=1)
+    assert (out["row_status"] == 0).all()
+    checked = 0
+    for i, c in enumerate(cells):
+        if not c["checkable"]:
+            continue
+        checked += 1
+        if c["acc"] is None:
+            assert out["n_accepted"][i] == 0 and out["is_bonus"][i] == 0, c
+            assert out["final_token"][i] == c["v"], c
+        else:
+            assert out["n_accepted"][i] == 1 and out["is_bonus"][i] == 1, c
+            assert out["path_nodes"][i, 1] == c["acc"], c
+            assert out["final_token"][i] == c["v"], c
+    assert checked >= 0.95 * B
+    probs = np.array([c["prob"] for c in cells])
+    assert abs(probs.sum() - 1) < 1e-12
+    law = np.bincount([c["first"] for c in cells], weights=probs, minlength=V)
+    assert np.max(np.abs(law - p[0])) < 1e-12
+
+
+def test_tree_mc_two_level_law(oracle_lib):
+    """Root -> nodes 1, 2; node 1 -> nodes 3, 4; node 2 -> node 5 (all siblings
+    i.i.d. from the parent's q).  First emitted token ~ p_0; given the walk
+    accepted node c at depth 1, the next emitted token ~ p_c."""
+    V, n = 4, 300_000
+    parent1 = np.array([-1, 0, 0, 1, 1, 2], np.int32)
+    N = parent1.size
+    rng = np.random.default_rng(77)
+    logits = rng.normal(0, 1.0, size=(N, V)).astype(np.float32)
+    p = target_rows(logits, 1.0)
+    q = dyadic_rows(rng, N, V)
+    toks = np.zeros((n, N), np.int32)
+    for node in range(1, N):
+        qp = q[parent1[node]]
+        toks[:, node] = rng.choice(V, size=n, p=qp)
+    out = oracle_lib.verify_tree(tile(logits, n), tile(q.astype(np.float32), n), "f32", toks,
+                                 tile(parent1, n), np.ones(n, np.float32),
+                                 W.philox_uniforms(66, (n, N)), max_depth=2, diagnostics=False)
+    assert (out["row_status"] == 0).all()
+    _assert_freq(out["out_tokens"][:, 0], p[0], V)
+    for c in (1, 2):
+        m = out["path_nodes"][:, 1] == c
+        assert m.sum() > 10_000
+        _assert_freq(out["out_tokens"][m, 1], p[c], V)
+
+
+def test_tree_residual_identity():
+    """After j rejected siblings the literally renormalised residual equals
+    (p - c_j q)+ / N_j with c_0 = 0, N_0 = 1, c_{j+1} = c_j + N_j and
+    N_{j+1} = sum (p - c_{j+1} q)+ (derived by induction; lets a kernel keep
+    only two scalars instead of a residual row)."""
+    rng = np.random.default_rng(4)
+    for _ in range(50):
+        V = 200
+        p = rng.dirichlet(np.ones(V) * 0.5)
+        q = rng.dirichlet(np.ones(V) * 0.5)
+        P = p.copy()
+        c, Nj = 0.0, 1.0
+        for _j in range(6):
+            lit = np.maximum(P - q, 0)
+            if lit.sum() <= 0:
+                break
+            P = lit / lit.sum()
+            c = c + Nj
+            Nj = np.maximum(p - c * q, 0).sum()
+            ident = np.maximum(p - c * q, 0) / Nj
+            assert np.max(np.abs(P - ident)) < 1e-12
+
+
+def test_tree_greedy_walk(oracle_lib):
+    B, N, V = 300, 20, 12
+    w = W.make_tree(B, N, V, "f32", seed=5, max_depth=4, branching=3)
+    rng = np.random.default_rng(9)
+    logits = rng.integers(-2, 3, size=(B, N, V)).astype(np.float32)
+    amax = logits.argmax(axis=-1)
+    toks = w.node_tokens.copy()
+    # make some children carry their parent's argmax token
+    for b in range(B):
+        for n in range(1, N):
+            if rng.random() < 0.4:
+                toks[b, n] = amax[b, w.parent[b, n]]
+    temp = np.zeros(B, np.float32)
+    out = oracle_lib.verify_tree(logits, w.q, "f32", toks, w.parent, temp, w.uniforms,
+                                 max_depth=4)
+    for b in range(B):
+        cur, path = 0, [0]
+        while True:
+            kids = [n for n in range(N) if w.parent[b, n] == cur]
+            hit = [n for n in kids if toks[b, n] == amax[b, cur]]
+            if hit:
+                cur = hit[0]
+                path.append(cur)
+                continue
+            break
+        assert list(out["path_nodes"][b][:len(path)]) == path
+        assert out["n_accepted"][b] == len(path) - 1
+        assert out["final_token"][b] == amax[b, cur]
+        leaf = not any(w.parent[b, n] == cur for n in range(N))
+        assert out["is_bonus"][b] == leaf
+
+
+def test_tree_status_bits(oracle_lib):
+    w = W.make_tree(6, 10, 30, "f32", seed=2, max_depth=3, branching=3)
+    parent = w.parent.copy()
+    toks = w.node_tokens.copy()
+    logits = w.logits.copy()
+    parent[1, 0] = 0                      # root must have parent -1
+    parent[2, 5] = 7                      # forward reference
+    toks[3, 4] = -2
+    logits[4, 9, 0] = np.nan
+    out = oracle_lib.verify_tree(logits, w.q, "f32", toks, parent, w.temperature,
+                                 w.uniforms, max_depth=3)
+    st = out["row_status"]
+    assert st[0] == 0 and st[5] == 0
+    assert st[1] & oracle_lib.ROW_BAD_TREE and st[2] & oracle_lib.ROW_BAD_TREE
+    assert st[3] == oracle_lib.ROW_BAD_TOKEN and st[4] == oracle_lib.ROW_NONFINITE
+    # depth bound: the same trees are too deep for max_depth = 1
+    out2 = oracle_lib.verify_tree(w.logits, w.q, "f32", w.node_tokens, w.parent,
+                                  w.temperature, w.uniforms, max_depth=1)
+    deep = np.array([(np.bincount(np.r_[0, w.parent[b, 1:]]) > 0).sum() > 1 for b in range(6)])
+    assert (out2["row_status"][deep] & oracle_lib.ROW_BAD_TREE).all()
