@@ -1,0 +1,522 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 verify step of speculative decoding.
+
+A step is one pass of the whole hot path over one batch: the row-statistics
+pass over every logit (phase 1) and the accept test + final draw (phase 2),
+for the default workload "linear_b256_g8_v128256_bf16" (B=256 requests,
+gamma=8 drafts, V=128256, bf16 logits, Zipf-shaped logits at T=0.7).
+
+Prints ONE JSON line (rank 0):
+  value      verified draft positions / s over all ranks (B * gamma per step),
+             inputs resident in HBM, CUDA events on the launching stream;
+  e2e        the same metric through the public call with pinned HOST
+             buffers: host->device copy of the step's inputs, the verify call
+             and device->host copy of its outputs inside the timed region;
+  roofline   the row-statistics kernel: algorithmic bytes per launch / its
+             CUDA-event time against the measured HBM copy peak;
+  cpu_baseline  the float64 oracle on the host cores, on a bounded sample.
+
+--impl reference times the oracle (the only other implementation there is)
+on the host cores instead.  Multi-rank (torchrun): every rank verifies its
+own batch (weak scaling, no collective on the data path); the timing is the
+max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verification_64_gb300 import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "linear_b256_g8_v128256_bf16"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "verified draft positions/sec and HBM GB/s (fraction of 8 TB/s) per verify step"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (weak scaling: one independent batch per rank)
+# ----------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float, device) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float, device) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    src = os.path.join(ROOT, "speculative_decoding_verification_64_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("row_stats.cu", "common.cuh"):
+        with open(os.path.join(src, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per row-stats launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "row_stats_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    want = kernel_source_hash()
+    for ln in lines:
+        if ln.startswith("#") or not ln.strip():
+            continue
+        kv = dict(x.split("=", 1) for x in ln.split() if "=" in x)
+        if kv.get("workload") == workload and kv.get("kernel_sha") == want:
+            try:
+                return float(kv["bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def mark(self, which):
+        if which == "begin":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [ln for t, ln in self.lines if self.t0 is not None and self.t0 <= t <= (self.t1 or t) + 0.06]
+        if not rows:
+            rows = [ln for _, ln in self.lines[-3:]]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in rows:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+def algorithmic_bytes(w, n_accepted_rows_rejected: float) -> dict:
+    """Bytes the method must move per step: every logit once, the q row of
+    each rejected request, the gathered p/q values and the small per-request
+    inputs and outputs."""
+    es = w.elem_bytes
+    R = w.rows
+    gamma = R - 1 if isinstance(w, W.LinearWorkload) else R - 1
+    logits = w.B * R * w.V * es
+    q_rows = n_accepted_rows_rejected * w.V * es
+    small = w.B * gamma * (2 * es + 4) + w.B * R * 4 + w.B * 4 + w.B * (R + 4) * 4
+    return dict(logits=logits, q_rows=q_rows, small=small, total=logits + q_rows + small)
+
+
+def run_ours(args, dist):
+    import torch
+    from speculative_decoding_verification_64_gb300 import binding
+    from speculative_decoding_verification_64_gb300 import build as builder
+
+    torch.cuda.set_device(dist.local_rank)
+    device = torch.device("cuda", dist.local_rank)
+    dist.init("nccl")
+    if dist.local_rank == 0:
+        builder.build()
+    dist.barrier()
+    binding.load_library()
+
+    w = W.make_workload(args.workload, seed_offset=1000 * dist.rank)
+    linear = isinstance(w, W.LinearWorkload)
+    R = w.rows
+    es = w.elem_bytes
+    if linear:
+        inputs = binding.linear_inputs_to_device(w, device)
+        gamma = w.gamma
+        units = w.B * gamma               # verified draft positions per step
+    else:
+        inputs = binding.tree_inputs_to_device(w, device)
+        gamma = w.N - 1
+        units = w.B * (w.N - 1)
+    # two resident input sets, alternated step to step (each > L2 for the bench workloads)
+    sets = [inputs, tuple(t.clone() for t in inputs)]
+    dt = binding.dtype_code(inputs[0])
+    ws = binding.alloc_workspace(w.B, R, w.V, dt, device)
+    out = (binding.LinearOut.empty(w.B, w.gamma, device) if linear
+           else binding.TreeOut.empty(w.B, w.N, w.max_depth, device))
+    stream = torch.cuda.current_stream(device)
+    lib = binding.load_library()
+
+    def step(s):
+        x = sets[s & 1]
+        binding.row_stats(x[0], x[4] if not linear else x[3], ws, stream=stream)
+        if linear:
+            binding.linear_finalize(*x, out, ws, stream=stream)
+        else:
+            binding.tree_finalize(*x, w.max_depth, out, ws, stream=stream)
+
+    def step_timed(s, e0, e1, e2):
+        x = sets[s & 1]
+        e0.record(stream)
+        binding.row_stats(x[0], x[4] if not linear else x[3], ws, stream=stream)
+        e1.record(stream)
+        if linear:
+            binding.linear_finalize(*x, out, ws, stream=stream)
+        else:
+            binding.tree_finalize(*x, w.max_depth, out, ws, stream=stream)
+        e2.record(stream)
+
+    for s in range(max(args.warmup, 3)):
+        step(s)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(dist.local_rank) if dist.rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("begin")
+    for s in range(K):
+        step_timed(s, *ev[s])
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("end")
+    dist.barrier()
+    clocks = sampler.stop() if sampler else None
+
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    k1_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    k2_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    total_ms = dist.max(total_ms, device)
+    ms_per_step = total_ms / K
+    value = dist.sum(units, device) * K / (total_ms / 1e3)
+
+    # rejected requests in the last step: their q row is part of the algorithmic bytes
+    nb = out.is_bonus.cpu().numpy()
+    rejected = float((nb == 0).sum())
+    ab = algorithmic_bytes(w, rejected)
+    gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # roofline of the dominant kernel (row statistics)
+    P = _splits(lib, w.B, R, w.V, dt)
+    k1_bytes = ab["logits"] + w.B * R * P * 16
+    k1_gbs = k1_bytes / (k1_ms / 1e3) / 1e9
+    traffic = ncu_traffic(args.workload)
+    roofline = {"bound": "hbm", "kernel": "row_stats_kernel", "achieved": round(k1_gbs, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(k1_gbs / peak, 4),
+                "peak_kind": peak_kind, "traffic": traffic,
+                "algorithmic_bytes_per_launch": int(k1_bytes), "avg_launch_us": round(k1_ms * 1e3, 2)}
+
+    # ---- e2e: pinned host buffers through the public verify call ----
+    e2e = run_e2e(args, w, linear, device, stream, dist, units)
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, linear, units, args.cpu_seconds)
+
+    res = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "positions/s",
+        "n_gpus": dist.world,
+        "steps": K,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": _config(w, args.workload, linear),
+        "requests_per_s": round(dist.sum(w.B, device) * K / (total_ms / 1e3), 1),
+        "accepted_tokens_per_s": round(dist.sum(float(out.n_accepted.sum().item() + w.B), device)
+                                       * K / (total_ms / 1e3), 1),
+        "gbs": round(gbs, 1),
+        "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+        "frac_of_measured_hbm": round(gbs / peak, 4),
+        "algorithmic_bytes_per_step": int(ab["total"]),
+        "phase_us": {"row_stats": round(k1_ms * 1e3, 2), "finalize": round(k2_ms * 1e3, 2)},
+        "roofline": roofline,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+    }
+    if dist.rank == 0:
+        print(json.dumps(res), flush=True)
+    dist.close()
+
+
+def _splits(lib, B, R, V, dt):
+    # the workspace holds one 16-byte partial per (row, split), rounded to 256 bytes
+    ws = lib.specdec_workspace_size(B, R, V, dt)
+    return max(1, (ws // 16) // (B * R))
+
+
+def _config(w, name, linear):
+    c = {"workload": name, "B": w.B, "V": w.V, "dtype": w.dtype,
+         "l2": "inputs larger than L2 (two resident input sets alternated)"}
+    if linear:
+        c["gamma"] = w.gamma
+        c["greedy_requests"] = int((w.temperature == 0).sum())
+    else:
+        c["N"] = w.N
+        c["max_depth"] = w.max_depth
+    return c
+
+
+def run_e2e(args, w, linear, device, stream, dist, units):
+    import torch
+    from speculative_decoding_verification_64_gb300 import binding
+
+    def pinned(a, bf16=False):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16) if bf16 else a)
+        t = t.view(torch.bfloat16) if bf16 else t
+        return t.pin_memory()
+
+    bf = w.dtype == "bf16"
+    if linear:
+        host_in = [pinned(w.logits, bf), pinned(w.q, bf), pinned(w.draft_tokens),
+                   pinned(w.temperature), pinned(w.uniforms)]
+    else:
+        host_in = [pinned(w.logits, bf), pinned(w.q, bf), pinned(w.node_tokens),
+                   pinned(w.parent), pinned(w.temperature), pinned(w.uniforms)]
+    dev_in = [torch.empty_like(t, device=device) for t in host_in]
+    out = (binding.LinearOut.empty(w.B, w.gamma, device) if linear
+           else binding.TreeOut.empty(w.B, w.N, w.max_depth, device))
+    ws = binding.alloc_workspace(w.B, w.rows, w.V, binding.dtype_code(dev_in[0]), device)
+    out_fields = [f for f in vars(out) if getattr(out, f) is not None]
+    host_out = {f: torch.empty_like(getattr(out, f), device="cpu").pin_memory() for f in out_fields}
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def one():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        if linear:
+            binding.verify_linear(*dev_in, out=out, workspace=ws, stream=stream)
+        else:
+            binding.verify_tree(*dev_in, w.max_depth, out=out, workspace=ws, stream=stream)
+        for f in out_fields:
+            host_out[f].copy_(getattr(out, f), non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    n = max(1, min(args.e2e_steps, args.steps))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = dist.max(e0.elapsed_time(e1), device)
+    val = dist.sum(units, device) * n / (ms / 1e3)
+    return {"value": round(val, 1), "unit": "positions/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": round(ms / n, 4)}
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host cores
+# ----------------------------------------------------------------------------
+
+def _oracle_run(o, w, linear):
+    if linear:
+        return o.verify_linear_workload(w, diagnostics=False)
+    return o.verify_tree_workload(w, diagnostics=False)
+
+
+def cpu_baseline(w, linear, units, seconds):
+    import oracle
+    oracle.build()
+    per_req = units / w.B
+    # size the sample: time a few requests, then take enough for ~`seconds`
+    probe = w.subset(np.arange(min(w.B, max(1, oracle.num_threads()))))
+    t = time.perf_counter()
+    _oracle_run(oracle, probe, linear)
+    dt = max(time.perf_counter() - t, 1e-6)
+    reps = max(1, int(seconds / dt))
+    n_req = probe.B * reps
+    t = time.perf_counter()
+    for _ in range(reps):
+        _oracle_run(oracle, probe, linear)
+    el = time.perf_counter() - t
+    return {"value": round(n_req * per_req / el, 1), "unit": "positions/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n_req} requests ({reps} x the first {probe.B} of the workload), "
+                      f"{el:.1f} s, float64 C with OpenMP over requests"}
+
+
+def run_reference(args, dist):
+    if dist.rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = W.make_workload(args.workload)
+    linear = isinstance(w, W.LinearWorkload)
+    units_per_req = w.gamma if linear else w.N - 1
+    cores = oracle.num_threads()
+    # one step = `cores` requests of the workload (one per thread), cycling through the batch
+    per_step = max(1, min(cores, w.B))
+    subsets = [w.subset((np.arange(per_step) + i * per_step) % w.B)
+               for i in range(max(1, w.B // per_step))]
+    for s in range(max(args.warmup, 3)):
+        _oracle_run(oracle, subsets[s % len(subsets)], linear)
+    t = time.perf_counter()
+    for s in range(args.steps):
+        _oracle_run(oracle, subsets[s % len(subsets)], linear)
+    el = time.perf_counter() - t
+    value = args.steps * per_step * units_per_req / el
+    sample = (f"{per_step} requests per step ({args.steps} steps), float64 C oracle, "
+              f"OpenMP over requests")
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "positions/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w, args.workload, linear), "impl": "reference",
+        "cpu_baseline": {"value": round(value, 1), "unit": "positions/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    dist = Dist()
+    if args.impl == "reference":
+        run_reference(args, dist)
+        return 0
+    run_ours(args, dist)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

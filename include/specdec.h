@@ -1,0 +1,192 @@
+/*
+ * specdec.h -- C ABI of the GB300 (sm_103a) verify step of speculative decoding.
+ *
+ * The operation (source: "Chapter 15: Decoding acceleration", LLM edge
+ * inference notes, section 15.1.2 "mathematical framework of speculative
+ * decoding", speculative sampling steps 2-4 and the theorem after them):
+ *
+ *   for one request with gamma drafted tokens x~_0 .. x~_{gamma-1}, the target
+ *   model's logits over gamma+1 positions and the draft's stored
+ *   distributions q_0 .. q_{gamma-1}:
+ *     p_i      = softmax(logits_i / T)              (T = 0: one-hot argmax)
+ *     accept x~_i iff u_i <= min(1, p_i(x~_i) / q_i(x~_i)), i = 0, 1, ...,
+ *              stopping at the first rejection k;
+ *     if k < gamma: final token ~ max(0, p_k - q_k) / Z        (correction)
+ *     else:         final token ~ p_gamma                      (bonus token)
+ *   The emitted tokens are x~_0 .. x~_{k-1} followed by the final token; their
+ *   law is the target model's (the section's theorem).
+ *
+ *   The token-tree form generalises the chain: a node's children were drawn
+ *   i.i.d. from that node's draft distribution; they are tried in ascending
+ *   node index and each rejection replaces the current target distribution P
+ *   by max(0, P - q) / sum (recursive rejection over siblings).  Accepting a
+ *   child descends; a leaf draws a bonus token from its own target row; a node
+ *   whose children are all rejected draws from the renormalised residual.
+ *
+ * Conventions (all functions):
+ *   - every array pointer is a DEVICE pointer owned by the caller; row-major;
+ *   - logits and q hold float32 (SPECDEC_F32) or bfloat16 bits (SPECDEC_BF16),
+ *     both in the same dtype;
+ *   - uniforms are float32 values in (0, 1) that the caller draws (e.g. from a
+ *     counter-based generator); the library draws no random numbers;
+ *   - the library allocates nothing; scratch lives in a caller-provided
+ *     workspace of at least specdec_workspace_size(...) bytes (no
+ *     initialisation needed, contents are overwritten);
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream); work is
+ *     asynchronous and stream-ordered; inputs are read only; outputs are
+ *     overwritten entirely;
+ *   - the return value reports synchronous argument checks and launch errors
+ *     (SPECDEC_ERR_*); data errors inside a request are reported per request
+ *     through row_status[b] (SPECDEC_ROW_* bits) and never trap the device;
+ *     a request with a nonzero status gets n_accepted = 0, is_bonus = 0 and
+ *     -1 in every token output;
+ *   - B = 0 is a no-op that returns SPECDEC_OK.
+ *
+ * Numerics: target probabilities are computed in float32 with base-2
+ * exponentials (exp(z) = 2^(z log2 e)) and compared in float64; the final
+ * draw sums its weights in float32 per 16 elements and in 52-bit fixed point
+ * above that, so the crossing index of the inverse CDF is exact for the
+ * weights the kernel computes.
+ */
+#ifndef SPECDEC_H
+#define SPECDEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPECDEC_ABI_VERSION 1
+
+/* element types of logits and q */
+#define SPECDEC_F32 0
+#define SPECDEC_BF16 1
+
+/* return codes */
+#define SPECDEC_OK 0
+#define SPECDEC_ERR_INVALID_ARG 1 /* null pointer, bad size or dtype */
+#define SPECDEC_ERR_UNSUPPORTED 2 /* sizes beyond the documented limits */
+#define SPECDEC_ERR_WORKSPACE 3   /* workspace missing or too small */
+#define SPECDEC_ERR_CUDA 4        /* a CUDA runtime call or launch failed */
+
+/* per-request status bits written to row_status[b] */
+#define SPECDEC_ROW_OK 0
+#define SPECDEC_ROW_BAD_TOKEN 1  /* a drafted token is outside [0, V) */
+#define SPECDEC_ROW_BAD_Q 2      /* q at a drafted token is <= 0, NaN or inf */
+#define SPECDEC_ROW_NONFINITE 4  /* a target row holds NaN or +inf, or only -inf */
+#define SPECDEC_ROW_BAD_TEMP 8   /* temperature not 0 and not in [1e-20, 1e20] */
+#define SPECDEC_ROW_BAD_TREE 16  /* parent[0] != -1, parent[n] not in [0, n), or depth > max_depth */
+#define SPECDEC_ROW_INTERNAL 32  /* a kernel's bounded wait for its own copy ran out */
+
+/* Limits. */
+#define SPECDEC_MAX_GAMMA 32       /* linear: drafted positions per request */
+#define SPECDEC_MAX_TREE_NODES 1024
+#define SPECDEC_MAX_TREE_DEPTH 64
+#define SPECDEC_MAX_V (1 << 21)
+
+/* ABI version of the loaded library (SPECDEC_ABI_VERSION at build time). */
+int specdec_abi_version(void);
+
+/* Static, human-readable text of a return code or of one SPECDEC_ROW_* bit. */
+const char *specdec_status_string(int code);
+
+/* Bytes of workspace a call with these sizes needs (rows_per_request is
+ * gamma+1 for the linear form and N for the tree form).  Depends only on its
+ * arguments, not on the device.  Returns 0 for invalid sizes. */
+size_t specdec_workspace_size(int B, int rows_per_request, int V, int dtype);
+
+/*
+ * Linear verify (section 15.1.2, steps 2-4; bonus draw per section 15.1.3).
+ *
+ *   logits        [B, gamma+1, V]  target logits; row i scores draft i, row gamma
+ *                                  is the bonus row
+ *   q             [B, gamma, V]    draft probabilities (as stored, no renormalisation)
+ *   draft_tokens  int32 [B, gamma]
+ *   temperature   float32 [B]      0 = greedy (argmax accept test, lowest index on ties)
+ *   uniforms      float32 [B, gamma+1]  slot i: test of draft i; slot gamma: final draw
+ *   n_accepted    int32 [B]        k in [0, gamma]
+ *   out_tokens    int32 [B, gamma+1]  x~_0..x~_{k-1}, final token, then -1
+ *   final_token   int32 [B]        correction or bonus token
+ *   is_bonus      uint8 [B]        1 iff every draft was accepted
+ *   row_status    int32 [B]        SPECDEC_ROW_* bits
+ *   p_draft       float32 [B, gamma] or NULL: p_i(x~_i) for every position
+ *                                  (greedy rows: 1 if x~_i is the argmax, else 0)
+ *   workspace     >= specdec_workspace_size(B, gamma+1, V, dtype) bytes
+ * Limits: 1 <= gamma <= SPECDEC_MAX_GAMMA, 1 <= V <= SPECDEC_MAX_V.
+ */
+int specdec_verify_linear(const void *logits, const void *q, int dtype,
+                          const int32_t *draft_tokens, const float *temperature,
+                          const float *uniforms, int B, int gamma, int V,
+                          int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
+                          uint8_t *is_bonus, int32_t *row_status, float *p_draft,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Phase 1 of either form, callable alone: per-row softmax statistics
+ * (section 15.1.2 step 2) of B*rows_per_request rows of V logits, written
+ * into the workspace as split partials (max, base-2 exponential sum, first
+ * arg-max position).  One streaming pass over the logits.
+ *   logits [B, rows_per_request, V], temperature float32 [B].
+ */
+int specdec_row_stats(const void *logits, int dtype, const float *temperature, int B,
+                      int rows_per_request, int V, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/*
+ * Phase 2 of the linear form: merge the row statistics in the workspace,
+ * run the accept test with early stop (section 15.1.2 step 3) and the
+ * correction / bonus draw (step 4).  Same arguments as specdec_verify_linear;
+ * the workspace must hold phase 1's result for the same logits, B, gamma, V.
+ */
+int specdec_linear_finalize(const void *logits, const void *q, int dtype,
+                            const int32_t *draft_tokens, const float *temperature,
+                            const float *uniforms, int B, int gamma, int V,
+                            int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
+                            uint8_t *is_bonus, int32_t *row_status, float *p_draft,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Token-tree verify (the chain form above with several i.i.d. siblings per
+ * node; siblings tried in ascending node index, residual renormalised after
+ * each rejected sibling; candidate-tree notation of section 15.4.1).
+ *
+ *   logits       [B, N, V]  row n: target distribution after the path to node n
+ *   q            [B, N, V]  row n: draft distribution node n's children were drawn from
+ *   node_tokens  int32 [B, N]  token of node n (entry 0, the root, is ignored)
+ *   parent       int32 [B, N]  parent[0] = -1, 0 <= parent[n] < n
+ *   temperature  float32 [B]
+ *   uniforms     float32 [B, N]  slot 0: final draw; slot n: test of node n
+ *   max_depth    deepest node depth allowed (root = 0)
+ *   n_accepted   int32 [B]      accepted nodes on the path (root excluded)
+ *   path_nodes   int32 [B, max_depth+1]  0, accepted node ids, then -1
+ *   out_tokens   int32 [B, max_depth+1]  accepted tokens, final token, then -1
+ *   final_token, is_bonus, row_status  as in the linear form
+ *   p_node       float32 [B, N] or NULL: p_parent(token of n) before any
+ *                renormalisation (entry 0: 0)
+ *   workspace    >= specdec_workspace_size(B, N, V, dtype) bytes
+ * Limits: 1 <= N <= SPECDEC_MAX_TREE_NODES, 0 <= max_depth <= SPECDEC_MAX_TREE_DEPTH.
+ */
+int specdec_verify_tree(const void *logits, const void *q, int dtype,
+                        const int32_t *node_tokens, const int32_t *parent,
+                        const float *temperature, const float *uniforms, int B, int N, int V,
+                        int max_depth, int32_t *n_accepted, int32_t *path_nodes,
+                        int32_t *out_tokens, int32_t *final_token, uint8_t *is_bonus,
+                        int32_t *row_status, float *p_node, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/* Phase 2 of the tree form (phase 1 is specdec_row_stats with rows_per_request = N). */
+int specdec_tree_finalize(const void *logits, const void *q, int dtype,
+                          const int32_t *node_tokens, const int32_t *parent,
+                          const float *temperature, const float *uniforms, int B, int N,
+                          int V, int max_depth, int32_t *n_accepted, int32_t *path_nodes,
+                          int32_t *out_tokens, int32_t *final_token, uint8_t *is_bonus,
+                          int32_t *row_status, float *p_node, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECDEC_H */

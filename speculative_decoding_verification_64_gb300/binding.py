@@ -1,0 +1,302 @@
+"""ctypes binding of ``libspecdec.so`` (argument marshalling only).
+
+Every step of the verify path runs in the library's CUDA kernels; this module
+checks tensor shapes, dtypes and devices, allocates outputs and the workspace
+with torch (device memory and streams are PyTorch's only role) and passes raw
+device pointers to the C ABI declared in ``include/specdec.h``.  There is no
+CPU fallback: if the library is missing or a call fails, an exception says so.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecdec.so")
+
+F32 = 0
+BF16 = 1
+OK = 0
+ROW_BAD_TOKEN = 1
+ROW_BAD_Q = 2
+ROW_NONFINITE = 4
+ROW_BAD_TEMP = 8
+ROW_BAD_TREE = 16
+ROW_INTERNAL = 32
+
+_lib = None
+
+_EXPORTS = {
+    "specdec_abi_version": ([], ctypes.c_int),
+    "specdec_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "specdec_workspace_size": ([ctypes.c_int] * 4, ctypes.c_size_t),
+    "specdec_row_stats": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                           ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                           ctypes.c_void_p], ctypes.c_int),
+    "specdec_verify_linear": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
+                              [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 +
+                              [ctypes.c_void_p] * 7 + [ctypes.c_size_t, ctypes.c_void_p],
+                              ctypes.c_int),
+    "specdec_linear_finalize": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
+                                [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 +
+                                [ctypes.c_void_p] * 7 + [ctypes.c_size_t, ctypes.c_void_p],
+                                ctypes.c_int),
+    "specdec_verify_tree": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
+                            [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 +
+                            [ctypes.c_void_p] * 8 + [ctypes.c_size_t, ctypes.c_void_p],
+                            ctypes.c_int),
+    "specdec_tree_finalize": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
+                              [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 +
+                              [ctypes.c_void_p] * 8 + [ctypes.c_size_t, ctypes.c_void_p],
+                              ctypes.c_int),
+}
+
+
+class SpecdecError(RuntimeError):
+    pass
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load ``libspecdec.so``; raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise SpecdecError(
+            f"{p} is missing: build it with __graft_entry__.build() or "
+            "`python -m speculative_decoding_verification_64_gb300.build`")
+    lib = ctypes.CDLL(p)
+    for name, (args, res) in _EXPORTS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().specdec_status_string(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise SpecdecError(f"{what} failed: {status_string(rc)} (code {rc})")
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"logits/q must be float32 or bfloat16, got {t.dtype}")
+
+
+def workspace_size(B: int, rows_per_request: int, V: int, dtype: int) -> int:
+    return int(load_library().specdec_workspace_size(B, rows_per_request, V, dtype))
+
+
+def alloc_workspace(B: int, rows_per_request: int, V: int, dtype: int,
+                    device="cuda") -> torch.Tensor:
+    n = max(workspace_size(B, rows_per_request, V, dtype), 256)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _req(t: torch.Tensor, name: str, dtype, shape, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+@dataclasses.dataclass
+class LinearOut:
+    n_accepted: torch.Tensor   # int32 [B]
+    out_tokens: torch.Tensor   # int32 [B, gamma+1]
+    final_token: torch.Tensor  # int32 [B]
+    is_bonus: torch.Tensor     # uint8 [B]
+    row_status: torch.Tensor   # int32 [B]
+    p_draft: Optional[torch.Tensor]  # float32 [B, gamma]
+
+    @staticmethod
+    def empty(B, gamma, device, with_p=True):
+        z = dict(dtype=torch.int32, device=device)
+        return LinearOut(torch.empty(B, **z), torch.empty(B, gamma + 1, **z),
+                         torch.empty(B, **z), torch.empty(B, dtype=torch.uint8, device=device),
+                         torch.empty(B, **z),
+                         torch.empty(B, gamma, dtype=torch.float32, device=device)
+                         if with_p else None)
+
+
+@dataclasses.dataclass
+class TreeOut:
+    n_accepted: torch.Tensor   # int32 [B]
+    path_nodes: torch.Tensor   # int32 [B, max_depth+1]
+    out_tokens: torch.Tensor   # int32 [B, max_depth+1]
+    final_token: torch.Tensor  # int32 [B]
+    is_bonus: torch.Tensor     # uint8 [B]
+    row_status: torch.Tensor   # int32 [B]
+    p_node: Optional[torch.Tensor]   # float32 [B, N]
+
+    @staticmethod
+    def empty(B, N, max_depth, device, with_p=True):
+        z = dict(dtype=torch.int32, device=device)
+        D1 = max_depth + 1
+        return TreeOut(torch.empty(B, **z), torch.empty(B, D1, **z), torch.empty(B, D1, **z),
+                       torch.empty(B, **z), torch.empty(B, dtype=torch.uint8, device=device),
+                       torch.empty(B, **z),
+                       torch.empty(B, N, dtype=torch.float32, device=device) if with_p else None)
+
+
+def _linear_args(logits, q, draft_tokens, temperature, uniforms, out, workspace):
+    B, R, V = logits.shape
+    gamma = R - 1
+    dev = logits.device
+    dt = dtype_code(logits)
+    _req(q, "q", logits.dtype, (B, gamma, V), dev)
+    _req(logits, "logits", logits.dtype, (B, R, V), dev)
+    _req(draft_tokens, "draft_tokens", torch.int32, (B, gamma), dev)
+    _req(temperature, "temperature", torch.float32, (B,), dev)
+    _req(uniforms, "uniforms", torch.float32, (B, R), dev)
+    if out is None:
+        out = LinearOut.empty(B, gamma, dev)
+    if workspace is None:
+        workspace = alloc_workspace(B, R, V, dt, dev)
+    return B, gamma, V, dt, out, workspace
+
+
+def verify_linear(logits: torch.Tensor, q: torch.Tensor, draft_tokens: torch.Tensor,
+                  temperature: torch.Tensor, uniforms: torch.Tensor,
+                  out: Optional[LinearOut] = None, workspace: Optional[torch.Tensor] = None,
+                  stream=None) -> LinearOut:
+    """Linear verify step (``specdec_verify_linear``) on CUDA tensors."""
+    B, gamma, V, dt, out, ws = _linear_args(logits, q, draft_tokens, temperature, uniforms,
+                                            out, workspace)
+    lib = load_library()
+    rc = lib.specdec_verify_linear(
+        _ptr(logits), _ptr(q), dt, _ptr(draft_tokens), _ptr(temperature), _ptr(uniforms),
+        B, gamma, V, _ptr(out.n_accepted), _ptr(out.out_tokens), _ptr(out.final_token),
+        _ptr(out.is_bonus), _ptr(out.row_status), _ptr(out.p_draft), _ptr(ws), ws.numel(),
+        _stream_ptr(stream))
+    _check(rc, "specdec_verify_linear")
+    return out
+
+
+def row_stats(logits: torch.Tensor, temperature: torch.Tensor, workspace: torch.Tensor,
+              stream=None) -> None:
+    """Phase 1 only (``specdec_row_stats``): logits [B, R, V] -> split partials in workspace."""
+    B, R, V = logits.shape
+    rc = load_library().specdec_row_stats(
+        _ptr(logits), dtype_code(logits), _ptr(temperature), B, R, V, _ptr(workspace),
+        workspace.numel(), _stream_ptr(stream))
+    _check(rc, "specdec_row_stats")
+
+
+def linear_finalize(logits, q, draft_tokens, temperature, uniforms, out: LinearOut,
+                    workspace: torch.Tensor, stream=None) -> LinearOut:
+    """Phase 2 of the linear form (``specdec_linear_finalize``)."""
+    B, gamma, V, dt, out, ws = _linear_args(logits, q, draft_tokens, temperature, uniforms,
+                                            out, workspace)
+    rc = load_library().specdec_linear_finalize(
+        _ptr(logits), _ptr(q), dt, _ptr(draft_tokens), _ptr(temperature), _ptr(uniforms),
+        B, gamma, V, _ptr(out.n_accepted), _ptr(out.out_tokens), _ptr(out.final_token),
+        _ptr(out.is_bonus), _ptr(out.row_status), _ptr(out.p_draft), _ptr(ws), ws.numel(),
+        _stream_ptr(stream))
+    _check(rc, "specdec_linear_finalize")
+    return out
+
+
+def _tree_args(logits, q, node_tokens, parent, temperature, uniforms, max_depth, out,
+               workspace):
+    B, N, V = logits.shape
+    dev = logits.device
+    dt = dtype_code(logits)
+    _req(q, "q", logits.dtype, (B, N, V), dev)
+    _req(logits, "logits", logits.dtype, (B, N, V), dev)
+    _req(node_tokens, "node_tokens", torch.int32, (B, N), dev)
+    _req(parent, "parent", torch.int32, (B, N), dev)
+    _req(temperature, "temperature", torch.float32, (B,), dev)
+    _req(uniforms, "uniforms", torch.float32, (B, N), dev)
+    if out is None:
+        out = TreeOut.empty(B, N, max_depth, dev)
+    if workspace is None:
+        workspace = alloc_workspace(B, N, V, dt, dev)
+    return B, N, V, dt, out, workspace
+
+
+def verify_tree(logits, q, node_tokens, parent, temperature, uniforms, max_depth: int,
+                out: Optional[TreeOut] = None, workspace: Optional[torch.Tensor] = None,
+                stream=None) -> TreeOut:
+    """Token-tree verify step (``specdec_verify_tree``) on CUDA tensors."""
+    B, N, V, dt, out, ws = _tree_args(logits, q, node_tokens, parent, temperature, uniforms,
+                                      max_depth, out, workspace)
+    rc = load_library().specdec_verify_tree(
+        _ptr(logits), _ptr(q), dt, _ptr(node_tokens), _ptr(parent), _ptr(temperature),
+        _ptr(uniforms), B, N, V, max_depth, _ptr(out.n_accepted), _ptr(out.path_nodes),
+        _ptr(out.out_tokens), _ptr(out.final_token), _ptr(out.is_bonus), _ptr(out.row_status),
+        _ptr(out.p_node), _ptr(ws), ws.numel(), _stream_ptr(stream))
+    _check(rc, "specdec_verify_tree")
+    return out
+
+
+def tree_finalize(logits, q, node_tokens, parent, temperature, uniforms, max_depth: int,
+                  out: TreeOut, workspace: torch.Tensor, stream=None) -> TreeOut:
+    """Phase 2 of the tree form (``specdec_tree_finalize``)."""
+    B, N, V, dt, out, ws = _tree_args(logits, q, node_tokens, parent, temperature, uniforms,
+                                      max_depth, out, workspace)
+    rc = load_library().specdec_tree_finalize(
+        _ptr(logits), _ptr(q), dt, _ptr(node_tokens), _ptr(parent), _ptr(temperature),
+        _ptr(uniforms), B, N, V, max_depth, _ptr(out.n_accepted), _ptr(out.path_nodes),
+        _ptr(out.out_tokens), _ptr(out.final_token), _ptr(out.is_bonus), _ptr(out.row_status),
+        _ptr(out.p_node), _ptr(ws), ws.numel(), _stream_ptr(stream))
+    _check(rc, "specdec_tree_finalize")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# host <-> device marshalling for numpy workloads
+# ---------------------------------------------------------------------------
+
+def to_device(a, device="cuda", bf16: bool = False) -> torch.Tensor:
+    """numpy array -> CUDA tensor; uint16 arrays with ``bf16`` are bfloat16 bits."""
+    import numpy as np
+    a = np.ascontiguousarray(a)
+    if bf16:
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(a)
+    return t.to(device)
+
+
+def linear_inputs_to_device(w, device="cuda"):
+    """A ``workloads.LinearWorkload`` as CUDA tensors (logits, q, tokens, T, u)."""
+    bf = w.dtype == "bf16"
+    return (to_device(w.logits, device, bf), to_device(w.q, device, bf),
+            to_device(w.draft_tokens, device), to_device(w.temperature, device),
+            to_device(w.uniforms, device))
+
+
+def tree_inputs_to_device(w, device="cuda"):
+    """A ``workloads.TreeWorkload`` as CUDA tensors (logits, q, tokens, parent, T, u)."""
+    bf = w.dtype == "bf16"
+    return (to_device(w.logits, device, bf), to_device(w.q, device, bf),
+            to_device(w.node_tokens, device), to_device(w.parent, device),
+            to_device(w.temperature, device), to_device(w.uniforms, device))

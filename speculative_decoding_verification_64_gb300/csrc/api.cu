@@ -1,0 +1,256 @@
+// C ABI of the verify step: argument checks, workspace sizing and launches.
+// Every entry point is asynchronous on the caller's stream and allocates
+// nothing; see include/specdec.h for the contract of each call.
+#include <climits>
+#include <cstring>
+
+#include "common.cuh"
+
+using namespace specdec;
+
+namespace {
+
+int elem_bytes(int dtype) { return dtype == SPECDEC_F32 ? 4 : 2; }
+
+bool dtype_ok(int dtype) { return dtype == SPECDEC_F32 || dtype == SPECDEC_BF16; }
+
+size_t workspace_bytes_for(long long B, int R, int V, int dtype) {
+  const long long rows = B * (long long)R;
+  const SplitPlan sp = make_split_plan(rows, V, elem_bytes(dtype));
+  const size_t bytes = (size_t)rows * (size_t)sp.splits * sizeof(RowPartial);
+  return (bytes + 255) / 256 * 256;
+}
+
+int check_sizes(int B, int R, int V, int dtype) {
+  if (!dtype_ok(dtype) || B < 0 || R < 1 || V < 1) return SPECDEC_ERR_INVALID_ARG;
+  if (V > SPECDEC_MAX_V) return SPECDEC_ERR_UNSUPPORTED;
+  if ((long long)B * 8 > INT_MAX) return SPECDEC_ERR_UNSUPPORTED;
+  return SPECDEC_OK;
+}
+
+int check_workspace(const void *ws, size_t ws_bytes, int B, int R, int V, int dtype) {
+  const size_t need = workspace_bytes_for(B, R, V, dtype);
+  if (need == 0) return SPECDEC_OK;
+  if (ws == nullptr || ws_bytes < need) return SPECDEC_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 15) != 0) return SPECDEC_ERR_WORKSPACE;
+  return SPECDEC_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA; }
+
+int launch_stats(const void *logits, int dtype, const float *temperature, int B, int R, int V,
+                 void *workspace, cudaStream_t stream) {
+  const long long rows = (long long)B * R;
+  const SplitPlan sp = make_split_plan(rows, V, elem_bytes(dtype));
+  RowStatsParams p;
+  p.logits = logits;
+  p.temperature = temperature;
+  p.part = reinterpret_cast<RowPartial *>(workspace);
+  p.items = rows * sp.splits;
+  p.dtype = dtype;
+  p.R = R;
+  p.V = V;
+  p.P = sp.splits;
+  p.chunk_elems = sp.chunk_elems;
+  return cuda_status(launch_row_stats(p, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int specdec_abi_version(void) { return SPECDEC_ABI_VERSION; }
+
+const char *specdec_status_string(int code) {
+  switch (code) {
+    case SPECDEC_OK: return "ok";
+    case SPECDEC_ERR_INVALID_ARG: return "invalid argument (null pointer, size or dtype)";
+    case SPECDEC_ERR_UNSUPPORTED: return "sizes beyond the supported limits";
+    case SPECDEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SPECDEC_ERR_CUDA: return "CUDA runtime or launch error";
+    default: break;
+  }
+  return "unknown status";
+}
+
+size_t specdec_workspace_size(int B, int rows_per_request, int V, int dtype) {
+  if (check_sizes(B, rows_per_request, V, dtype) != SPECDEC_OK) return 0;
+  return workspace_bytes_for(B, rows_per_request, V, dtype);
+}
+
+int specdec_row_stats(const void *logits, int dtype, const float *temperature, int B,
+                      int rows_per_request, int V, void *workspace, size_t workspace_bytes,
+                      void *stream) {
+  int st = check_sizes(B, rows_per_request, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  if (B == 0) return SPECDEC_OK;
+  if (!logits || !temperature) return SPECDEC_ERR_INVALID_ARG;
+  st = check_workspace(workspace, workspace_bytes, B, rows_per_request, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  return launch_stats(logits, dtype, temperature, B, rows_per_request, V, workspace,
+                      static_cast<cudaStream_t>(stream));
+}
+
+static int linear_checks(const void *logits, const void *q, int dtype, const int32_t *tokens,
+                         const float *temperature, const float *uniforms, int B, int gamma,
+                         int V, int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
+                         uint8_t *is_bonus, int32_t *row_status, void *workspace,
+                         size_t workspace_bytes) {
+  if (gamma < 1) return SPECDEC_ERR_INVALID_ARG;
+  if (gamma > SPECDEC_MAX_GAMMA) return SPECDEC_ERR_UNSUPPORTED;
+  int st = check_sizes(B, gamma + 1, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  if (B == 0) return SPECDEC_OK;
+  if (!logits || !q || !tokens || !temperature || !uniforms || !n_accepted || !out_tokens ||
+      !final_token || !is_bonus || !row_status)
+    return SPECDEC_ERR_INVALID_ARG;
+  return check_workspace(workspace, workspace_bytes, B, gamma + 1, V, dtype);
+}
+
+static int linear_finalize_launch(const void *logits, const void *q, int dtype,
+                                  const int32_t *tokens, const float *temperature,
+                                  const float *uniforms, int B, int gamma, int V,
+                                  int32_t *n_accepted, int32_t *out_tokens,
+                                  int32_t *final_token, uint8_t *is_bonus, int32_t *row_status,
+                                  float *p_draft, void *workspace, cudaStream_t stream) {
+  const SplitPlan sp = make_split_plan((long long)B * (gamma + 1), V, elem_bytes(dtype));
+  LinearFinalizeParams p;
+  p.logits = logits;
+  p.q = q;
+  p.tokens = tokens;
+  p.temperature = temperature;
+  p.uniforms = uniforms;
+  p.part = reinterpret_cast<const RowPartial *>(workspace);
+  p.n_accepted = n_accepted;
+  p.out_tokens = out_tokens;
+  p.final_token = final_token;
+  p.is_bonus = is_bonus;
+  p.row_status = row_status;
+  p.p_draft = p_draft;
+  p.dtype = dtype;
+  p.B = B;
+  p.gamma = gamma;
+  p.V = V;
+  p.P = sp.splits;
+  return cuda_status(launch_linear_finalize(p, stream));
+}
+
+int specdec_linear_finalize(const void *logits, const void *q, int dtype,
+                            const int32_t *draft_tokens, const float *temperature,
+                            const float *uniforms, int B, int gamma, int V,
+                            int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
+                            uint8_t *is_bonus, int32_t *row_status, float *p_draft,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+  const int st = linear_checks(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma,
+                               V, n_accepted, out_tokens, final_token, is_bonus, row_status,
+                               workspace, workspace_bytes);
+  if (st != SPECDEC_OK || B == 0) return st;
+  return linear_finalize_launch(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma,
+                                V, n_accepted, out_tokens, final_token, is_bonus, row_status,
+                                p_draft, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int specdec_verify_linear(const void *logits, const void *q, int dtype,
+                          const int32_t *draft_tokens, const float *temperature,
+                          const float *uniforms, int B, int gamma, int V,
+                          int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
+                          uint8_t *is_bonus, int32_t *row_status, float *p_draft,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+  int st = linear_checks(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
+                         n_accepted, out_tokens, final_token, is_bonus, row_status, workspace,
+                         workspace_bytes);
+  if (st != SPECDEC_OK || B == 0) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = launch_stats(logits, dtype, temperature, B, gamma + 1, V, workspace, s);
+  if (st != SPECDEC_OK) return st;
+  return linear_finalize_launch(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma,
+                                V, n_accepted, out_tokens, final_token, is_bonus, row_status,
+                                p_draft, workspace, s);
+}
+
+static int tree_checks(const void *logits, const void *q, int dtype, const int32_t *tokens,
+                       const int32_t *parent, const float *temperature, const float *uniforms,
+                       int B, int N, int V, int max_depth, int32_t *n_accepted,
+                       int32_t *path_nodes, int32_t *out_tokens, int32_t *final_token,
+                       uint8_t *is_bonus, int32_t *row_status, void *workspace,
+                       size_t workspace_bytes) {
+  if (N < 1 || max_depth < 0) return SPECDEC_ERR_INVALID_ARG;
+  if (N > SPECDEC_MAX_TREE_NODES || max_depth > SPECDEC_MAX_TREE_DEPTH)
+    return SPECDEC_ERR_UNSUPPORTED;
+  int st = check_sizes(B, N, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  if (B == 0) return SPECDEC_OK;
+  if (!logits || !q || !tokens || !parent || !temperature || !uniforms || !n_accepted ||
+      !path_nodes || !out_tokens || !final_token || !is_bonus || !row_status)
+    return SPECDEC_ERR_INVALID_ARG;
+  return check_workspace(workspace, workspace_bytes, B, N, V, dtype);
+}
+
+static int tree_finalize_launch(const void *logits, const void *q, int dtype,
+                                const int32_t *tokens, const int32_t *parent,
+                                const float *temperature, const float *uniforms, int B, int N,
+                                int V, int max_depth, int32_t *n_accepted, int32_t *path_nodes,
+                                int32_t *out_tokens, int32_t *final_token, uint8_t *is_bonus,
+                                int32_t *row_status, float *p_node, void *workspace,
+                                cudaStream_t stream) {
+  const SplitPlan sp = make_split_plan((long long)B * N, V, elem_bytes(dtype));
+  TreeFinalizeParams p;
+  p.logits = logits;
+  p.q = q;
+  p.tokens = tokens;
+  p.parent = parent;
+  p.temperature = temperature;
+  p.uniforms = uniforms;
+  p.part = reinterpret_cast<const RowPartial *>(workspace);
+  p.n_accepted = n_accepted;
+  p.path_nodes = path_nodes;
+  p.out_tokens = out_tokens;
+  p.final_token = final_token;
+  p.is_bonus = is_bonus;
+  p.row_status = row_status;
+  p.p_node = p_node;
+  p.dtype = dtype;
+  p.B = B;
+  p.N = N;
+  p.V = V;
+  p.P = sp.splits;
+  p.max_depth = max_depth;
+  return cuda_status(launch_tree_finalize(p, stream));
+}
+
+int specdec_tree_finalize(const void *logits, const void *q, int dtype,
+                          const int32_t *node_tokens, const int32_t *parent,
+                          const float *temperature, const float *uniforms, int B, int N, int V,
+                          int max_depth, int32_t *n_accepted, int32_t *path_nodes,
+                          int32_t *out_tokens, int32_t *final_token, uint8_t *is_bonus,
+                          int32_t *row_status, float *p_node, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+  const int st = tree_checks(logits, q, dtype, node_tokens, parent, temperature, uniforms, B, N,
+                             V, max_depth, n_accepted, path_nodes, out_tokens, final_token,
+                             is_bonus, row_status, workspace, workspace_bytes);
+  if (st != SPECDEC_OK || B == 0) return st;
+  return tree_finalize_launch(logits, q, dtype, node_tokens, parent, temperature, uniforms, B, N,
+                              V, max_depth, n_accepted, path_nodes, out_tokens, final_token,
+                              is_bonus, row_status, p_node, workspace,
+                              static_cast<cudaStream_t>(stream));
+}
+
+int specdec_verify_tree(const void *logits, const void *q, int dtype, const int32_t *node_tokens,
+                        const int32_t *parent, const float *temperature, const float *uniforms,
+                        int B, int N, int V, int max_depth, int32_t *n_accepted,
+                        int32_t *path_nodes, int32_t *out_tokens, int32_t *final_token,
+                        uint8_t *is_bonus, int32_t *row_status, float *p_node, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+  int st = tree_checks(logits, q, dtype, node_tokens, parent, temperature, uniforms, B, N, V,
+                       max_depth, n_accepted, path_nodes, out_tokens, final_token, is_bonus,
+                       row_status, workspace, workspace_bytes);
+  if (st != SPECDEC_OK || B == 0) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = launch_stats(logits, dtype, temperature, B, N, V, workspace, s);
+  if (st != SPECDEC_OK) return st;
+  return tree_finalize_launch(logits, q, dtype, node_tokens, parent, temperature, uniforms, B, N,
+                              V, max_depth, n_accepted, path_nodes, out_tokens, final_token,
+                              is_bonus, row_status, p_node, workspace, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,248 @@
+// Shared device helpers and launch-side structures of the verify-step kernels.
+// sm_103a only: 1-D bulk TMA copies (cp.async.bulk) completing on shared-memory
+// mbarriers, thread-block clusters with distributed shared memory.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "specdec.h"
+
+namespace specdec {
+
+// ---------------------------------------------------------------------------
+// workspace layout: one partial per (row, split) written by the row-stats pass
+// ---------------------------------------------------------------------------
+struct RowPartial {
+  float m;      // max of the raw logits in the split (-inf if none is finite)
+  float s;      // sum over the split of 2^((l - m) * c), c = log2(e) / T
+  int32_t arg;  // start index of the first 16-byte group (or lone element) holding m
+  int32_t flags;  // SPECDEC_ROW_INTERNAL when a bounded wait ran out
+};
+static_assert(sizeof(RowPartial) == 16, "RowPartial is 16 bytes");
+
+// Split plan of a row-stats pass: a pure function of the sizes, so the
+// workspace size can be computed on the host without a device.
+struct SplitPlan {
+  int splits;       // P: splits per row
+  int chunk_elems;  // elements per split (a multiple of 16 bytes of elements)
+};
+
+inline SplitPlan make_split_plan(long long rows, int V, int elem_bytes) {
+  const long long kTargetItemBytes = 32 * 1024;  // one work item ~ two 16 KB stages
+  const long long kMinItemBytes = 2 * 1024;
+  const long long kTargetItems = 8 * 152;        // keep small batches spread over the SMs
+  const int kMaxSplits = 64;
+  const long long row_bytes = (long long)V * elem_bytes;
+  long long p = (row_bytes + kTargetItemBytes / 2) / kTargetItemBytes;
+  if (p < 1) p = 1;
+  long long p_items = (kTargetItems + rows - 1) / (rows > 0 ? rows : 1);
+  if (p < p_items) p = p_items;
+  long long p_cap = row_bytes / kMinItemBytes;
+  if (p_cap < 1) p_cap = 1;
+  if (p > p_cap) p = p_cap;
+  if (p > kMaxSplits) p = kMaxSplits;
+  const int vec = 16 / elem_bytes;
+  long long chunk = (V + p - 1) / p;
+  chunk = (chunk + vec - 1) / vec * vec;
+  SplitPlan sp;
+  sp.chunk_elems = (int)chunk;
+  sp.splits = (int)((V + chunk - 1) / chunk);
+  return sp;
+}
+
+// ---------------------------------------------------------------------------
+// kernel parameter blocks
+// ---------------------------------------------------------------------------
+struct RowStatsParams {
+  const void *logits;
+  const float *temperature;
+  RowPartial *part;
+  long long items;  // B * R * P
+  int dtype;
+  int R, V, P, chunk_elems;
+};
+
+struct LinearFinalizeParams {
+  const void *logits;
+  const void *q;
+  const int32_t *tokens;
+  const float *temperature;
+  const float *uniforms;
+  const RowPartial *part;
+  int32_t *n_accepted;
+  int32_t *out_tokens;
+  int32_t *final_token;
+  uint8_t *is_bonus;
+  int32_t *row_status;
+  float *p_draft;
+  int dtype, B, gamma, V, P;
+};
+
+struct TreeFinalizeParams {
+  const void *logits;
+  const void *q;
+  const int32_t *tokens;
+  const int32_t *parent;
+  const float *temperature;
+  const float *uniforms;
+  const RowPartial *part;
+  int32_t *n_accepted;
+  int32_t *path_nodes;
+  int32_t *out_tokens;
+  int32_t *final_token;
+  uint8_t *is_bonus;
+  int32_t *row_status;
+  float *p_node;
+  int dtype, B, N, V, P, max_depth;
+};
+
+// host launchers (defined in the .cu files)
+cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream);
+cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream);
+cudaError_t launch_tree_finalize(const TreeFinalizeParams &p, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Temperature check shared by both phases (0 = greedy, else [1e-20, 1e20]).
+__device__ __forceinline__ bool temperature_valid(float T) {
+  return T == 0.0f || (T >= 1e-20f && T <= 1e20f);
+}
+
+// Exponent scale c such that exp(l / T) = 2^(l * c).  Greedy rows and invalid
+// temperatures use T = 1: their sums only serve the finiteness check.
+__device__ __forceinline__ float temperature_scale(float T) {
+  if (T > 0.0f && temperature_valid(T)) return (float)(1.4426950408889634 / (double)T);
+  return kLog2e;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float load_elem(const void *base, int dtype, long long idx) {
+  if (dtype == SPECDEC_F32) return __ldg(reinterpret_cast<const float *>(base) + idx);
+  const unsigned short h = __ldg(reinterpret_cast<const unsigned short *>(base) + idx);
+  return __uint_as_float(((uint32_t)h) << 16);
+}
+
+// Exact floor(w * 2^52) for a finite w >= 0 (truncation of smaller bits),
+// with integer operations only.
+__device__ __forceinline__ unsigned long long to_fixed52(float w) {
+  const uint32_t b = __float_as_uint(w);
+  const int e = (int)(b >> 23) & 0xFF;
+  if (e == 0 || (b >> 31)) return 0ull;
+  const unsigned long long m = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
+  const int s = e - 98;  // w * 2^52 = m * 2^(e - 127 - 23 + 52)
+  if (s >= 0) return m << s;
+  if (s <= -24) return 0ull;
+  return m >> (-s);
+}
+
+// floor(U * Z) for U in (0, 1) given as float32 and Z in 52-bit fixed point:
+// exact 88-bit product of U's significand with Z, then the exponent shift.
+__device__ __forceinline__ unsigned long long uniform_target(float U, unsigned long long Z) {
+  if (!(U > 0.0f)) return 0ull;
+  if (!(U < 1.0f)) return Z ? Z - 1 : 0ull;
+  const uint32_t ub = __float_as_uint(U);
+  const int e = (int)(ub >> 23) & 0xFF;
+  const unsigned long long mant = (ub & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+  const int sh = (e ? 150 - e : 149);  // U = mant * 2^-sh, sh >= 24
+  const unsigned long long lo = mant * Z;
+  const unsigned long long hi = __umul64hi(mant, Z);
+  if (sh >= 128) return 0ull;
+  if (sh >= 64) return hi >> (sh - 64);
+  return (lo >> sh) | (hi << (64 - sh));
+}
+
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
+__device__ __forceinline__ unsigned long long shfl_up_u64(unsigned long long v, int d) {
+  const uint32_t lo = __shfl_up_sync(0xffffffffu, (uint32_t)v, d);
+  const uint32_t hi = __shfl_up_sync(0xffffffffu, (uint32_t)(v >> 32), d);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
+// --- mbarrier / bulk-copy wrappers (PTX ISA 8.x, sm_90 and later) ----------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: gives up after ~2 s of wall time (returns false).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` of transaction count on
+// `bar`.  Source and destination 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst_smem, const void *src_gmem,
+                                              uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+#endif  // __CUDACC__
+
+}  // namespace specdec

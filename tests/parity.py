@@ -1,0 +1,130 @@
+"""GPU-vs-oracle comparison rules for the verify step.
+
+Tolerances (written here, used by every parity test):
+* target probabilities p_i(x~_i) / p_parent(t_n): absolute 2e-5 for float32
+  inputs, 2e-3 for bfloat16 inputs;
+* accepted counts, paths and every token: bit-exact, except in a request with
+  a boundary draw: an accept test the oracle ran with |u - min(1, p/q)| < 1e-6,
+  or a final draw whose U*Z lies within 1e-6*Z of a CDF boundary around the
+  oracle's token.  Such requests are counted and excluded from the exact
+  comparison; at most max(1, 1e-4 * draws) of them may occur.
+* request status bitmasks: exact.
+"""
+import numpy as np
+
+BOUNDARY = 1e-6
+P_TOL = {"f32": 2e-5, "bf16": 2e-3}
+
+
+def linear_draws(o, gamma):
+    k = o["n_accepted"].astype(np.int64)
+    tests = np.minimum(k + 1, gamma)
+    return int(tests.sum() + k.size)
+
+
+def compare_linear(w, g, o, max_boundary_frac=1e-4):
+    """g: GPU outputs as numpy dict; o: oracle outputs (with diagnostics)."""
+    B, gamma = w.B, w.gamma
+    rep = dict(B=B, boundary=0, mismatched_boundary=0, max_p_err=0.0)
+    assert np.array_equal(g["row_status"], o["row_status"]), \
+        (np.nonzero(g["row_status"] != o["row_status"]), g["row_status"], o["row_status"])
+    ok = o["row_status"] == 0
+    bad = ~ok
+    if bad.any():
+        assert (g["n_accepted"][bad] == 0).all() and (g["final_token"][bad] == -1).all()
+        assert (g["out_tokens"][bad] == -1).all() and (g["is_bonus"][bad] == 0).all()
+    if not ok.any():
+        return rep
+    if g.get("p_draft") is not None:
+        err = np.abs(g["p_draft"][ok].astype(np.float64) - o["p_draft"][ok])
+        rep["max_p_err"] = float(err.max())
+        assert rep["max_p_err"] <= P_TOL[w.dtype], rep
+    u = w.uniforms.astype(np.float64)
+    for b in np.nonzero(ok)[0]:
+        k = int(o["n_accepted"][b])
+        ran = range(min(k + 1, gamma))
+        greedy = w.temperature[b] == 0
+        near = (not greedy) and any(abs(u[b, i] - o["ratio"][b, i]) < BOUNDARY for i in ran)
+        near = near or ((not greedy) and o["final_margin"][b] < BOUNDARY)
+        same = (g["n_accepted"][b] == k and g["final_token"][b] == o["final_token"][b]
+                and g["is_bonus"][b] == o["is_bonus"][b]
+                and np.array_equal(g["out_tokens"][b], o["out_tokens"][b]))
+        if near:
+            rep["boundary"] += 1
+            rep["mismatched_boundary"] += int(not same)
+            continue
+        assert same, dict(b=int(b), gpu_k=int(g["n_accepted"][b]), ora_k=k,
+                          gpu_tok=int(g["final_token"][b]), ora_tok=int(o["final_token"][b]),
+                          ratio=o["ratio"][b], u=u[b], margin=o["final_margin"][b],
+                          gpu_out=g["out_tokens"][b], ora_out=o["out_tokens"][b])
+    draws = linear_draws(o, gamma)
+    assert rep["boundary"] <= max(1, max_boundary_frac * draws), rep
+    return rep
+
+
+def compare_tree(w, g, o, max_boundary_frac=1e-4):
+    B = w.B
+    rep = dict(B=B, boundary=0, mismatched_boundary=0, max_p_err=0.0)
+    assert np.array_equal(g["row_status"], o["row_status"]), (g["row_status"], o["row_status"])
+    ok = o["row_status"] == 0
+    bad = ~ok
+    if bad.any():
+        assert (g["n_accepted"][bad] == 0).all() and (g["final_token"][bad] == -1).all()
+        assert (g["out_tokens"][bad] == -1).all() and (g["path_nodes"][bad] == -1).all()
+    if not ok.any():
+        return rep
+    if g.get("p_node") is not None:
+        err = np.abs(g["p_node"][ok][:, 1:].astype(np.float64) - o["p_node"][ok][:, 1:])
+        rep["max_p_err"] = float(err.max()) if err.size else 0.0
+        assert rep["max_p_err"] <= P_TOL[w.dtype], rep
+    for b in np.nonzero(ok)[0]:
+        greedy = w.temperature[b] == 0
+        near = (not greedy) and (o["test_margin"][b] < BOUNDARY or o["final_margin"][b] < BOUNDARY)
+        same = all(np.array_equal(g[key][b], o[key][b]) for key in
+                   ("n_accepted", "path_nodes", "out_tokens", "final_token", "is_bonus"))
+        if near:
+            rep["boundary"] += 1
+            rep["mismatched_boundary"] += int(not same)
+            continue
+        assert same, dict(b=int(b), **{key: (g[key][b], o[key][b]) for key in
+                                       ("n_accepted", "path_nodes", "out_tokens",
+                                        "final_token", "is_bonus")},
+                          tm=o["test_margin"][b], fm=o["final_margin"][b])
+    draws = int(o["n_accepted"].sum() + 2 * B)
+    assert rep["boundary"] <= max(1, max_boundary_frac * draws), rep
+    return rep
+
+
+def gpu_linear(w, device="cuda", offset_elems=0):
+    """Run the CUDA path on a LinearWorkload; returns numpy outputs.  With
+    ``offset_elems`` the logits and q start that many elements past a
+    16-byte boundary (exercises the unaligned edges of the bulk copies)."""
+    import torch
+    from speculative_decoding_verification_64_gb300 import binding
+    logits, q, toks, temp, uni = binding.linear_inputs_to_device(w, device)
+    if offset_elems:
+        logits = _offset_copy(logits, offset_elems)
+        q = _offset_copy(q, offset_elems)
+    out = binding.verify_linear(logits, q, toks, temp, uni)
+    torch.cuda.synchronize()
+    return {k: (None if v is None else v.cpu().numpy()) for k, v in vars(out).items()}
+
+
+def gpu_tree(w, device="cuda", offset_elems=0):
+    import torch
+    from speculative_decoding_verification_64_gb300 import binding
+    logits, q, toks, par, temp, uni = binding.tree_inputs_to_device(w, device)
+    if offset_elems:
+        logits = _offset_copy(logits, offset_elems)
+        q = _offset_copy(q, offset_elems)
+    out = binding.verify_tree(logits, q, toks, par, temp, uni, w.max_depth)
+    torch.cuda.synchronize()
+    return {k: (None if v is None else v.cpu().numpy()) for k, v in vars(out).items()}
+
+
+def _offset_copy(t, off):
+    import torch
+    flat = torch.empty(t.numel() + off, dtype=t.dtype, device=t.device)
+    view = flat[off:].view(t.shape)
+    view.copy_(t)
+    return view

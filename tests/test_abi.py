@@ -1,0 +1,108 @@
+"""The C-ABI library loads and exports every symbol include/specdec.h declares.
+
+Runs without a GPU: only host-side entry points are called (version, status
+strings, workspace sizing, and argument checks that return before any CUDA
+call).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specdec.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_64_gb300 import build, binding
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(specdec_[a-z_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("specdec_verify_linear", "specdec_verify_tree", "specdec_workspace_size",
+                 "specdec_status_string", "specdec_row_stats", "specdec_linear_finalize",
+                 "specdec_tree_finalize", "specdec_abi_version"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.specdec_abi_version() == 1
+    for code in range(5):
+        s = lib.specdec_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.specdec_status_string(99).decode() == "unknown status"
+
+
+def test_workspace_size_is_a_pure_function(lib):
+    from speculative_decoding_verification_64_gb300.binding import BF16, F32
+    a = lib.specdec_workspace_size(256, 9, 128256, BF16)
+    assert a == lib.specdec_workspace_size(256, 9, 128256, BF16)
+    assert a > 0 and a % 256 == 0
+    assert a >= 256 * 9 * 16                      # at least one partial per row
+    assert lib.specdec_workspace_size(0, 9, 128256, BF16) == 0
+    assert lib.specdec_workspace_size(-1, 9, 128256, BF16) == 0
+    assert lib.specdec_workspace_size(4, 9, 0, BF16) == 0
+    assert lib.specdec_workspace_size(4, 9, 100, 7) == 0
+    assert lib.specdec_workspace_size(4, 9, (1 << 21) + 1, F32) == 0
+    assert lib.specdec_workspace_size(1, 5, 32000, F32) > 0
+
+
+def test_argument_checks_before_any_device_work(lib):
+    from speculative_decoding_verification_64_gb300.binding import BF16
+    N = None
+    vl = lib.specdec_verify_linear
+    # B = 0 is a no-op
+    assert vl(N, N, BF16, N, N, N, 0, 8, 1000, N, N, N, N, N, N, N, 0, N) == 0
+    # null pointers
+    assert vl(N, N, BF16, N, N, N, 4, 8, 1000, N, N, N, N, N, N, N, 0, N) == 1
+    # gamma out of range
+    assert vl(N, N, BF16, N, N, N, 4, 0, 1000, N, N, N, N, N, N, N, 0, N) == 1
+    assert vl(N, N, BF16, N, N, N, 4, 33, 1000, N, N, N, N, N, N, N, 0, N) == 2
+    # dtype
+    assert vl(N, N, 5, N, N, N, 4, 4, 1000, N, N, N, N, N, N, N, 0, N) == 1
+    # vocabulary limit
+    assert vl(N, N, BF16, N, N, N, 4, 4, (1 << 21) + 1, N, N, N, N, N, N, N, 0, N) == 2
+    # workspace too small (all other pointers are non-null dummies that are never touched)
+    d = ctypes.c_void_p(16)
+    assert vl(d, d, BF16, d, d, d, 4, 4, 1000, d, d, d, d, d, N, d, 8, N) == 3
+    assert vl(d, d, BF16, d, d, d, 4, 4, 1000, d, d, d, d, d, N, N, 1 << 20, N) == 3
+    vt = lib.specdec_verify_tree
+    assert vt(N, N, BF16, N, N, N, N, 0, 64, 1000, 5, N, N, N, N, N, N, N, N, 0, N) == 0
+    assert vt(N, N, BF16, N, N, N, N, 2, 0, 1000, 5, N, N, N, N, N, N, N, N, 0, N) == 1
+    assert vt(N, N, BF16, N, N, N, N, 2, 2000, 1000, 5, N, N, N, N, N, N, N, N, 0, N) == 2
+    assert vt(N, N, BF16, N, N, N, N, 2, 64, 1000, 65, N, N, N, N, N, N, N, N, 0, N) == 2
+    rs = lib.specdec_row_stats
+    assert rs(N, BF16, N, 0, 9, 1000, N, 0, N) == 0
+    assert rs(N, BF16, N, 2, 9, 1000, N, 0, N) == 1
+
+
+def test_binding_refuses_to_run_without_the_library(tmp_path):
+    from speculative_decoding_verification_64_gb300 import binding
+    with pytest.raises(binding.SpecdecError):
+        binding.load_library(str(tmp_path / "missing.so"))
+
+
+def test_oracle_is_not_reachable_from_the_product_package():
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_64_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "specdec_oracle" not in text, f
