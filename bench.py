@@ -56,6 +56,10 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B (a smaller case for profiling; not a bench line)")
+    ap.add_argument("--vocab", type=int, default=None,
+                    help="override V (a smaller case for profiling; not a bench line)")
     return ap.parse_args(argv)
 
 
@@ -242,7 +246,7 @@ def run_ours(args, dist):
     dist.barrier()
     binding.load_library()
 
-    w = W.make_workload(args.workload, seed_offset=1000 * dist.rank)
+    w = W.make_workload(args.workload, B=args.batch, V=args.vocab, seed_offset=1000 * dist.rank)
     linear = isinstance(w, W.LinearWorkload)
     R = w.rows
     es = w.elem_bytes
@@ -322,7 +326,7 @@ def run_ours(args, dist):
     P = _splits(lib, w.B, R, w.V, dt)
     k1_bytes = ab["logits"] + w.B * R * P * 16
     k1_gbs = k1_bytes / (k1_ms / 1e3) / 1e9
-    traffic = ncu_traffic(args.workload)
+    traffic = ncu_traffic(_workload_name(args))
     roofline = {"bound": "hbm", "kernel": "row_stats_kernel", "achieved": round(k1_gbs, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(k1_gbs / peak, 4),
                 "peak_kind": peak_kind, "traffic": traffic,
@@ -348,7 +352,7 @@ def run_ours(args, dist):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic",
-        "config": _config(w, args.workload, linear),
+        "config": _config(w, _workload_name(args), linear),
         "requests_per_s": round(dist.sum(w.B, device) * K / (total_ms / 1e3), 1),
         "accepted_tokens_per_s": round(dist.sum(float(out.n_accepted.sum().item() + w.B), device)
                                        * K / (total_ms / 1e3), 1),
@@ -372,6 +376,13 @@ def _splits(lib, B, R, V, dt):
     # the workspace holds one 16-byte partial per (row, split), rounded to 256 bytes
     ws = lib.specdec_workspace_size(B, R, V, dt)
     return max(1, (ws // 16) // (B * R))
+
+
+def _workload_name(args):
+    name = args.workload
+    if args.batch is not None or args.vocab is not None:
+        name += f" (override B={args.batch} V={args.vocab})"
+    return name
 
 
 def _config(w, name, linear):
@@ -477,7 +488,7 @@ def run_reference(args, dist):
         return
     import oracle
     oracle.build()
-    w = W.make_workload(args.workload)
+    w = W.make_workload(args.workload, B=args.batch, V=args.vocab)
     linear = isinstance(w, W.LinearWorkload)
     units_per_req = w.gamma if linear else w.N - 1
     cores = oracle.num_threads()
@@ -499,7 +510,7 @@ def run_reference(args, dist):
         "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(w, args.workload, linear), "impl": "reference",
+        "config": _config(w, _workload_name(args), linear), "impl": "reference",
         "cpu_baseline": {"value": round(value, 1), "unit": "positions/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": "positions/s", "h2d_bytes_per_step": 0,

@@ -75,8 +75,8 @@ extern "C" {
 #define SPECDEC_ROW_OK 0
 #define SPECDEC_ROW_BAD_TOKEN 1  /* a drafted token is outside [0, V) */
 #define SPECDEC_ROW_BAD_Q 2      /* q at a drafted token is <= 0, NaN or inf */
-#define SPECDEC_ROW_NONFINITE 4  /* a target row holds NaN or +inf, or only -inf */
-#define SPECDEC_ROW_BAD_TEMP 8   /* temperature not 0 and not in [1e-20, 1e20] */
+#define SPECDEC_ROW_NONFINITE 4  /* a target row holds NaN or +inf, no finite value, or a max > 2^100 */
+#define SPECDEC_ROW_BAD_TEMP 8   /* temperature not 0 and not in [2^-20, 2^20] */
 #define SPECDEC_ROW_BAD_TREE 16  /* parent[0] != -1, parent[n] not in [0, n), or depth > max_depth */
 #define SPECDEC_ROW_INTERNAL 32  /* a kernel's bounded wait for its own copy ran out */
 

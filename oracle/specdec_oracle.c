@@ -23,7 +23,8 @@
  * Readings taken where the pages are silent (each is listed in the design
  * notes of the repository):
  *   - temperature: p = softmax(l / T); T = 0 means greedy, i.e. the T -> 0
- *     limit: p is one-hot at the first maximal logit;
+ *     limit: p is one-hot at the first maximal logit; other valid T lie in
+ *     [2^-20, 2^20];
  *   - accept compare is "u <= min(1, p/q)" (the chapter's pseudo-code);
  *   - a draw from weights w with uniform U picks the smallest v whose
  *     running sum C_v = w_0 + ... + w_v exceeds U * Z, Z = sum w (strict);
@@ -67,19 +68,22 @@ static double load_elem(const void *base, int dtype, size_t idx) {
   return (double)f;
 }
 
+/* Valid temperatures: 0 (greedy) or 2^-20 <= T <= 2^20. */
 static int temperature_valid(float T) {
-  return T == 0.0f || (T >= 1e-20f && T <= 1e20f);
+  return T == 0.0f || (T >= 0x1p-20f && T <= 0x1p20f);
 }
 
-/* A target row is unusable when it holds a NaN or +Inf, or no finite value. */
+/* A target row is unusable when it holds a NaN or +Inf, when no value is
+ * finite, or when its largest logit exceeds 2^100 (so l / T stays far inside
+ * the float range for every valid temperature). */
 static int row_nonfinite(const void *base, int dtype, size_t off, int V) {
-  int any = 0;
+  double mx = -INFINITY;
   for (int v = 0; v < V; ++v) {
     double x = load_elem(base, dtype, off + (size_t)v);
     if (isnan(x) || x == INFINITY) return 1;
-    if (x != -INFINITY) any = 1;
+    if (x > mx) mx = x;
   }
-  return !any;
+  return mx == -INFINITY || mx > 0x1p100;
 }
 
 /* Target distribution of one row (section 15.1.2 step 2 with temperature):

@@ -16,15 +16,15 @@ bool dtype_ok(int dtype) { return dtype == SPECDEC_F32 || dtype == SPECDEC_BF16;
 
 size_t workspace_bytes_for(long long B, int R, int V, int dtype) {
   const long long rows = B * (long long)R;
-  const SplitPlan sp = make_split_plan(rows, V, elem_bytes(dtype));
-  const size_t bytes = (size_t)rows * (size_t)sp.splits * sizeof(RowPartial);
+  const size_t bytes = (size_t)rows * (size_t)stages_per_row(V, elem_bytes(dtype)) *
+                       sizeof(RowPartial);
   return (bytes + 255) / 256 * 256;
 }
 
 int check_sizes(int B, int R, int V, int dtype) {
   if (!dtype_ok(dtype) || B < 0 || R < 1 || V < 1) return SPECDEC_ERR_INVALID_ARG;
   if (V > SPECDEC_MAX_V) return SPECDEC_ERR_UNSUPPORTED;
-  if ((long long)B * 8 > INT_MAX) return SPECDEC_ERR_UNSUPPORTED;
+  if ((long long)B * 8 > INT_MAX || (long long)B * R > INT_MAX) return SPECDEC_ERR_UNSUPPORTED;
   return SPECDEC_OK;
 }
 
@@ -41,17 +41,16 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPECDEC_OK : SPECDEC_
 int launch_stats(const void *logits, int dtype, const float *temperature, int B, int R, int V,
                  void *workspace, cudaStream_t stream) {
   const long long rows = (long long)B * R;
-  const SplitPlan sp = make_split_plan(rows, V, elem_bytes(dtype));
+  const int spr = stages_per_row(V, elem_bytes(dtype));
   RowStatsParams p;
   p.logits = logits;
   p.temperature = temperature;
   p.part = reinterpret_cast<RowPartial *>(workspace);
-  p.items = rows * sp.splits;
+  p.stages = rows * spr;
   p.dtype = dtype;
   p.R = R;
   p.V = V;
-  p.P = sp.splits;
-  p.chunk_elems = sp.chunk_elems;
+  p.spr = spr;
   return cuda_status(launch_row_stats(p, stream));
 }
 
@@ -113,7 +112,6 @@ static int linear_finalize_launch(const void *logits, const void *q, int dtype,
                                   int32_t *n_accepted, int32_t *out_tokens,
                                   int32_t *final_token, uint8_t *is_bonus, int32_t *row_status,
                                   float *p_draft, void *workspace, cudaStream_t stream) {
-  const SplitPlan sp = make_split_plan((long long)B * (gamma + 1), V, elem_bytes(dtype));
   LinearFinalizeParams p;
   p.logits = logits;
   p.q = q;
@@ -131,7 +129,7 @@ static int linear_finalize_launch(const void *logits, const void *q, int dtype,
   p.B = B;
   p.gamma = gamma;
   p.V = V;
-  p.P = sp.splits;
+  p.spr = stages_per_row(V, elem_bytes(dtype));
   return cuda_status(launch_linear_finalize(p, stream));
 }
 
@@ -193,7 +191,6 @@ static int tree_finalize_launch(const void *logits, const void *q, int dtype,
                                 int32_t *out_tokens, int32_t *final_token, uint8_t *is_bonus,
                                 int32_t *row_status, float *p_node, void *workspace,
                                 cudaStream_t stream) {
-  const SplitPlan sp = make_split_plan((long long)B * N, V, elem_bytes(dtype));
   TreeFinalizeParams p;
   p.logits = logits;
   p.q = q;
@@ -213,7 +210,7 @@ static int tree_finalize_launch(const void *logits, const void *q, int dtype,
   p.B = B;
   p.N = N;
   p.V = V;
-  p.P = sp.splits;
+  p.spr = stages_per_row(V, elem_bytes(dtype));
   p.max_depth = max_depth;
   return cuda_status(launch_tree_finalize(p, stream));
 }

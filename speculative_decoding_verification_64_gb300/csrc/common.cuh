@@ -11,44 +11,26 @@
 namespace specdec {
 
 // ---------------------------------------------------------------------------
-// workspace layout: one partial per (row, split) written by the row-stats pass
+// workspace layout: one partial per (row, stage) written by the row-stats pass
 // ---------------------------------------------------------------------------
 struct RowPartial {
-  float m;      // max of the raw logits in the split (-inf if none is finite)
-  float s;      // sum over the split of 2^((l - m) * c), c = log2(e) / T
-  int32_t arg;  // start index of the first 16-byte group (or lone element) holding m
+  float m;        // max of the raw logits in the stage (NaN if one is NaN, -inf if none finite)
+  float s;        // sum over the stage of 2^((l - m) c), c = log2(e) / T
+  int32_t arg;    // first index holding m (greedy rows only; else INT_MAX)
   int32_t flags;  // SPECDEC_ROW_INTERNAL when a bounded wait ran out
 };
 static_assert(sizeof(RowPartial) == 16, "RowPartial is 16 bytes");
 
-// Split plan of a row-stats pass: a pure function of the sizes, so the
-// workspace size can be computed on the host without a device.
-struct SplitPlan {
-  int splits;       // P: splits per row
-  int chunk_elems;  // elements per split (a multiple of 16 bytes of elements)
-};
+// Every row is cut into stages of kStageBytes of its 16-byte aligned interior;
+// a pure function of the sizes, so the workspace size needs no device.
+#ifndef SPECDEC_STAGE_BYTES
+#define SPECDEC_STAGE_BYTES 8192
+#endif
+constexpr int kStageBytes = SPECDEC_STAGE_BYTES;
 
-inline SplitPlan make_split_plan(long long rows, int V, int elem_bytes) {
-  const long long kTargetItemBytes = 32 * 1024;  // one work item ~ two 16 KB stages
-  const long long kMinItemBytes = 2 * 1024;
-  const long long kTargetItems = 8 * 152;        // keep small batches spread over the SMs
-  const int kMaxSplits = 64;
-  const long long row_bytes = (long long)V * elem_bytes;
-  long long p = (row_bytes + kTargetItemBytes / 2) / kTargetItemBytes;
-  if (p < 1) p = 1;
-  long long p_items = (kTargetItems + rows - 1) / (rows > 0 ? rows : 1);
-  if (p < p_items) p = p_items;
-  long long p_cap = row_bytes / kMinItemBytes;
-  if (p_cap < 1) p_cap = 1;
-  if (p > p_cap) p = p_cap;
-  if (p > kMaxSplits) p = kMaxSplits;
-  const int vec = 16 / elem_bytes;
-  long long chunk = (V + p - 1) / p;
-  chunk = (chunk + vec - 1) / vec * vec;
-  SplitPlan sp;
-  sp.chunk_elems = (int)chunk;
-  sp.splits = (int)((V + chunk - 1) / chunk);
-  return sp;
+inline int stages_per_row(int V, int elem_bytes) {
+  const long long b = (long long)V * elem_bytes;
+  return (int)((b + kStageBytes - 1) / kStageBytes);
 }
 
 // ---------------------------------------------------------------------------
@@ -58,9 +40,9 @@ struct RowStatsParams {
   const void *logits;
   const float *temperature;
   RowPartial *part;
-  long long items;  // B * R * P
+  long long stages;  // rows * spr
   int dtype;
-  int R, V, P, chunk_elems;
+  int R, V, spr;     // rows per request, vocabulary, stages per row
 };
 
 struct LinearFinalizeParams {
@@ -76,7 +58,7 @@ struct LinearFinalizeParams {
   uint8_t *is_bonus;
   int32_t *row_status;
   float *p_draft;
-  int dtype, B, gamma, V, P;
+  int dtype, B, gamma, V, spr;
 };
 
 struct TreeFinalizeParams {
@@ -94,7 +76,7 @@ struct TreeFinalizeParams {
   uint8_t *is_bonus;
   int32_t *row_status;
   float *p_node;
-  int dtype, B, N, V, P, max_depth;
+  int dtype, B, N, V, spr, max_depth;
 };
 
 // host launchers (defined in the .cu files)
@@ -109,16 +91,33 @@ cudaError_t launch_tree_finalize(const TreeFinalizeParams &p, cudaStream_t strea
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Temperature check shared by both phases (0 = greedy, else [1e-20, 1e20]).
+// Temperature check shared by both phases (0 = greedy, else [2^-20, 2^20]).
 __device__ __forceinline__ bool temperature_valid(float T) {
-  return T == 0.0f || (T >= 1e-20f && T <= 1e20f);
+  return T == 0.0f || (T >= 0x1p-20f && T <= 0x1p20f);
 }
 
-// Exponent scale c such that exp(l / T) = 2^(l * c).  Greedy rows and invalid
+// Exponent scale c such that exp(l / T) = 2^(l * c), in float32 (one IEEE
+// division; the same value in every kernel).  Greedy rows and invalid
 // temperatures use T = 1: their sums only serve the finiteness check.
 __device__ __forceinline__ float temperature_scale(float T) {
-  if (T > 0.0f && temperature_valid(T)) return (float)(1.4426950408889634 / (double)T);
+  if (T > 0.0f && temperature_valid(T)) return __fdiv_rn(kLog2e, T);
   return kLog2e;
+}
+
+// The low part of log2(e)/T beyond temperature_scale(T), for the draws that
+// need the exponent argument to float precision (computed once per CTA).
+__device__ __forceinline__ float temperature_scale_lo(float T, float c_hi) {
+  if (!(T > 0.0f && temperature_valid(T))) return 0.0f;
+  return (float)(1.4426950408889634 / (double)T - (double)c_hi);
+}
+
+// Largest logit a usable row may hold: with T >= 2^-20, (l - M) c stays finite.
+constexpr float kMaxLogit = 0x1p100f;
+
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -136,20 +135,20 @@ __device__ __forceinline__ float load_elem(const void *base, int dtype, long lon
   return __uint_as_float(((uint32_t)h) << 16);
 }
 
-// Exact floor(w * 2^52) for a finite w >= 0 (truncation of smaller bits),
-// with integer operations only.
-__device__ __forceinline__ unsigned long long to_fixed52(float w) {
+// Exact floor(w * 2^40) for a finite w >= 0 (weights in units of the row
+// maximum, w <= 2^20).
+__device__ __forceinline__ unsigned long long to_fixed40(float w) {
   const uint32_t b = __float_as_uint(w);
   const int e = (int)(b >> 23) & 0xFF;
   if (e == 0 || (b >> 31)) return 0ull;
   const unsigned long long m = (unsigned long long)((b & 0x7FFFFFu) | 0x800000u);
-  const int s = e - 98;  // w * 2^52 = m * 2^(e - 127 - 23 + 52)
+  const int s = e - 110;  // w * 2^40 = m * 2^(e - 127 - 23 + 40)
   if (s >= 0) return m << s;
   if (s <= -24) return 0ull;
   return m >> (-s);
 }
 
-// floor(U * Z) for U in (0, 1) given as float32 and Z in 52-bit fixed point:
+// floor(U * Z) for U in (0, 1) given as float32 and an integer Z:
 // exact 88-bit product of U's significand with Z, then the exponent shift.
 __device__ __forceinline__ unsigned long long uniform_target(float U, unsigned long long Z) {
   if (!(U > 0.0f)) return 0ull;

@@ -1,6 +1,17 @@
-// Pieces shared by the linear and tree finalize kernels: merging the split
-// partials of a row, the exact first arg-max, and the cluster-wide
-// inverse-CDF draw over one vocabulary row.
+// Pieces shared by the linear and tree finalize kernels: merging the stage
+// partials of a row, and the cluster-wide inverse-CDF draw over one
+// vocabulary row.
+//
+// Draw weights are kept in units of the row maximum: with
+//     e_v = 2^((l_v - M) c),  c = log2(e) / T    (e_v <= 1, e = 1 at the maximum),
+// computed exactly as the stats pass computes its terms, the target row is
+// p = e / S with S the merged sum of the stats pass, and every weight the
+// method draws from is w_v = max(0, e_v - K q_v) for a scalar K >= 0
+// (K = 0: the target row itself; K = S: the residual max(0, p - q) times S;
+// tree walk: K = S c_j after j rejected siblings).  Each thread sums 16
+// contiguous weights in float32, and everything above that is summed in
+// 40-bit fixed point (exact, associative integer adds), so the search for the
+// crossing sees exactly the prefix sums that the totals were made of.
 #pragma once
 
 #include <cfloat>
@@ -18,161 +29,199 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPerThread = 16;        // contiguous elements per thread in a tile
 constexpr int kTile = kThreads * kPerThread;
+constexpr int kBatch = 4;             // tiles whose loads are in flight together
 constexpr int kMaxTilesPerCta = (SPECDEC_MAX_V + kTile * kG - 1) / (kTile * kG);
+constexpr double kFixedUnit = 0x1p-40;  // value of one unit of the fixed-point sums
 
 struct RowStat {
-  float M;    // row max of the raw logits
+  float M;    // row max of the raw logits (NaN if the row holds a NaN)
   float S;    // sum of 2^((l - M) c)
-  int arg;    // start of the 16-byte group holding the first maximum
+  int arg;    // first index holding M (greedy rows)
   int flags;
 };
 
-// Merge the P split partials of one row (same rule as inside the stats pass).
-__device__ __forceinline__ RowStat merge_row(const RowPartial *part, long long row, int P,
-                                             float c) {
-  const RowPartial *pr = part + row * (long long)P;
-  RowStat r;
-  r.M = -INFINITY;
-  r.S = 0.0f;
-  r.arg = 0x7FFFFFFF;
-  r.flags = 0;
-  for (int j = 0; j < P; ++j) {
-    const RowPartial x = pr[j];
-    r.flags |= x.flags;
-    const float M = fmaxf(r.M, x.m);
-    const float Mref = fmaxf(M, -FLT_MAX);
-    const float f1 = ex2_approx((fmaxf(r.M, -FLT_MAX) - Mref) * c);
-    const float f2 = ex2_approx((fmaxf(x.m, -FLT_MAX) - Mref) * c);
-    r.arg = (r.M > x.m) ? r.arg : (x.m > r.M) ? x.arg : min(r.arg, x.arg);
-    r.S = r.S * f1 + x.s * f2;
-    r.M = M;
+// Merge of two stage partials (each sum is taken relative to its own max).
+__device__ __forceinline__ void merge2(float &m, float &s, int &a, float m2, float s2, int a2,
+                                       float c) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    a = a2;
+    return;
   }
+  const float M = fmax_nan(m, m2);
+  const float f1 = ex2_approx((m - M) * c);
+  const float f2 = ex2_approx((m2 - M) * c);
+  a = (m > m2) ? a : (m2 > m) ? a2 : min(a, a2);
+  s = s * f1 + s2 * f2;
+  m = M;
+}
+
+// Warp-cooperative merge of one row's stage partials; every lane gets the result.
+__device__ __forceinline__ RowStat warp_merge_row(const RowPartial *part, long long row, int spr,
+                                                  float c, int lane) {
+  const RowPartial *pr = part + row * (long long)spr;
+  float m = -INFINITY, s = 0.0f;
+  int a = 0x7FFFFFFF, fl = 0;
+  for (int j = lane; j < spr; j += 32) {
+    const RowPartial x = pr[j];
+    fl |= x.flags;
+    merge2(m, s, a, x.m, x.s, x.arg, c);
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, d);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, d);
+    const int a2 = __shfl_xor_sync(0xffffffffu, a, d);
+    merge2(m, s, a, m2, s2, a2, c);
+  }
+  RowStat r;
+  r.M = m;
+  r.S = s;
+  r.arg = a;
+  r.flags = __reduce_or_sync(0xffffffffu, fl);
   return r;
 }
 
 __device__ __forceinline__ bool row_usable(const RowStat &r) {
-  return r.M > -INFINITY && r.M < INFINITY && r.S > 0.0f && r.S < INFINITY;
+  return r.M > -INFINITY && r.M <= kMaxLogit && r.S > 0.0f && r.S < INFINITY;
 }
 
-// First index holding the row maximum: it lies in the 16-byte group that
-// starts at r.arg (or is r.arg itself for an unaligned edge element).
-__device__ __forceinline__ int exact_argmax(const void *logits, int dtype, long long row_off,
-                                            int V, const RowStat &r) {
-  const int span = (dtype == SPECDEC_F32) ? 4 : 8;
-  const int a0 = max(0, min(r.arg, V - 1));
-  const int a1 = min(V, a0 + span);
-  for (int e = a0; e < a1; ++e)
-    if (load_elem(logits, dtype, row_off + e) == r.M) return e;
-  return a0;  // unreachable for a usable row
+// p(x) from the merged row statistics (accept tests and the p outputs).
+__device__ __forceinline__ float target_prob(float lx, const RowStat &r, float c) {
+  return exp2f((lx - r.M) * c) / r.S;
 }
 
-// Draw weights of one row, 16 contiguous elements starting at e:
-//   w_v = max(0, 2^((l_v - M) c) / S - cq * q_v)     (cq = 0: the target row itself)
-// Elements at or beyond V get weight 0.
-__device__ __forceinline__ void row_weights16(const void *lrow, const void *qrow, int dtype,
-                                              int V, int e, float M, float c, float invS,
-                                              float cq, bool vec_ok, float w[kPerThread]) {
-  float l[kPerThread], qv[kPerThread];
-  const bool full = vec_ok && (e + kPerThread <= V);
-  if (full && dtype == SPECDEC_BF16) {
-    const uint4 *lp = reinterpret_cast<const uint4 *>(
-        reinterpret_cast<const uint16_t *>(lrow) + e);
-    const uint4 a = __ldg(lp), bb = __ldg(lp + 1);
-    const uint32_t wd[8] = {a.x, a.y, a.z, a.w, bb.x, bb.y, bb.z, bb.w};
+struct DrawRow {
+  const uint8_t *lrow;  // logits row
+  const uint8_t *qrow;  // q row (read only when use_q)
+  int V;
+  float M, c;           // e_v = 2^((l - M) c)
+  float K;              // w_v = max(0, e_v - K q_v)
+  bool use_q;
+  bool vec_ok;          // rows 16-byte aligned: vector loads
+};
+
+__device__ __forceinline__ float elem_e(const DrawRow &r, float l) { return ex2_approx((l - r.M) * r.c); }
+
+__device__ __forceinline__ float elem_w(const DrawRow &r, float e, float q) {
+  return r.use_q ? fmaxf(fmaf(-r.K, q, e), 0.0f) : e;
+}
+
+// 16 contiguous elements of a tile as raw 16-byte vectors (bf16: 2 vectors per
+// row, float32: 4), so several tiles' loads can be in flight at once.
+template <int DT>
+struct Raw16 {
+  uint4 l[DT == SPECDEC_F32 ? 4 : 2];
+  uint4 q[DT == SPECDEC_F32 ? 4 : 2];
+};
+
+template <int DT>
+__device__ __forceinline__ void load_raw(const DrawRow &r, int e, Raw16<DT> &x) {
+  constexpr int n = (DT == SPECDEC_F32) ? 4 : 2;
+  constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
+  if (r.vec_ok && e + kPerThread <= r.V) {
+    const uint4 *lp = reinterpret_cast<const uint4 *>(r.lrow + (size_t)e * es);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      l[2 * k] = bf16_lo(wd[k]);
-      l[2 * k + 1] = bf16_hi(wd[k]);
-    }
-    if (cq != 0.0f) {
-      const uint4 *qp = reinterpret_cast<const uint4 *>(
-          reinterpret_cast<const uint16_t *>(qrow) + e);
-      const uint4 x = __ldg(qp), y = __ldg(qp + 1);
-      const uint32_t qd[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+    for (int k = 0; k < n; ++k) x.l[k] = lp[k];
+    if (r.use_q) {
+      const uint4 *qp = reinterpret_cast<const uint4 *>(r.qrow + (size_t)e * es);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        qv[2 * k] = bf16_lo(qd[k]);
-        qv[2 * k + 1] = bf16_hi(qd[k]);
-      }
-    }
-  } else if (full) {
-    const float4 *lp = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(lrow) + e);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 t = __ldg(lp + k);
-      l[4 * k] = t.x;
-      l[4 * k + 1] = t.y;
-      l[4 * k + 2] = t.z;
-      l[4 * k + 3] = t.w;
-    }
-    if (cq != 0.0f) {
-      const float4 *qp =
-          reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(qrow) + e);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 t = __ldg(qp + k);
-        qv[4 * k] = t.x;
-        qv[4 * k + 1] = t.y;
-        qv[4 * k + 2] = t.z;
-        qv[4 * k + 3] = t.w;
-      }
+      for (int k = 0; k < n; ++k) x.q[k] = qp[k];
     }
   } else {
+    // ragged or unaligned: element by element; beyond V the logit is -inf (weight 0)
+    uint32_t lw[4 * n], qw[4 * n];
 #pragma unroll
     for (int k = 0; k < kPerThread; ++k) {
       const int v = e + k;
-      l[k] = (v < V) ? load_elem(lrow, dtype, v) : -INFINITY;
-      qv[k] = (v < V && cq != 0.0f) ? load_elem(qrow, dtype, v) : 0.0f;
+      uint32_t lb, qb = 0;
+      if (DT == SPECDEC_F32) {
+        lb = (v < r.V) ? __float_as_uint(load_elem(r.lrow, DT, v)) : 0xFF800000u;
+        if (r.use_q && v < r.V) qb = __float_as_uint(load_elem(r.qrow, DT, v));
+        lw[k] = lb;
+        qw[k] = qb;
+      } else {
+        lb = (v < r.V) ? (__float_as_uint(load_elem(r.lrow, DT, v)) >> 16) : 0xFF80u;
+        if (r.use_q && v < r.V) qb = __float_as_uint(load_elem(r.qrow, DT, v)) >> 16;
+        if (k & 1) {
+          lw[k >> 1] |= lb << 16;
+          qw[k >> 1] |= qb << 16;
+        } else {
+          lw[k >> 1] = lb;
+          qw[k >> 1] = qb;
+        }
+      }
     }
-  }
 #pragma unroll
-  for (int k = 0; k < kPerThread; ++k) {
-    const float pv = ex2_approx((l[k] - M) * c) * invS;
-    const float x = (cq != 0.0f) ? pv - cq * qv[k] : pv;
-    w[k] = (e + k < V) ? fmaxf(x, 0.0f) : 0.0f;
+    for (int k = 0; k < n; ++k) {
+      x.l[k] = make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+      x.q[k] = make_uint4(qw[4 * k], qw[4 * k + 1], qw[4 * k + 2], qw[4 * k + 3]);
+    }
   }
 }
 
-// fp32 sum of the 16 weights in index order, then to 52-bit fixed point.
-__device__ __forceinline__ unsigned long long fixed_sum16(const float w[kPerThread]) {
+template <int DT>
+__device__ __forceinline__ float raw_elem(const uint4 *v, int k) {
+  if (DT == SPECDEC_F32) {
+    const uint4 t = v[k >> 2];
+    const uint32_t w = (k & 3) == 0 ? t.x : (k & 3) == 1 ? t.y : (k & 3) == 2 ? t.z : t.w;
+    return __uint_as_float(w);
+  }
+  const uint4 t = v[k >> 3];
+  const int j = (k >> 1) & 3;
+  const uint32_t w = j == 0 ? t.x : j == 1 ? t.y : j == 2 ? t.z : t.w;
+  return (k & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+
+// Weights of 16 elements and their float32 sum in index order, as fixed point.
+template <int DT>
+__device__ __forceinline__ unsigned long long weights16(const DrawRow &r, const Raw16<DT> &x, int e,
+                                                        float w[kPerThread]) {
   float s = 0.0f;
 #pragma unroll
-  for (int k = 0; k < kPerThread; ++k) s += w[k];
-  return to_fixed52(s);
+  for (int k = 0; k < kPerThread; ++k) {
+    const float q = r.use_q ? raw_elem<DT>(x.q, k) : 0.0f;
+    w[k] = (e + k < r.V) ? elem_w(r, elem_e(r, raw_elem<DT>(x.l, k)), q) : 0.0f;
+    s += w[k];
+  }
+  return to_fixed40(s);
 }
 
 struct DrawSmem {
   unsigned long long warp_tile[kMaxTilesPerCta][kWarps];
   unsigned long long tile_tot[kMaxTilesPerCta];
-  unsigned long long cta_total;     // this pass's CTA total
+  unsigned long long cta_total;        // this pass's CTA total
   unsigned long long shared_total[2];  // read by the other CTAs; double-buffered by pass
   unsigned long long prefix, Z, base;
+  float Zf;  // Z as a float, in units of the row maximum
   unsigned long long scan_warp[kWarps];
   int tile;
   int found;
 };
 
-struct DrawRow {
-  const void *lrow;
-  const void *qrow;  // may be null when cq == 0
-  int dtype, V;
-  float M, c, invS, cq;
-  bool vec_ok;
-};
-
-// Pass over this CTA's tiles of the row: per-tile fixed-point totals in smem
-// and the CTA total (published in slot `pass & 1` for the other CTAs).
+// One pass over this CTA's tiles [t0, t1) of the row: per-tile fixed-point
+// totals in smem and the CTA total, published in slot `pass & 1`.
+template <int DT>
 __device__ __forceinline__ void draw_sums(DrawSmem &ds, const DrawRow &r, int t0, int t1,
                                           int pass) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int t = t0; t < t1; ++t) {
-    float w[kPerThread];
-    row_weights16(r.lrow, r.qrow, r.dtype, r.V, t * kTile + tid * kPerThread, r.M, r.c, r.invS,
-                  r.cq, r.vec_ok, w);
-    unsigned long long f = fixed_sum16(w);
+  for (int tb = t0; tb < t1; tb += kBatch) {
+    Raw16<DT> x[kBatch];
 #pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) f += shfl_xor_u64(f, d);
-    if (lane == 0) ds.warp_tile[t - t0][warp] = f;
+    for (int u = 0; u < kBatch; ++u)
+      if (tb + u < t1) load_raw<DT>(r, (tb + u) * kTile + tid * kPerThread, x[u]);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (tb + u < t1) {
+        float w[kPerThread];
+        unsigned long long f = weights16<DT>(r, x[u], (tb + u) * kTile + tid * kPerThread, w);
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) f += shfl_xor_u64(f, d);
+        if (lane == 0) ds.warp_tile[tb + u - t0][warp] = f;
+      }
+    }
   }
   __syncthreads();
   for (int i = tid; i < t1 - t0; i += kThreads) {
@@ -207,12 +256,15 @@ __device__ __forceinline__ void draw_exchange(DrawSmem &ds, cg::cluster_group &c
     }
     ds.prefix = pre;
     ds.Z = tot;
+    ds.Zf = __ull2float_rn(tot) * (float)kFixedUnit;
   }
   __syncthreads();
 }
 
 // If the crossing of `target` lies in this CTA, find the smallest v with
-// C_v > target and return it (in thread 0 of the CTA: -1 otherwise).
+// C_v > target (C: prefix sums of the last pass's weights).  Returns v in
+// every thread of that CTA, -1 elsewhere.
+template <int DT>
 __device__ __forceinline__ int draw_search(DrawSmem &ds, const DrawRow &r, int t0, int t1,
                                            unsigned long long target) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -235,10 +287,10 @@ __device__ __forceinline__ int draw_search(DrawSmem &ds, const DrawRow &r, int t
   }
   __syncthreads();
   const int e = ds.tile * kTile + tid * kPerThread;
+  Raw16<DT> x;
   float w[kPerThread];
-  row_weights16(r.lrow, r.qrow, r.dtype, r.V, e, r.M, r.c, r.invS, r.cq, r.vec_ok, w);
-  const unsigned long long f = fixed_sum16(w);
-  // block exclusive scan of f
+  load_raw<DT>(r, e, x);
+  const unsigned long long f = weights16<DT>(r, x, e, w);
   unsigned long long inc = f;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -256,7 +308,7 @@ __device__ __forceinline__ int draw_search(DrawSmem &ds, const DrawRow &r, int t
 #pragma unroll
     for (int k = 0; k < kPerThread; ++k) {
       run += w[k];
-      if (excl + to_fixed52(run) > target) {
+      if (excl + to_fixed40(run) > target) {
         v = e + k;
         break;
       }
@@ -265,6 +317,14 @@ __device__ __forceinline__ int draw_search(DrawSmem &ds, const DrawRow &r, int t
   }
   __syncthreads();
   return ds.found;
+}
+
+// Tiles of the row owned by cluster rank `rank`.
+__device__ __forceinline__ void cta_tiles(int V, int rank, int &t0, int &t1) {
+  const int nt = (V + kTile - 1) / kTile;
+  const int tpc = (nt + kG - 1) / kG;
+  t0 = min(nt, rank * tpc);
+  t1 = min(nt, t0 + tpc);
 }
 
 }  // namespace fin

@@ -11,16 +11,19 @@
 //
 // The kernel never stores a residual row.  By induction, after j rejections
 //     P_j = max(0, p - c_j q) / N_j,  c_0 = 0, N_0 = 1,
-//     c_{j+1} = c_j + N_j,  N_{j+1} = sum_v max(0, p_v - c_{j+1} q_v),
-// so each rejection costs one reduction over the (L2-resident) logits and q
-// rows of the current node, and the test of the next sibling needs only its
-// gathered p(t) and q(t).
+//     c_{j+1} = c_j + N_j,  N_{j+1} = sum_v max(0, p_v - c_{j+1} q_v).
+// In units of the row maximum (e_v = 2^((l_v - M) c), p = e / S) this reads
+//     P_j = max(0, e - K_j q) / E_j,  K_0 = 0, E_0 = S,  K_{j+1} = K_j + E_j,
+//     E_{j+1} = sum_v max(0, e_v - K_{j+1} q_v),
+// so a rejection costs one reduction over the current node's logits and q
+// rows (L2-resident after the first), and the next sibling's test needs only
+// its gathered logit and q value.
 //
 // One 8-CTA cluster per request.  Every CTA validates the tree, merges the
-// row statistics and gathers p_parent(t_n), q_parent(t_n) for all nodes; the
-// walk itself is replicated in every CTA (the decisions depend only on those
-// shared values and on exact fixed-point cluster sums, so all CTAs agree);
-// reductions over the vocabulary are split across the cluster.
+// row statistics and gathers l_parent(t_n), q_parent(t_n) for all nodes; the
+// walk is replicated in every CTA (the decisions depend only on those values
+// and on exact fixed-point cluster sums, so all CTAs agree); reductions over
+// the vocabulary are split across the cluster.
 #include "finalize_common.cuh"
 
 namespace specdec {
@@ -36,11 +39,12 @@ struct TreeSmem {
   int anc[kMaxN];
   int dep[kMaxN];
   int kids[kMaxN];
+  float lg[kMaxN];    // l_parent(t_n)
   float pg[kMaxN];    // p_parent(t_n) before renormalisation (greedy: 1 / 0)
   float qg[kMaxN];    // q_parent(t_n)
   float rowM[kMaxN];
   float rowS[kMaxN];
-  int rowA[kMaxN];    // exact arg-max (greedy requests)
+  int rowA[kMaxN];    // first arg-max (greedy requests)
   int path[SPECDEC_MAX_TREE_DEPTH + 1];
   int status, nkids;
 };
@@ -51,15 +55,17 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
-__global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads)
+template <int DT>
+__global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
     tree_finalize_kernel(const TreeFinalizeParams p) {
   __shared__ TreeSmem sm;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  const long long b = blockIdx.x / kG;
+  const long long b = (long long)p.B - 1 - blockIdx.x / kG;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int N = p.N, V = p.V, D1 = p.max_depth + 1;
   const long long nodebase = b * (long long)N;
+  constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
 
   const float T = __ldg(p.temperature + b);
   const bool greedy = (T == 0.0f);
@@ -67,7 +73,7 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads)
   if (tid == 0) sm.status = temperature_valid(T) ? 0 : SPECDEC_ROW_BAD_TEMP;
   __syncthreads();
 
-  // ---- structure, tokens, row statistics ---------------------------------
+  // ---- structure, row statistics ---------------------------------------------
   int st = 0;
   for (int n = tid; n < N; n += kThreads) {
     const int a = __ldg(p.parent + nodebase + n);
@@ -75,13 +81,16 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads)
     if (n == 0 ? (a != -1) : (a < 0 || a >= n)) st |= SPECDEC_ROW_BAD_TREE;
     sm.anc[n] = (n == 0) ? -1 : a;
     sm.dep[n] = (n == 0) ? 0 : 1;
-    const RowStat r = merge_row(p.part, nodebase + n, p.P, c);
-    st |= r.flags;
-    const bool ok = row_usable(r);
-    if (!ok) st |= SPECDEC_ROW_NONFINITE;
-    sm.rowM[n] = r.M;
-    sm.rowS[n] = r.S;
-    sm.rowA[n] = (greedy && ok) ? exact_argmax(p.logits, p.dtype, (nodebase + n) * V, V, r) : 0;
+  }
+  for (int n = warp; n < N; n += kWarps) {
+    const RowStat r = warp_merge_row(p.part, nodebase + n, p.spr, c, lane);
+    if (lane == 0) {
+      sm.rowM[n] = r.M;
+      sm.rowS[n] = r.S;
+      sm.rowA[n] = r.arg;
+      if (r.flags) st |= r.flags;
+      if (!row_usable(r)) st |= SPECDEC_ROW_NONFINITE;
+    }
   }
   if (st) atomicOr(&sm.status, st);
   __syncthreads();
@@ -111,32 +120,35 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads)
       __syncthreads();
     }
   }
+
+  // ---- tokens and gathers ----------------------------------------------------
   st = 0;
   for (int n = tid; n < N; n += kThreads) {
     if (tree_ok && sm.dep[n] > p.max_depth) st |= SPECDEC_ROW_BAD_TREE;
-    if (n == 0) {
-      sm.pg[0] = 0.0f;
-      sm.qg[0] = 1.0f;
-      continue;
-    }
-    const int t = __ldg(p.tokens + nodebase + n);
-    const int a = sm.par[n];
+    sm.lg[n] = 0.0f;
     sm.pg[n] = 0.0f;
     sm.qg[n] = 1.0f;
+    if (n == 0) continue;
+    const int t = __ldg(p.tokens + nodebase + n);
+    const int a = sm.par[n];
     if (t < 0 || t >= V) {
       st |= SPECDEC_ROW_BAD_TOKEN;
       continue;
     }
     if (a < 0 || a >= n) continue;
     const long long prow = nodebase + a;
-    const float qt = load_elem(p.q, p.dtype, prow * V + t);
+    const float qt = load_elem(p.q, DT, prow * V + t);
+    const float lt = load_elem(p.logits, DT, prow * V + t);
     if (!(qt > 0.0f) || qt == INFINITY) st |= SPECDEC_ROW_BAD_Q;
     sm.qg[n] = qt;
+    sm.lg[n] = lt;
     if (greedy) {
       sm.pg[n] = (t == sm.rowA[a]) ? 1.0f : 0.0f;
     } else {
-      const float lt = load_elem(p.logits, p.dtype, prow * V + t);
-      sm.pg[n] = exp2f((lt - sm.rowM[a]) * c) / sm.rowS[a];
+      RowStat r;
+      r.M = sm.rowM[a];
+      r.S = sm.rowS[a];
+      sm.pg[n] = target_prob(lt, r, c);
     }
   }
   if (st) atomicOr(&sm.status, st);
@@ -164,23 +176,23 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads)
     for (int n = tid; n < N; n += kThreads) p.p_node[nodebase + n] = sm.pg[n];
 
   // ---- the walk ------------------------------------------------------------
-  const int es = (p.dtype == SPECDEC_F32) ? 4 : 2;
-  const int nt = (V + kTile - 1) / kTile;
-  const int tpc = (nt + kG - 1) / kG;
-  const int t0 = min(nt, rank * tpc), t1 = min(nt, t0 + tpc);
+  // State of the current node in units of its row maximum: P_j = max(0, e - K q) / E,
+  // starting from (K, E) = (0, S) with S the merged sum of the stats pass.
+  int t0, t1;
+  cta_tiles(V, rank, t0, t1);
   int cur = 0, nacc = 0, pass = 0;
-  float cj = 0.0f;       // c_j of the current node
-  double Nj = 1.0;       // N_j of the current node
-  bool sums_match = false;  // the draw sums in smem are those of (cur, cj)
+  float K = 0.0f, E = 0.0f;
+  bool rejected_any = false;  // the node has a rejected child (state (K, E) in use)
+  bool sums_match = false;    // the draw sums in smem are those of (cur, K)
   bool bonus = false;
   if (tid == 0) sm.path[0] = 0;
   DrawRow r;
-  r.dtype = p.dtype;
   r.V = V;
   r.c = c;
+  r.use_q = false;
+  r.K = 0.0f;
   for (;;) {
     __syncthreads();  // every thread is done with the previous node's child list
-    // children of cur, ascending
     if (warp == 0) {
       int cnt = 0;
       for (int base = cur + 1; base < N; base += 32) {
@@ -194,47 +206,51 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads)
     }
     __syncthreads();
     const int nk = sm.nkids;
-    cj = 0.0f;
-    Nj = 1.0;
+    K = 0.0f;
+    E = sm.rowS[cur];
+    rejected_any = false;
     sums_match = false;
+    r.lrow = reinterpret_cast<const uint8_t *>(p.logits) + (size_t)(nodebase + cur) * V * es;
+    r.qrow = reinterpret_cast<const uint8_t *>(p.q) + (size_t)(nodebase + cur) * V * es;
+    r.M = sm.rowM[cur];
+    r.vec_ok = ((reinterpret_cast<uintptr_t>(r.lrow) & 15) == 0) &&
+               ((reinterpret_cast<uintptr_t>(r.qrow) & 15) == 0);
     if (nk == 0) {
       bonus = true;
       break;
     }
-    r.lrow = reinterpret_cast<const uint8_t *>(p.logits) + (size_t)(nodebase + cur) * V * es;
-    r.qrow = reinterpret_cast<const uint8_t *>(p.q) + (size_t)(nodebase + cur) * V * es;
-    r.M = sm.rowM[cur];
-    r.invS = 1.0f / sm.rowS[cur];
-    r.vec_ok = ((reinterpret_cast<uintptr_t>(r.lrow) & 15) == 0) &&
-               ((reinterpret_cast<uintptr_t>(r.qrow) & 15) == 0);
     int accepted = -1;
     for (int i = 0; i < nk; ++i) {
       const int child = sm.kids[i];
-      const double pt = sm.pg[child], qt = sm.qg[child];
+      const float qt = sm.qg[child];
+      const float u = __ldg(p.uniforms + nodebase + child);
       bool acc;
       if (greedy) {
-        acc = (pt == 1.0);
+        acc = (sm.pg[child] == 1.0f);
+      } else if (!rejected_any) {
+        // first sibling: the plain test u <= min(1, p(t) / q(t)), i.e. u q <= p
+        acc = (u * qt <= sm.pg[child]);
       } else {
-        // u <= min(1, P_j(t) / q(t)),  P_j(t) = max(0, p(t) - c_j q(t)) / N_j
-        const double u = __ldg(p.uniforms + nodebase + child);
-        const double num = fmax(pt - (double)cj * qt, 0.0);
-        acc = (u * qt * Nj <= num);
+        // u <= min(1, P_j(t) / q(t)),  P_j(t) = max(0, e(t) - K q(t)) / E
+        const float et = elem_e(r, sm.lg[child]);
+        acc = (u * qt * E <= fmaxf(fmaf(-K, qt, et), 0.0f));
       }
       if (acc) {
         accepted = child;
         break;
       }
       if (greedy) continue;
-      // rejected: N_{j+1} = sum max(0, p - c_{j+1} q) over the vocabulary
-      const float cn = (float)((double)cj + Nj);
-      r.cq = cn;
-      draw_sums(sm.ds, r, t0, t1, pass);
+      rejected_any = true;
+      // rejected: K' = K + E, E' = sum max(0, e - K' q)
+      const float Kn = K + E;
+      r.K = Kn;
+      r.use_q = true;
+      draw_sums<DT>(sm.ds, r, t0, t1, pass);
       draw_exchange(sm.ds, cluster, pass);
       ++pass;
-      const unsigned long long Zn = sm.ds.Z;
-      if (Zn > 0) {
-        cj = cn;
-        Nj = (double)Zn * 0x1p-52;
+      if (sm.ds.Z > 0) {
+        K = Kn;
+        E = sm.ds.Zf;
         sums_match = true;
       } else {
         sums_match = false;  // keep P (rounding-only case)
@@ -251,22 +267,16 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads)
   if (greedy) {
     fin_tok = sm.rowA[cur];
   } else {
-    if (bonus) {
-      r.lrow = reinterpret_cast<const uint8_t *>(p.logits) + (size_t)(nodebase + cur) * V * es;
-      r.qrow = nullptr;
-      r.M = sm.rowM[cur];
-      r.invS = 1.0f / sm.rowS[cur];
-      r.vec_ok = (reinterpret_cast<uintptr_t>(r.lrow) & 15) == 0;
-    }
-    r.cq = bonus ? 0.0f : cj;
-    if (!sums_match) {
-      draw_sums(sm.ds, r, t0, t1, pass);
+    r.use_q = !bonus && K > 0.0f;
+    r.K = K;
+    if (!(sums_match && r.use_q)) {
+      draw_sums<DT>(sm.ds, r, t0, t1, pass);
       draw_exchange(sm.ds, cluster, pass);
       ++pass;
     }
     const float U = __ldg(p.uniforms + nodebase);
     const unsigned long long target = uniform_target(U, sm.ds.Z);
-    const int v = draw_search(sm.ds, r, t0, t1, target);
+    const int v = draw_search<DT>(sm.ds, r, t0, t1, target);
     if (tid == 0 && v >= 0) {
       p.final_token[b] = v;
       p.out_tokens[b * D1 + nacc] = v;
@@ -296,7 +306,10 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads)
 
 cudaError_t launch_tree_finalize(const TreeFinalizeParams &p, cudaStream_t stream) {
   if (p.B <= 0) return cudaSuccess;
-  tree_finalize_kernel<<<(unsigned)(p.B * kG), kThreads, 0, stream>>>(p);
+  if (p.dtype == SPECDEC_F32)
+    tree_finalize_kernel<SPECDEC_F32><<<(unsigned)(p.B * kG), kThreads, 0, stream>>>(p);
+  else
+    tree_finalize_kernel<SPECDEC_BF16><<<(unsigned)(p.B * kG), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -1,20 +1,28 @@
 // Row statistics of the target logits: the "parallel verification" step of
 // speculative sampling ("Chapter 15: Decoding acceleration", section 15.1.2,
-// step 2), which scores every drafted position in one pass.  For each row and
-// each split of the vocabulary the kernel produces
-//     m = max_v l_v,   s = sum_v 2^((l_v - m) c),   c = log2(e) / T,
-// and the position of the first maximum, so that p(x) = 2^((l_x - M) c) / S
-// after a merge over splits.  This pass reads every logit exactly once and is
-// the HBM-bound part of the verify step.
+// step 2), which scores every drafted position in one pass.  Every row is cut
+// into 8 KB stages of its 16-byte aligned interior; for each stage the kernel
+// produces
+//     m = max_v l_v,   s = sum_v 2^((l_v - m) c),   c = log2(e)/T,
+// and, for greedy rows (T = 0), the first index holding m.  A merge over the
+// stages of a row gives p(x) = 2^((l_x - M) c) / S.  This pass
+// reads every logit exactly once and carries almost all of the verify step's
+// HBM traffic.
 //
-// Structure (GB300): a persistent grid of 2 CTAs per SM walks the (row, split)
-// work items round robin.  In each CTA one producer thread streams the 16-byte
-// aligned interior of each split into a ring of 6 x 16 KB shared-memory
-// stages with 1-D bulk TMA copies (cp.async.bulk) that complete on "full"
-// mbarriers; 8 consumer warps read the stages with 128-bit shared loads,
-// update an online (max, sum) per thread and release each stage on an "empty"
-// mbarrier.  The few unaligned elements at the ends of a split are read with
-// plain loads.  Every wait is bounded in time.
+// Structure (GB300): a persistent grid of one CTA per SM; stage g goes to CTA
+// g mod grid, so at any moment the CTAs sweep neighbouring stages and a
+// request's rows are read close together in time.  In each CTA one producer
+// thread streams its stages into a ring of 24 x 8 KB shared-memory slots
+// with 1-D bulk TMA copies (cp.async.bulk) that complete on per-slot "full"
+// mbarriers.  Eight consumer warps each own every eighth slot: a warp reads a
+// whole stage with 128-bit shared loads (16 vectors per lane), takes the
+// stage max with NaN-propagating packed bf16 max, then forms the exponent
+// arguments (l - m) c with packed fp32x2 add and multiply (l - m is exact for
+// bf16 inputs), one ex2 per element and packed adds,
+// reduces over the warp with shuffles and releases the slot on its "empty"
+// mbarrier.  Consumer warps never wait on each other.  The unaligned edge
+// elements of a row (< 16 bytes at each end) are read with plain loads by the
+// warp of the row's first stage.  Every wait is bounded in time.
 #include <cfloat>
 
 #include "common.cuh"
@@ -22,185 +30,245 @@
 namespace specdec {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
-constexpr int kStageBytes = 16384;
-constexpr int kStages = 6;
-constexpr int kVecPerThread = kStageBytes / 16 / kConsumers;  // 4
-static_assert(kVecPerThread * kConsumers * 16 == kStageBytes, "stage split");
+#ifndef SPECDEC_K1_WARPS
+#define SPECDEC_K1_WARPS 8
+#endif
+#ifndef SPECDEC_K1_SLOTS
+#define SPECDEC_K1_SLOTS 24
+#endif
+#ifndef SPECDEC_K1_UNIT
+#define SPECDEC_K1_UNIT 1
+#endif
+constexpr int kConsumerWarps = SPECDEC_K1_WARPS;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kSlots = SPECDEC_K1_SLOTS;             // a multiple of the consumer warps
+constexpr int kUnit = SPECDEC_K1_UNIT;               // stages moved by one bulk copy
+constexpr int kUnitBytes = kUnit * kStageBytes;
+constexpr int kVecPerLane = kStageBytes / 16 / 32;   // 16-byte vectors per lane per stage
+static_assert(kSlots % kConsumerWarps == 0, "slot i belongs to warp i % kConsumerWarps");
+static_assert(kVecPerLane * 32 * 16 == kStageBytes, "a stage is a whole number of warp loads");
 
 struct StatsSmem {
-  alignas(128) uint8_t stage[kStages][kStageBytes];
-  alignas(8) uint64_t full[kStages];
-  alignas(8) uint64_t empty[kStages];
-  float red_m[2][kConsumerWarps];
-  float red_s[2][kConsumerWarps];
-  int red_a[2][kConsumerWarps];
+  alignas(128) uint8_t stage[kSlots][kUnitBytes];
+  alignas(8) uint64_t full[kSlots];
+  alignas(8) uint64_t empty[kSlots];
   volatile int abort_flag;
 };
 
-struct ItemGeom {
-  long long row;
-  int e0, e1;            // element range of the split
-  int head_end;          // elements [e0, head_end) read with plain loads
-  int tail_begin;        // elements [tail_begin, e1) read with plain loads
-  const uint8_t *i0;     // 16-byte aligned interior [i0, i1) moved by TMA
-  long long ibytes;
+struct UnitGeom {
+  int row;
+  int j0;               // first stage of the unit within the row
+  int nst;              // stages in the unit (<= kUnit)
+  const uint8_t *src;   // 16-byte aligned start of the unit's bytes
+  int bytes;            // 0 .. kUnitBytes, a multiple of 16
+  int elem0;            // row index of the unit's first element
+  int head_end;         // row elements [0, head_end) and [tail_begin, V)
+  int tail_begin;       // are read with plain loads by stage 0's warp
 };
 
-__device__ __forceinline__ ItemGeom item_geometry(const RowStatsParams &p, long long item,
-                                                  int es) {
-  ItemGeom g;
-  g.row = item / p.P;
-  const int split = (int)(item - g.row * p.P);
-  g.e0 = split * p.chunk_elems;
-  g.e1 = min(p.V, g.e0 + p.chunk_elems);
-  const uint8_t *row_base =
-      reinterpret_cast<const uint8_t *>(p.logits) + (size_t)g.row * (size_t)p.V * es;
-  const uintptr_t a0 = reinterpret_cast<uintptr_t>(row_base) + (uintptr_t)g.e0 * es;
-  const uintptr_t a1 = reinterpret_cast<uintptr_t>(row_base) + (uintptr_t)g.e1 * es;
-  const uintptr_t i0 = (a0 + 15) & ~(uintptr_t)15;
-  const uintptr_t i1 = a1 & ~(uintptr_t)15;
-  if (i1 > i0) {
-    g.i0 = reinterpret_cast<const uint8_t *>(i0);
-    g.ibytes = (long long)(i1 - i0);
-    g.head_end = g.e0 + (int)((i0 - a0) / es);
-    g.tail_begin = g.e0 + (int)((i1 - a0) / es);
-  } else {
-    g.i0 = nullptr;
-    g.ibytes = 0;
-    g.head_end = g.e1;
-    g.tail_begin = g.e1;
+// (row, unit) of a unit index, advanced by a fixed step without divisions.
+struct UnitCursor {
+  int row;  // B * R < 2^31 (checked by the host)
+  int ju;
+  int drow;
+  int dj;
+  __device__ __forceinline__ void init(long long g, long long step, int upr) {
+    row = (int)(g / upr);
+    ju = (int)(g - (long long)row * upr);
+    drow = (int)(step / upr);
+    dj = (int)(step - (long long)drow * upr);
   }
-  return g;
-}
-
-// ---- per-thread online statistics ----------------------------------------
-
-struct Stat {
-  float m;     // running max (never NaN)
-  float mref;  // max(m, -FLT_MAX): exponent reference that keeps -inf - -inf out
-  float s;
-  int arg;
+  __device__ __forceinline__ void advance(int upr) {
+    row += drow;
+    ju += dj;
+    if (ju >= upr) {
+      ju -= upr;
+      ++row;
+    }
+  }
 };
 
-__device__ __forceinline__ void stat_raise(Stat &st, float vmax, float c, int arg) {
-  // rescale the running sum to the new maximum
-  st.s = st.s * ex2_approx((st.mref - vmax) * c);
-  st.m = vmax;
-  st.mref = fmaxf(vmax, -FLT_MAX);
-  st.arg = arg;
+__device__ __forceinline__ UnitGeom unit_geometry(const RowStatsParams &p, int row, int ju, int es) {
+  UnitGeom s;
+  s.row = row;
+  s.j0 = ju * kUnit;
+  s.nst = min(kUnit, p.spr - s.j0);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p.logits) + (uintptr_t)row * p.V * es;
+  const uintptr_t e = a + (uintptr_t)p.V * es;
+  const uintptr_t i0 = (a + 15) & ~(uintptr_t)15;
+  uintptr_t i1 = e & ~(uintptr_t)15;
+  if (i1 < i0) i1 = i0;
+  const uintptr_t s0 = i0 + (uintptr_t)s.j0 * kStageBytes;
+  const uintptr_t s1 = (s0 + kUnitBytes < i1) ? s0 + kUnitBytes : i1;
+  s.src = reinterpret_cast<const uint8_t *>(s0);
+  s.bytes = (s1 > s0) ? (int)(s1 - s0) : 0;
+  s.elem0 = (int)((s0 - a) / es);
+  s.head_end = min(p.V, (int)((i0 - a) / es));
+  s.tail_begin = max(s.head_end, (int)((i1 - a) / es));
+  return s;
 }
 
-__device__ __forceinline__ void stat_scalar(Stat &st, float x, float c, int idx) {
-  if (x > st.m) stat_raise(st, x, c, idx);
-  st.s += ex2_approx((x - st.mref) * c);
-}
-
-__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
   uint32_t r;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 
-__device__ __forceinline__ float vec_max_bf16(const uint4 &v) {
-  const uint32_t m = bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w));
-  return fmaxf(bf16_lo(m), bf16_hi(m));
-}
-
-__device__ __forceinline__ float vec_max_f32(const uint4 &v) {
-  return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
-               fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
-}
-
-__device__ __forceinline__ float vec_sum_bf16(const uint4 &v, float mref, float c) {
-  const float e0 = ex2_approx((bf16_lo(v.x) - mref) * c);
-  const float e1 = ex2_approx((bf16_hi(v.x) - mref) * c);
-  const float e2 = ex2_approx((bf16_lo(v.y) - mref) * c);
-  const float e3 = ex2_approx((bf16_hi(v.y) - mref) * c);
-  const float e4 = ex2_approx((bf16_lo(v.z) - mref) * c);
-  const float e5 = ex2_approx((bf16_hi(v.z) - mref) * c);
-  const float e6 = ex2_approx((bf16_lo(v.w) - mref) * c);
-  const float e7 = ex2_approx((bf16_hi(v.w) - mref) * c);
-  return ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7));
-}
-
-__device__ __forceinline__ float vec_sum_f32(const uint4 &v, float mref, float c) {
-  const float e0 = ex2_approx((__uint_as_float(v.x) - mref) * c);
-  const float e1 = ex2_approx((__uint_as_float(v.y) - mref) * c);
-  const float e2 = ex2_approx((__uint_as_float(v.z) - mref) * c);
-  const float e3 = ex2_approx((__uint_as_float(v.w) - mref) * c);
-  return (e0 + e1) + (e2 + e3);
-}
-
-// One stage: this thread's (up to) four 16-byte vectors.
-template <int DT>
-__device__ __forceinline__ void stat_stage(Stat &st, const uint8_t *stage, int nvec,
-                                           int first_elem, float c, int tid) {
-  constexpr int kElemsPerVec = (DT == SPECDEC_F32) ? 4 : 8;
-  uint4 v[kVecPerThread];
-  float vm[kVecPerThread];
-  float smax = -INFINITY;
+__device__ __forceinline__ float warp_max_nan(float v) {
 #pragma unroll
-  for (int k = 0; k < kVecPerThread; ++k) {
-    const int j = tid + k * kConsumers;
-    if (j < nvec) {
-      v[k] = *reinterpret_cast<const uint4 *>(stage + (size_t)j * 16);
-      vm[k] = (DT == SPECDEC_F32) ? vec_max_f32(v[k]) : vec_max_bf16(v[k]);
-    } else {
-      v[k] = make_uint4(0, 0, 0, 0);
-      vm[k] = -INFINITY;
+  for (int d = 16; d >= 1; d >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xffffffffu, v, d));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
+__device__ __forceinline__ int warp_min(int v) { return __reduce_min_sync(0xffffffffu, v); }
+
+// Elements held by one lane for one stage: kVecPerLane 16-byte vectors of the
+// stage (vector k is the stage's vector lane + 32 k) plus at most one edge
+// element of the row.
+template <int DT>
+struct LaneData {
+  uint4 v[kVecPerLane];
+  float edge;      // -inf when the lane has no edge element
+  int edge_idx;
+};
+
+template <int DT>
+__device__ __forceinline__ void load_lane(LaneData<DT> &d, const uint8_t *stage, int nvec, int lane) {
+  const uint32_t ninf = (DT == SPECDEC_F32) ? 0xFF800000u : 0xFF80FF80u;
+  if (nvec == kStageBytes / 16) {
+#pragma unroll
+    for (int k = 0; k < kVecPerLane; ++k)
+      d.v[k] = *reinterpret_cast<const uint4 *>(stage + (size_t)(lane + 32 * k) * 16);
+  } else {
+#pragma unroll
+    for (int k = 0; k < kVecPerLane; ++k) {
+      const int j = lane + 32 * k;
+      d.v[k] = (j < nvec) ? *reinterpret_cast<const uint4 *>(stage + (size_t)j * 16)
+                          : make_uint4(ninf, ninf, ninf, ninf);
     }
-    smax = fmaxf(smax, vm[k]);
   }
-  if (smax > st.m) {
-    int first = 0;
-#pragma unroll
-    for (int k = kVecPerThread - 1; k >= 0; --k)
-      if (vm[k] == smax) first = k;
-    stat_raise(st, smax, c, first_elem + (tid + first * kConsumers) * kElemsPerVec);
-  }
-  float acc = 0.0f;
-#pragma unroll
-  for (int k = 0; k < kVecPerThread; ++k) {
-    const int j = tid + k * kConsumers;
-    if (j < nvec)
-      acc += (DT == SPECDEC_F32) ? vec_sum_f32(v[k], st.mref, c) : vec_sum_bf16(v[k], st.mref, c);
-  }
-  st.s += acc;
-}
-
-// merge two partial statistics of the same row
-__device__ __forceinline__ void stat_merge(float &m, float &s, int &a, float m2, float s2, int a2,
-                                           float c) {
-  const float M = fmaxf(m, m2);
-  const float Mref = fmaxf(M, -FLT_MAX);
-  const float f1 = ex2_approx((fmaxf(m, -FLT_MAX) - Mref) * c);
-  const float f2 = ex2_approx((fmaxf(m2, -FLT_MAX) - Mref) * c);
-  const int an = (m > m2) ? a : (m2 > m) ? a2 : min(a, a2);
-  s = s * f1 + s2 * f2;
-  m = M;
-  a = an;
-}
-
-__device__ __forceinline__ void consumer_bar() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumers) : "memory");
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) row_stats_kernel(const RowStatsParams p) {
+__device__ __forceinline__ float lane_max(const LaneData<DT> &d) {
+  float m;
+  if (DT == SPECDEC_F32) {
+    m = d.edge;
+#pragma unroll
+    for (int k = 0; k < kVecPerLane; ++k) {
+      m = fmax_nan(m, fmax_nan(fmax_nan(__uint_as_float(d.v[k].x), __uint_as_float(d.v[k].y)),
+                               fmax_nan(__uint_as_float(d.v[k].z), __uint_as_float(d.v[k].w))));
+    }
+  } else {
+    uint32_t a = bf16x2_max_nan(d.v[0].x, d.v[0].y), b = bf16x2_max_nan(d.v[0].z, d.v[0].w);
+#pragma unroll
+    for (int k = 1; k < kVecPerLane; ++k) {
+      a = bf16x2_max_nan(a, bf16x2_max_nan(d.v[k].x, d.v[k].y));
+      b = bf16x2_max_nan(b, bf16x2_max_nan(d.v[k].z, d.v[k].w));
+    }
+    a = bf16x2_max_nan(a, b);
+    m = fmax_nan(fmax_nan(bf16_lo(a), bf16_hi(a)), d.edge);
+  }
+  return m;
+}
+
+// Sum of 2^((l - m) c) over the lane's elements (packed fp32x2 math).
+template <int DT>
+__device__ __forceinline__ float lane_sum(const LaneData<DT> &d, float c, float m) {
+  const float2 cc = make_float2(c, c);
+  const float2 nm = make_float2(-m, -m);
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
+#pragma unroll
+  for (int k = 0; k < kVecPerLane; ++k) {
+    const uint4 w = d.v[k];
+    float2 x0, x1, x2, x3;
+    if (DT == SPECDEC_F32) {
+      x0 = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+      x1 = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+      x0 = __fmul2_rn(__fadd2_rn(x0, nm), cc);
+      x1 = __fmul2_rn(__fadd2_rn(x1, nm), cc);
+      x0.x = ex2_approx(x0.x);
+      x0.y = ex2_approx(x0.y);
+      x1.x = ex2_approx(x1.x);
+      x1.y = ex2_approx(x1.y);
+      if (k & 1) {
+        acc2 = __fadd2_rn(acc2, x0);
+        acc3 = __fadd2_rn(acc3, x1);
+      } else {
+        acc0 = __fadd2_rn(acc0, x0);
+        acc1 = __fadd2_rn(acc1, x1);
+      }
+    } else {
+      x0 = __fmul2_rn(__fadd2_rn(make_float2(bf16_lo(w.x), bf16_hi(w.x)), nm), cc);
+      x1 = __fmul2_rn(__fadd2_rn(make_float2(bf16_lo(w.y), bf16_hi(w.y)), nm), cc);
+      x2 = __fmul2_rn(__fadd2_rn(make_float2(bf16_lo(w.z), bf16_hi(w.z)), nm), cc);
+      x3 = __fmul2_rn(__fadd2_rn(make_float2(bf16_lo(w.w), bf16_hi(w.w)), nm), cc);
+      x0.x = ex2_approx(x0.x);
+      x0.y = ex2_approx(x0.y);
+      x1.x = ex2_approx(x1.x);
+      x1.y = ex2_approx(x1.y);
+      x2.x = ex2_approx(x2.x);
+      x2.y = ex2_approx(x2.y);
+      x3.x = ex2_approx(x3.x);
+      x3.y = ex2_approx(x3.y);
+      acc0 = __fadd2_rn(acc0, x0);
+      acc1 = __fadd2_rn(acc1, x1);
+      acc2 = __fadd2_rn(acc2, x2);
+      acc3 = __fadd2_rn(acc3, x3);
+    }
+  }
+  acc0 = __fadd2_rn(acc0, acc1);
+  acc2 = __fadd2_rn(acc2, acc3);
+  acc0 = __fadd2_rn(acc0, acc2);
+  const float e = ex2_approx((d.edge - m) * c);  // -inf edge -> 0
+  return (acc0.x + acc0.y) + e;
+}
+
+// First index (in the row) of a lane element equal to wm, INT_MAX if none.
+// Fully unrolled so the stage stays in registers.
+template <int DT>
+__device__ __forceinline__ int lane_first(const LaneData<DT> &d, float wm, int elem0, int lane) {
+  constexpr int kPerVec = (DT == SPECDEC_F32) ? 4 : 8;
+  int best = 0x7FFFFFFF;
+#pragma unroll
+  for (int k = kVecPerLane - 1; k >= 0; --k) {
+    const uint32_t w[4] = {d.v[k].x, d.v[k].y, d.v[k].z, d.v[k].w};
+#pragma unroll
+    for (int t = kPerVec - 1; t >= 0; --t) {
+      const float x = (DT == SPECDEC_F32) ? __uint_as_float(w[t])
+                                          : ((t & 1) ? bf16_hi(w[t >> 1]) : bf16_lo(w[t >> 1]));
+      if (x == wm) best = elem0 + (lane + 32 * k) * kPerVec + t;
+    }
+  }
+  if (d.edge == wm) best = min(best, d.edge_idx);
+  return best;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   StatsSmem &sm = *reinterpret_cast<StatsSmem *>(smem_raw);
   constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
+  constexpr int kPerVec = 16 / es;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const int upr = (p.spr + kUnit - 1) / kUnit;  // units per row
+  const long long units = p.stages / p.spr * upr;
+  const long long first = blockIdx.x;
+  const long long stride = gridDim.x;
+  const long long n_local = (units > first) ? (units - first + stride - 1) / stride : 0;
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kSlots; ++i) {
       mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], kConsumerWarps);
+      mbar_init(&sm.empty[i], 1);
     }
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -210,21 +278,26 @@ __global__ void __launch_bounds__(kThreads, 2) row_stats_kernel(const RowStatsPa
   if (warp == kConsumerWarps) {
     // ------------------------------ producer ------------------------------
     if (lane == 0) {
-      uint32_t gstage = 0;
-      for (long long item = blockIdx.x; item < p.items; item += gridDim.x) {
-        const ItemGeom g = item_geometry(p, item, es);
-        for (long long off = 0; off < g.ibytes; off += kStageBytes) {
-          const uint32_t bytes = (uint32_t)min((long long)kStageBytes, g.ibytes - off);
-          const uint32_t slot = gstage % kStages;
-          const uint32_t use = gstage / kStages;
-          if (use > 0 && !mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1)) {
-            sm.abort_flag = 1;
-            return;
-          }
-          if (sm.abort_flag) return;
-          mbar_arrive_expect_tx(&sm.full[slot], bytes);
-          bulk_copy_g2s(sm.stage[slot], g.i0 + off, bytes, &sm.full[slot]);
-          ++gstage;
+      UnitCursor cur;
+      cur.init(first, stride, upr);
+      uint32_t slot = 0, use = 0;
+      for (long long i = 0; i < n_local; ++i) {
+        if (use > 0 && !mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1)) {
+          sm.abort_flag = 1;
+          return;
+        }
+        if (sm.abort_flag) return;
+        const UnitGeom g = unit_geometry(p, cur.row, cur.ju, es);
+        cur.advance(upr);
+        if (g.bytes > 0) {
+          mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)g.bytes);
+          bulk_copy_g2s(sm.stage[slot], g.src, (uint32_t)g.bytes, &sm.full[slot]);
+        } else {
+          mbar_arrive(&sm.full[slot]);
+        }
+        if (++slot == kSlots) {
+          slot = 0;
+          ++use;
         }
       }
     }
@@ -232,81 +305,73 @@ __global__ void __launch_bounds__(kThreads, 2) row_stats_kernel(const RowStatsPa
   }
 
   // ------------------------------ consumers -------------------------------
-  uint32_t gstage = 0;
-  int par = 0;
-  for (long long item = blockIdx.x; item < p.items; item += gridDim.x) {
-    const ItemGeom g = item_geometry(p, item, es);
-    const long long b = g.row / p.R;
-    const float c = temperature_scale(__ldg(p.temperature + b));
-    Stat st;
-    st.m = -INFINITY;
-    st.mref = -FLT_MAX;
-    st.s = 0.0f;
-    st.arg = 0x7FFFFFFF;
-    const long long row_off = g.row * (long long)p.V;
+  // This warp handles local units warp, warp + W, ...; its slot cycles through
+  // warp, warp + W, ... (kSlots / W slots).  The temperature of the next unit
+  // is loaded one iteration ahead.
+  UnitCursor cur;
+  cur.init(first + warp * stride, stride * kConsumerWarps, upr);
+  uint32_t slot = warp, use = 0;
+  float T_next = (warp < n_local) ? __ldg(p.temperature + cur.row / p.R) : 0.0f;
+  for (long long i = warp; i < n_local; i += kConsumerWarps) {
+    const UnitGeom g = unit_geometry(p, cur.row, cur.ju, es);
+    cur.advance(upr);
+    const float T = T_next;
+    if (i + kConsumerWarps < n_local) T_next = __ldg(p.temperature + cur.row / p.R);
 
-    for (int e = g.e0 + tid; e < g.head_end; e += kConsumers)
-      stat_scalar(st, load_elem(p.logits, DT, row_off + e), c, e);
-
-    for (long long off = 0; off < g.ibytes; off += kStageBytes) {
-      const int bytes = (int)min((long long)kStageBytes, g.ibytes - off);
-      const uint32_t slot = gstage % kStages;
-      const uint32_t use = gstage / kStages;
-      bool ok = !sm.abort_flag && mbar_wait_bounded(&sm.full[slot], use & 1);
-      if (!ok) sm.abort_flag = 1;
-      if (ok) stat_stage<DT>(st, sm.stage[slot], bytes / 16, g.head_end + (int)(off / es), c, tid);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[slot]);
-      ++gstage;
-    }
-
-    for (int e = g.tail_begin + tid; e < g.e1; e += kConsumers)
-      stat_scalar(st, load_elem(p.logits, DT, row_off + e), c, e);
-
-    // block merge of the per-thread statistics
-    float m = st.m, s = st.s;
-    int a = st.arg;
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, d);
-      const float s2 = __shfl_xor_sync(0xffffffffu, s, d);
-      const int a2 = __shfl_xor_sync(0xffffffffu, a, d);
-      stat_merge(m, s, a, m2, s2, a2, c);
-    }
-    if (lane == 0) {
-      sm.red_m[par][warp] = m;
-      sm.red_s[par][warp] = s;
-      sm.red_a[par][warp] = a;
-    }
-    consumer_bar();
-    if (warp == 0) {
-      if (lane < kConsumerWarps) {
-        m = sm.red_m[par][lane];
-        s = sm.red_s[par][lane];
-        a = sm.red_a[par][lane];
-      } else {
-        m = -INFINITY;
-        s = 0.0f;
-        a = 0x7FFFFFFF;
-      }
-#pragma unroll
-      for (int d = kConsumerWarps / 2; d >= 1; d >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, d);
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, d);
-        const int a2 = __shfl_xor_sync(0xffffffffu, a, d);
-        stat_merge(m, s, a, m2, s2, a2, c);
-      }
-      if (lane == 0) {
-        RowPartial r;
-        r.m = m;
-        r.s = s;
-        r.arg = a;
-        r.flags = sm.abort_flag ? SPECDEC_ROW_INTERNAL : 0;
-        p.part[item] = r;
+    float edge = -INFINITY;
+    int edge_idx = 0x7FFFFFFF;
+    if (g.j0 == 0) {
+      const int n_head = g.head_end, n_tail = p.V - g.tail_begin;
+      int e = -1;
+      if (lane < n_head) e = lane;
+      else if (lane < n_head + n_tail) e = g.tail_begin + (lane - n_head);
+      if (e >= 0) {
+        edge = load_elem(p.logits, DT, (long long)g.row * p.V + e);
+        edge_idx = e;
       }
     }
-    par ^= 1;
+
+    const bool ok = !sm.abort_flag && mbar_wait_bounded(&sm.full[slot], use & 1);
+    if (!ok) sm.abort_flag = 1;
+    for (int t = 0; t < g.nst; ++t) {
+      LaneData<DT> d;
+      d.edge = (t == 0) ? edge : -INFINITY;
+      d.edge_idx = (t == 0) ? edge_idx : 0x7FFFFFFF;
+      const int sbytes = max(0, min(kStageBytes, g.bytes - t * kStageBytes));
+      if (ok) load_lane<DT>(d, sm.stage[slot] + t * kStageBytes, sbytes / 16, lane);
+      if (t == g.nst - 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);  // the unit is in registers now
+      }
+      RowPartial r;
+      r.flags = ok ? 0 : SPECDEC_ROW_INTERNAL;
+      r.arg = 0x7FFFFFFF;
+      r.m = -INFINITY;
+      r.s = 0.0f;
+      if (ok) {
+        const float wm = warp_max_nan(lane_max<DT>(d));
+        r.m = wm;
+        if (T == 0.0f) {
+          // greedy row: only the maximum and its first index are needed
+          const int first_idx =
+              (wm == wm && wm != -INFINITY)
+                  ? lane_first<DT>(d, wm, g.elem0 + t * (kStageBytes / es), lane)
+                  : 0x7FFFFFFF;
+          r.arg = warp_min(first_idx);
+          r.s = (wm == -INFINITY) ? 0.0f : 1.0f;
+        } else if (wm != -INFINITY) {
+          r.s = warp_sum(lane_sum<DT>(d, temperature_scale(T), wm));
+        }
+      }
+      if (lane == 0) p.part[(long long)g.row * p.spr + g.j0 + t] = r;
+    }
+    slot += kConsumerWarps;
+    if (slot >= kSlots) {
+      slot = warp;
+      ++use;
+    }
   }
+  (void)kPerVec;
 }
 
 int g_sm_count[64];
@@ -336,8 +401,9 @@ cudaError_t launch_dt(const RowStatsParams &p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
-  long long grid = 2LL * sm_count_of_current_device();
-  if (grid > p.items) grid = p.items;
+  const long long units = p.stages / p.spr * ((p.spr + kUnit - 1) / kUnit);
+  long long grid = sm_count_of_current_device();
+  if (grid > units) grid = units;
   row_stats_kernel<DT><<<(unsigned)grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
@@ -345,7 +411,7 @@ cudaError_t launch_dt(const RowStatsParams &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream) {
-  if (p.items <= 0) return cudaSuccess;
+  if (p.stages <= 0) return cudaSuccess;
   return p.dtype == SPECDEC_F32 ? launch_dt<SPECDEC_F32>(p, stream)
                                 : launch_dt<SPECDEC_BF16>(p, stream);
 }

@@ -6,8 +6,11 @@ Tolerances (written here, used by every parity test):
 * accepted counts, paths and every token: bit-exact, except in a request with
   a boundary draw: an accept test the oracle ran with |u - min(1, p/q)| < 1e-6,
   or a final draw whose U*Z lies within 1e-6*Z of a CDF boundary around the
-  oracle's token.  Such requests are counted and excluded from the exact
-  comparison; at most max(1, 1e-4 * draws) of them may occur.
+  oracle's token.  A mismatch outside that band fails the test.  Mismatches
+  inside the band ("excused") are counted and at most max(1, 1e-4 * draws) of
+  them may occur in one case.  (With V ~ 1e5 every CDF cell is only ~1e-5
+  wide, so a quarter of all final draws lie inside the band; the allowance
+  therefore limits the draws that actually differ, not the in-band ones.)
 * request status bitmasks: exact.
 """
 import numpy as np
@@ -25,7 +28,7 @@ def linear_draws(o, gamma):
 def compare_linear(w, g, o, max_boundary_frac=1e-4):
     """g: GPU outputs as numpy dict; o: oracle outputs (with diagnostics)."""
     B, gamma = w.B, w.gamma
-    rep = dict(B=B, boundary=0, mismatched_boundary=0, max_p_err=0.0)
+    rep = dict(B=B, draws=0, in_band=0, excused=0, max_p_err=0.0)
     assert np.array_equal(g["row_status"], o["row_status"]), \
         (np.nonzero(g["row_status"] != o["row_status"]), g["row_status"], o["row_status"])
     ok = o["row_status"] == 0
@@ -50,21 +53,21 @@ def compare_linear(w, g, o, max_boundary_frac=1e-4):
                 and g["is_bonus"][b] == o["is_bonus"][b]
                 and np.array_equal(g["out_tokens"][b], o["out_tokens"][b]))
         if near:
-            rep["boundary"] += 1
-            rep["mismatched_boundary"] += int(not same)
+            rep["in_band"] += 1
+            rep["excused"] += int(not same)
             continue
         assert same, dict(b=int(b), gpu_k=int(g["n_accepted"][b]), ora_k=k,
                           gpu_tok=int(g["final_token"][b]), ora_tok=int(o["final_token"][b]),
                           ratio=o["ratio"][b], u=u[b], margin=o["final_margin"][b],
                           gpu_out=g["out_tokens"][b], ora_out=o["out_tokens"][b])
-    draws = linear_draws(o, gamma)
-    assert rep["boundary"] <= max(1, max_boundary_frac * draws), rep
+    rep["draws"] = linear_draws(o, gamma)
+    assert rep["excused"] <= max(1, max_boundary_frac * rep["draws"]), rep
     return rep
 
 
 def compare_tree(w, g, o, max_boundary_frac=1e-4):
     B = w.B
-    rep = dict(B=B, boundary=0, mismatched_boundary=0, max_p_err=0.0)
+    rep = dict(B=B, draws=0, in_band=0, excused=0, max_p_err=0.0)
     assert np.array_equal(g["row_status"], o["row_status"]), (g["row_status"], o["row_status"])
     ok = o["row_status"] == 0
     bad = ~ok
@@ -83,15 +86,15 @@ def compare_tree(w, g, o, max_boundary_frac=1e-4):
         same = all(np.array_equal(g[key][b], o[key][b]) for key in
                    ("n_accepted", "path_nodes", "out_tokens", "final_token", "is_bonus"))
         if near:
-            rep["boundary"] += 1
-            rep["mismatched_boundary"] += int(not same)
+            rep["in_band"] += 1
+            rep["excused"] += int(not same)
             continue
         assert same, dict(b=int(b), **{key: (g[key][b], o[key][b]) for key in
                                        ("n_accepted", "path_nodes", "out_tokens",
                                         "final_token", "is_bonus")},
                           tm=o["test_margin"][b], fm=o["final_margin"][b])
-    draws = int(o["n_accepted"].sum() + 2 * B)
-    assert rep["boundary"] <= max(1, max_boundary_frac * draws), rep
+    rep["draws"] = int(o["n_accepted"].sum() + 2 * B)
+    assert rep["excused"] <= max(1, max_boundary_frac * rep["draws"]), rep
     return rep
 
 

@@ -144,6 +144,20 @@ def test_malformed_requests_report_status(oracle_lib):
     assert g["row_status"][9] == 0
 
 
+def test_input_domain_edges(oracle_lib):
+    w = W.make_linear("normal2_tq08", B=8, gamma=2, V=3001, dtype="f32", seed=12)
+    w.temperature[0] = 2.0 ** -20
+    w.temperature[1] = 2.0 ** -21
+    w.temperature[2] = 2.0 ** 20
+    w.temperature[3] = 2.0 ** 21
+    w.logits[4, 1, 3] = 2.0 ** 101
+    w.logits[5, 0, 2] = -(2.0 ** 110)
+    w.logits[6, 2, 7] = 2.0 ** 100
+    w.logits[7, 0, :] = -(2.0 ** 120)
+    g, o, rep = run(w, oracle_lib)
+    assert list(g["row_status"]) == [0, 8, 0, 8, 4, 0, 0, 0]
+
+
 def test_deterministic_and_phase_split_agree(oracle_lib):
     import torch
     from speculative_decoding_verification_64_gb300 import binding

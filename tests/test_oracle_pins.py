@@ -386,6 +386,29 @@ def test_small_temperature_tends_to_greedy(oracle_lib):
 # malformed requests
 # ----------------------------------------------------------------------------
 
+def test_input_domain_edges(oracle_lib):
+    """Valid temperatures are 0 or [2^-20, 2^20]; a row whose largest logit
+    exceeds 2^100 is not usable (so l/T cannot overflow float32); very
+    negative finite logits are valid (zero mass)."""
+    B, gamma, V = 6, 1, 8
+    logits = np.zeros((B, gamma + 1, V), np.float32)
+    q = np.full((B, gamma, V), 1.0 / V, np.float32)
+    toks = np.zeros((B, gamma), np.int32)
+    temp = np.ones(B, np.float32)
+    temp[0] = 2.0 ** -20
+    temp[1] = 2.0 ** -21
+    temp[2] = 2.0 ** 20
+    temp[3] = 2.0 ** 21
+    logits[4, 1, 3] = 2.0 ** 101
+    logits[5, 0, 2] = -(2.0 ** 110)
+    logits[5, 1, 0] = 2.0 ** 100
+    out = oracle_lib.verify_linear(logits, q, "f32", toks, temp,
+                                   W.philox_uniforms(3, (B, gamma + 1)))
+    assert list(out["row_status"]) == [0, oracle_lib.ROW_BAD_TEMP, 0, oracle_lib.ROW_BAD_TEMP,
+                                       oracle_lib.ROW_NONFINITE, 0]
+    assert out["final_token"][5] >= 0
+
+
 def test_status_bits_and_sentinels(oracle_lib):
     B, gamma, V = 8, 2, 16
     rng = np.random.default_rng(1)
