@@ -9,18 +9,20 @@
 // reads every logit exactly once and carries almost all of the verify step's
 // HBM traffic.
 //
-// Structure (GB300): a persistent grid of one CTA per SM; stage g goes to CTA
-// g mod grid, so at any moment the CTAs sweep neighbouring stages and a
-// request's rows are read close together in time.  In each CTA one producer
-// thread streams its stages into a ring of 24 x 8 KB shared-memory slots
-// with 1-D bulk TMA copies (cp.async.bulk) that complete on per-slot "full"
-// mbarriers.  Eight consumer warps each own every eighth slot: a warp reads a
-// whole stage with 128-bit shared loads (16 vectors per lane), takes the
+// Structure (GB300): a persistent grid of one CTA per SM.  Rows are moved in
+// units of two consecutive 8 KB stages (16 KB: one 1-D bulk TMA copy,
+// cp.async.bulk, per unit, since the copy engine's cost is per operation);
+// unit g goes to CTA g mod grid, so at any moment the CTAs sweep neighbouring
+// units and a request's rows are read close together in time.  In each CTA
+// one producer thread streams its units into a ring of 12 shared-memory slots
+// whose "full" mbarriers the copies complete.  Twelve consumer warps take the
+// stages round robin: a warp reads a whole stage with 128-bit shared loads
+// (16 vectors per lane), arrives on the unit's "empty" barrier, takes the
 // stage max with NaN-propagating packed bf16 max, then forms the exponent
 // arguments (l - m) c with packed fp32x2 add and multiply (l - m is exact for
 // bf16 inputs), one ex2 per element and packed adds,
-// reduces over the warp with shuffles and releases the slot on its "empty"
-// mbarrier.  Consumer warps never wait on each other.  The unaligned edge
+// reduces over the warp with shuffles and writes the stage's partial.
+// Consumer warps never wait on each other.  The unaligned edge
 // elements of a row (< 16 bytes at each end) are read with plain loads by the
 // warp of the row's first stage.  Every wait is bounded in time.
 #include <cfloat>
@@ -30,23 +32,27 @@
 namespace specdec {
 namespace {
 
+// Defaults measured on GB300 (B=256, V=128256 bf16): 16 KB copies, 12 slots
+// (192 KB in flight per SM) and 12 consumer warps stream at ~96% of the
+// measured copy bandwidth; 8 KB copies are limited by the per-copy cost and
+// fewer warps by the arithmetic.
 #ifndef SPECDEC_K1_WARPS
-#define SPECDEC_K1_WARPS 8
+#define SPECDEC_K1_WARPS 12
 #endif
 #ifndef SPECDEC_K1_SLOTS
-#define SPECDEC_K1_SLOTS 24
+#define SPECDEC_K1_SLOTS 12
 #endif
 #ifndef SPECDEC_K1_UNIT
-#define SPECDEC_K1_UNIT 1
+#define SPECDEC_K1_UNIT 2
 #endif
 constexpr int kConsumerWarps = SPECDEC_K1_WARPS;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kSlots = SPECDEC_K1_SLOTS;             // a multiple of the consumer warps
+constexpr int kSlots = SPECDEC_K1_SLOTS;             // units in flight per CTA
 constexpr int kUnit = SPECDEC_K1_UNIT;               // stages moved by one bulk copy
 constexpr int kUnitBytes = kUnit * kStageBytes;
 constexpr int kVecPerLane = kStageBytes / 16 / 32;   // 16-byte vectors per lane per stage
-static_assert(kSlots % kConsumerWarps == 0, "slot i belongs to warp i % kConsumerWarps");
 static_assert(kVecPerLane * 32 * 16 == kStageBytes, "a stage is a whole number of warp loads");
+static_assert(kSlots * kUnitBytes <= 200 * 1024, "stage ring fits in shared memory");
 
 struct StatsSmem {
   alignas(128) uint8_t stage[kSlots][kUnitBytes];
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
   if (tid == 0) {
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], 1);
+      mbar_init(&sm.empty[i], kUnit);  // one arrival per stage of the unit
     }
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -305,71 +311,74 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
   }
 
   // ------------------------------ consumers -------------------------------
-  // This warp handles local units warp, warp + W, ...; its slot cycles through
-  // warp, warp + W, ... (kSlots / W slots).  The temperature of the next unit
-  // is loaded one iteration ahead.
-  UnitCursor cur;
-  cur.init(first + warp * stride, stride * kConsumerWarps, upr);
-  uint32_t slot = warp, use = 0;
-  float T_next = (warp < n_local) ? __ldg(p.temperature + cur.row / p.R) : 0.0f;
-  for (long long i = warp; i < n_local; i += kConsumerWarps) {
-    const UnitGeom g = unit_geometry(p, cur.row, cur.ju, es);
-    cur.advance(upr);
+  // Local stage c = i * kUnit + t (stage t of local unit i) belongs to warp
+  // c % W.  Every warp assigned to a unit waits for the unit's copy, takes its
+  // stage into registers and arrives once on the unit's "empty" barrier (also
+  // for stages past the end of a row, which hold no data), so the barrier
+  // completes exactly when all kUnit stages of the unit have been read.  The
+  // temperature of the warp's next stage is loaded one iteration ahead.
+  const long long n_stages_local = n_local * kUnit;
+  auto unit_row = [&](long long c) -> int {
+    const long long g = first + (c / kUnit) * stride;
+    return (int)(g / upr);
+  };
+  float T_next = (warp < n_stages_local) ? __ldg(p.temperature + unit_row(warp) / p.R) : 0.0f;
+  for (long long c = warp; c < n_stages_local; c += kConsumerWarps) {
+    const long long i = c / kUnit;
+    const int t = (int)(c - i * kUnit);
+    const long long g = first + i * stride;
+    const int row = (int)(g / upr);
+    const UnitGeom u = unit_geometry(p, row, (int)(g - (long long)row * upr), es);
+    const uint32_t slot = (uint32_t)(i % kSlots);
+    const uint32_t use = (uint32_t)(i / kSlots);
     const float T = T_next;
-    if (i + kConsumerWarps < n_local) T_next = __ldg(p.temperature + cur.row / p.R);
+    if (c + kConsumerWarps < n_stages_local)
+      T_next = __ldg(p.temperature + unit_row(c + kConsumerWarps) / p.R);
+    const bool real = t < u.nst;
 
-    float edge = -INFINITY;
-    int edge_idx = 0x7FFFFFFF;
-    if (g.j0 == 0) {
-      const int n_head = g.head_end, n_tail = p.V - g.tail_begin;
+    LaneData<DT> d;
+    d.edge = -INFINITY;
+    d.edge_idx = 0x7FFFFFFF;
+    if (real && u.j0 + t == 0) {
+      const int n_head = u.head_end, n_tail = p.V - u.tail_begin;
       int e = -1;
       if (lane < n_head) e = lane;
-      else if (lane < n_head + n_tail) e = g.tail_begin + (lane - n_head);
+      else if (lane < n_head + n_tail) e = u.tail_begin + (lane - n_head);
       if (e >= 0) {
-        edge = load_elem(p.logits, DT, (long long)g.row * p.V + e);
-        edge_idx = e;
+        d.edge = load_elem(p.logits, DT, (long long)row * p.V + e);
+        d.edge_idx = e;
       }
     }
 
     const bool ok = !sm.abort_flag && mbar_wait_bounded(&sm.full[slot], use & 1);
     if (!ok) sm.abort_flag = 1;
-    for (int t = 0; t < g.nst; ++t) {
-      LaneData<DT> d;
-      d.edge = (t == 0) ? edge : -INFINITY;
-      d.edge_idx = (t == 0) ? edge_idx : 0x7FFFFFFF;
-      const int sbytes = max(0, min(kStageBytes, g.bytes - t * kStageBytes));
-      if (ok) load_lane<DT>(d, sm.stage[slot] + t * kStageBytes, sbytes / 16, lane);
-      if (t == g.nst - 1) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[slot]);  // the unit is in registers now
+    const int sbytes = max(0, min(kStageBytes, u.bytes - t * kStageBytes));
+    if (ok && real) load_lane<DT>(d, sm.stage[slot] + t * kStageBytes, sbytes / 16, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[slot]);  // this stage is in registers now
+    if (!real) continue;
+
+    RowPartial r;
+    r.flags = ok ? 0 : SPECDEC_ROW_INTERNAL;
+    r.arg = 0x7FFFFFFF;
+    r.m = -INFINITY;
+    r.s = 0.0f;
+    if (ok) {
+      const float wm = warp_max_nan(lane_max<DT>(d));
+      r.m = wm;
+      if (T == 0.0f) {
+        // greedy row: only the maximum and its first index are needed
+        const int first_idx =
+            (wm == wm && wm != -INFINITY)
+                ? lane_first<DT>(d, wm, u.elem0 + t * (kStageBytes / es), lane)
+                : 0x7FFFFFFF;
+        r.arg = warp_min(first_idx);
+        r.s = (wm == -INFINITY) ? 0.0f : 1.0f;
+      } else if (wm != -INFINITY) {
+        r.s = warp_sum(lane_sum<DT>(d, temperature_scale(T), wm));
       }
-      RowPartial r;
-      r.flags = ok ? 0 : SPECDEC_ROW_INTERNAL;
-      r.arg = 0x7FFFFFFF;
-      r.m = -INFINITY;
-      r.s = 0.0f;
-      if (ok) {
-        const float wm = warp_max_nan(lane_max<DT>(d));
-        r.m = wm;
-        if (T == 0.0f) {
-          // greedy row: only the maximum and its first index are needed
-          const int first_idx =
-              (wm == wm && wm != -INFINITY)
-                  ? lane_first<DT>(d, wm, g.elem0 + t * (kStageBytes / es), lane)
-                  : 0x7FFFFFFF;
-          r.arg = warp_min(first_idx);
-          r.s = (wm == -INFINITY) ? 0.0f : 1.0f;
-        } else if (wm != -INFINITY) {
-          r.s = warp_sum(lane_sum<DT>(d, temperature_scale(T), wm));
-        }
-      }
-      if (lane == 0) p.part[(long long)g.row * p.spr + g.j0 + t] = r;
     }
-    slot += kConsumerWarps;
-    if (slot >= kSlots) {
-      slot = warp;
-      ++use;
-    }
+    if (lane == 0) p.part[(long long)row * p.spr + u.j0 + t] = r;
   }
   (void)kPerVec;
 }
