@@ -267,9 +267,15 @@ def run_ours(args, dist):
     stream = torch.cuda.current_stream(device)
     lib = binding.load_library()
 
+    def stats(x):
+        if linear:
+            binding.row_stats(x[0], x[3], ws, q=x[1], draft_tokens=x[2], stream=stream)
+        else:
+            binding.row_stats(x[0], x[4], ws, stream=stream)
+
     def step(s):
         x = sets[s & 1]
-        binding.row_stats(x[0], x[4] if not linear else x[3], ws, stream=stream)
+        stats(x)
         if linear:
             binding.linear_finalize(*x, out, ws, stream=stream)
         else:
@@ -278,7 +284,7 @@ def run_ours(args, dist):
     def step_timed(s, e0, e1, e2):
         x = sets[s & 1]
         e0.record(stream)
-        binding.row_stats(x[0], x[4] if not linear else x[3], ws, stream=stream)
+        stats(x)
         e1.record(stream)
         if linear:
             binding.linear_finalize(*x, out, ws, stream=stream)

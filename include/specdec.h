@@ -126,19 +126,24 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
 /*
  * Phase 1 of either form, callable alone: per-row softmax statistics
  * (section 15.1.2 step 2) of B*rows_per_request rows of V logits, written
- * into the workspace as split partials (max, base-2 exponential sum, first
- * arg-max position).  One streaming pass over the logits.
- *   logits [B, rows_per_request, V], temperature float32 [B].
+ * into the workspace as per-stage partials (max, base-2 exponential sum,
+ * first arg-max position).  One streaming pass over the logits.
+ *   logits        [B, rows_per_request, V], temperature float32 [B]
+ *   q, draft_tokens  linear form: [B, rows_per_request-1, V] and int32
+ *                 [B, rows_per_request-1]; the pass also gathers each drafted
+ *                 token's logit and q value for phase 2.  Both NULL for the
+ *                 tree form or for statistics alone.
  */
-int specdec_row_stats(const void *logits, int dtype, const float *temperature, int B,
-                      int rows_per_request, int V, void *workspace, size_t workspace_bytes,
-                      void *stream);
+int specdec_row_stats(const void *logits, const void *q, int dtype, const int32_t *draft_tokens,
+                      const float *temperature, int B, int rows_per_request, int V,
+                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Phase 2 of the linear form: merge the row statistics in the workspace,
  * run the accept test with early stop (section 15.1.2 step 3) and the
  * correction / bonus draw (step 4).  Same arguments as specdec_verify_linear;
- * the workspace must hold phase 1's result for the same logits, B, gamma, V.
+ * the workspace must hold phase 1's result for the same logits, q,
+ * draft_tokens, B, gamma, V (phase 1 called with q and draft_tokens).
  */
 int specdec_linear_finalize(const void *logits, const void *q, int dtype,
                             const int32_t *draft_tokens, const float *temperature,

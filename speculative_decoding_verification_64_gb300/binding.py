@@ -34,9 +34,9 @@ _EXPORTS = {
     "specdec_abi_version": ([], ctypes.c_int),
     "specdec_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "specdec_workspace_size": ([ctypes.c_int] * 4, ctypes.c_size_t),
-    "specdec_row_stats": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
-                           ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
-                           ctypes.c_void_p], ctypes.c_int),
+    "specdec_row_stats": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                           ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
     "specdec_verify_linear": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
                               [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 +
                               [ctypes.c_void_p] * 7 + [ctypes.c_size_t, ctypes.c_void_p],
@@ -201,12 +201,15 @@ def verify_linear(logits: torch.Tensor, q: torch.Tensor, draft_tokens: torch.Ten
 
 
 def row_stats(logits: torch.Tensor, temperature: torch.Tensor, workspace: torch.Tensor,
+              q: Optional[torch.Tensor] = None, draft_tokens: Optional[torch.Tensor] = None,
               stream=None) -> None:
-    """Phase 1 only (``specdec_row_stats``): logits [B, R, V] -> split partials in workspace."""
+    """Phase 1 only (``specdec_row_stats``): logits [B, R, V] -> stage partials in the
+    workspace.  For the linear form pass q and draft_tokens too (phase 2 needs the
+    drafted tokens' logits and q values, gathered here)."""
     B, R, V = logits.shape
     rc = load_library().specdec_row_stats(
-        _ptr(logits), dtype_code(logits), _ptr(temperature), B, R, V, _ptr(workspace),
-        workspace.numel(), _stream_ptr(stream))
+        _ptr(logits), _ptr(q), dtype_code(logits), _ptr(draft_tokens), _ptr(temperature), B, R, V,
+        _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     _check(rc, "specdec_row_stats")
 
 

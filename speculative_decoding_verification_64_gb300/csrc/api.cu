@@ -14,11 +14,29 @@ int elem_bytes(int dtype) { return dtype == SPECDEC_F32 ? 4 : 2; }
 
 bool dtype_ok(int dtype) { return dtype == SPECDEC_F32 || dtype == SPECDEC_BF16; }
 
-size_t workspace_bytes_for(long long B, int R, int V, int dtype) {
+// Workspace regions, each 256-byte aligned: the stage partials of the stats
+// pass, the gathered (logit, q) of every drafted token, one decision record
+// per request, and the fixed-point chunk totals of the draw.
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct WsLayout {
+  size_t part, gather, dec, chunk, total;
+};
+
+WsLayout workspace_layout(long long B, int R, int V, int dtype) {
   const long long rows = B * (long long)R;
-  const size_t bytes = (size_t)rows * (size_t)stages_per_row(V, elem_bytes(dtype)) *
-                       sizeof(RowPartial);
-  return (bytes + 255) / 256 * 256;
+  WsLayout w;
+  w.part = 0;
+  w.gather = align256((size_t)rows * (size_t)stages_per_row(V, elem_bytes(dtype)) *
+                      sizeof(RowPartial));
+  w.dec = w.gather + align256((size_t)rows * sizeof(float2));
+  w.chunk = w.dec + align256((size_t)B * sizeof(LinearDecision));
+  w.total = w.chunk + align256((size_t)B * draw_chunks(V) * sizeof(unsigned long long));
+  return w;
+}
+
+size_t workspace_bytes_for(long long B, int R, int V, int dtype) {
+  return workspace_layout(B, R, V, dtype).total;
 }
 
 int check_sizes(int B, int R, int V, int dtype) {
@@ -38,10 +56,12 @@ int check_workspace(const void *ws, size_t ws_bytes, int B, int R, int V, int dt
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA; }
 
-int launch_stats(const void *logits, int dtype, const float *temperature, int B, int R, int V,
-                 void *workspace, cudaStream_t stream) {
+int launch_stats(const void *logits, const void *q, int dtype, const int32_t *tokens,
+                 const float *temperature, int B, int R, int V, void *workspace,
+                 cudaStream_t stream) {
   const long long rows = (long long)B * R;
   const int spr = stages_per_row(V, elem_bytes(dtype));
+  const WsLayout w = workspace_layout(B, R, V, dtype);
   RowStatsParams p;
   p.logits = logits;
   p.temperature = temperature;
@@ -51,6 +71,9 @@ int launch_stats(const void *logits, int dtype, const float *temperature, int B,
   p.R = R;
   p.V = V;
   p.spr = spr;
+  p.tokens = (q != nullptr) ? tokens : nullptr;
+  p.q = q;
+  p.gather = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(workspace) + w.gather);
   return cuda_status(launch_row_stats(p, stream));
 }
 
@@ -77,17 +100,19 @@ size_t specdec_workspace_size(int B, int rows_per_request, int V, int dtype) {
   return workspace_bytes_for(B, rows_per_request, V, dtype);
 }
 
-int specdec_row_stats(const void *logits, int dtype, const float *temperature, int B,
-                      int rows_per_request, int V, void *workspace, size_t workspace_bytes,
-                      void *stream) {
+int specdec_row_stats(const void *logits, const void *q, int dtype, const int32_t *draft_tokens,
+                      const float *temperature, int B, int rows_per_request, int V,
+                      void *workspace, size_t workspace_bytes, void *stream) {
   int st = check_sizes(B, rows_per_request, V, dtype);
   if (st != SPECDEC_OK) return st;
   if (B == 0) return SPECDEC_OK;
   if (!logits || !temperature) return SPECDEC_ERR_INVALID_ARG;
+  if ((q == nullptr) != (draft_tokens == nullptr)) return SPECDEC_ERR_INVALID_ARG;
+  if (q != nullptr && rows_per_request < 2) return SPECDEC_ERR_INVALID_ARG;
   st = check_workspace(workspace, workspace_bytes, B, rows_per_request, V, dtype);
   if (st != SPECDEC_OK) return st;
-  return launch_stats(logits, dtype, temperature, B, rows_per_request, V, workspace,
-                      static_cast<cudaStream_t>(stream));
+  return launch_stats(logits, q, dtype, draft_tokens, temperature, B, rows_per_request, V,
+                      workspace, static_cast<cudaStream_t>(stream));
 }
 
 static int linear_checks(const void *logits, const void *q, int dtype, const int32_t *tokens,
@@ -125,11 +150,17 @@ static int linear_finalize_launch(const void *logits, const void *q, int dtype,
   p.is_bonus = is_bonus;
   p.row_status = row_status;
   p.p_draft = p_draft;
+  const WsLayout w = workspace_layout(B, gamma + 1, V, dtype);
+  uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+  p.dec = reinterpret_cast<LinearDecision *>(ws + w.dec);
+  p.gather = reinterpret_cast<const float2 *>(ws + w.gather);
+  p.chunk_tot = reinterpret_cast<unsigned long long *>(ws + w.chunk);
   p.dtype = dtype;
   p.B = B;
   p.gamma = gamma;
   p.V = V;
   p.spr = stages_per_row(V, elem_bytes(dtype));
+  p.nchunk = draw_chunks(V);
   return cuda_status(launch_linear_finalize(p, stream));
 }
 
@@ -159,7 +190,7 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
                          workspace_bytes);
   if (st != SPECDEC_OK || B == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = launch_stats(logits, dtype, temperature, B, gamma + 1, V, workspace, s);
+  st = launch_stats(logits, q, dtype, draft_tokens, temperature, B, gamma + 1, V, workspace, s);
   if (st != SPECDEC_OK) return st;
   return linear_finalize_launch(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma,
                                 V, n_accepted, out_tokens, final_token, is_bonus, row_status,
@@ -243,7 +274,7 @@ int specdec_verify_tree(const void *logits, const void *q, int dtype, const int3
                        row_status, workspace, workspace_bytes);
   if (st != SPECDEC_OK || B == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = launch_stats(logits, dtype, temperature, B, N, V, workspace, s);
+  st = launch_stats(logits, nullptr, dtype, nullptr, temperature, B, N, V, workspace, s);
   if (st != SPECDEC_OK) return st;
   return tree_finalize_launch(logits, q, dtype, node_tokens, parent, temperature, uniforms, B, N,
                               V, max_depth, n_accepted, path_nodes, out_tokens, final_token,

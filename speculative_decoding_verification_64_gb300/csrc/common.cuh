@@ -28,6 +28,11 @@ static_assert(sizeof(RowPartial) == 16, "RowPartial is 16 bytes");
 #endif
 constexpr int kStageBytes = SPECDEC_STAGE_BYTES;
 
+// Elements per chunk of the linear draw (one CTA each).
+#define SPECDEC_DRAW_CHUNK 8192
+
+inline int draw_chunks(int V) { return (V + SPECDEC_DRAW_CHUNK - 1) / SPECDEC_DRAW_CHUNK; }
+
 inline int stages_per_row(int V, int elem_bytes) {
   const long long b = (long long)V * elem_bytes;
   return (int)((b + kStageBytes - 1) / kStageBytes);
@@ -43,7 +48,27 @@ struct RowStatsParams {
   long long stages;  // rows * spr
   int dtype;
   int R, V, spr;     // rows per request, vocabulary, stages per row
+  // Linear form only (tokens == nullptr otherwise): row i < R - 1 of request b
+  // scores draft token tokens[b * (R - 1) + i]; the pass stores that token's
+  // logit and its q value in gather[row] (left unwritten if the token is out
+  // of range).
+  const int32_t *tokens;
+  const void *q;
+  float2 *gather;
 };
+
+// Per-request decision of the linear accept test, handed from the decide
+// kernel to the draw kernel through the workspace (after the partials).
+struct LinearDecision {
+  int32_t k;       // first rejected position (gamma: all accepted)
+  int32_t status;  // SPECDEC_ROW_* bits; nonzero: nothing to draw
+  int32_t greedy;  // T == 0: final token already written
+  float M;         // max of the final row
+  float S;         // sum of 2^((l - M) c) over the final row
+  float c;         // log2(e) / T
+  int32_t pad[2];
+};
+static_assert(sizeof(LinearDecision) == 32, "LinearDecision is 32 bytes");
 
 struct LinearFinalizeParams {
   const void *logits;
@@ -58,7 +83,10 @@ struct LinearFinalizeParams {
   uint8_t *is_bonus;
   int32_t *row_status;
   float *p_draft;
-  int dtype, B, gamma, V, spr;
+  LinearDecision *dec;
+  const float2 *gather;          // (l_i(x~_i), q_i(x~_i)) per row, from the stats pass
+  unsigned long long *chunk_tot; // [B, nchunk] fixed-point chunk sums of the draw
+  int dtype, B, gamma, V, spr, nchunk;
 };
 
 struct TreeFinalizeParams {

@@ -30,7 +30,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kPerThread = 16;        // contiguous elements per thread in a tile
 constexpr int kTile = kThreads * kPerThread;
 constexpr int kBatch = 4;             // tiles whose loads are in flight together
-constexpr int kMaxTilesPerCta = (SPECDEC_MAX_V + kTile * kG - 1) / (kTile * kG);
+constexpr int kMaxTilesPerCta = ((SPECDEC_MAX_V + kG - 1) / kG + 15 + kTile - 1) / kTile;
 constexpr double kFixedUnit = 0x1p-40;  // value of one unit of the fixed-point sums
 
 struct RowStat {
@@ -93,20 +93,30 @@ __device__ __forceinline__ float target_prob(float lx, const RowStat &r, float c
   return exp2f((lx - r.M) * c) / r.S;
 }
 
+// One CTA's share of a draw: the slice [v0, v1) of the row, read through
+// lrow/qrow (element v at byte v * es; the pointers may point at a copy of
+// the slice in shared memory, offset so that the same indexing holds).
 struct DrawRow {
   const uint8_t *lrow;  // logits row
   const uint8_t *qrow;  // q row (read only when use_q)
-  int V;
+  int v0, v1;           // the slice
   float M, c;           // e_v = 2^((l - M) c)
   float K;              // w_v = max(0, e_v - K q_v)
   bool use_q;
-  bool vec_ok;          // rows 16-byte aligned: vector loads
+  bool vec_ok;          // 16-byte aligned rows: vector loads
 };
 
 __device__ __forceinline__ float elem_e(const DrawRow &r, float l) { return ex2_approx((l - r.M) * r.c); }
 
 __device__ __forceinline__ float elem_w(const DrawRow &r, float e, float q) {
   return r.use_q ? fmaxf(fmaf(-r.K, q, e), 0.0f) : e;
+}
+
+// Plain (generic) element load: the row may live in global or shared memory.
+template <int DT>
+__device__ __forceinline__ uint32_t load_bits(const uint8_t *row, int v) {
+  if (DT == SPECDEC_F32) return *reinterpret_cast<const uint32_t *>(row + (size_t)v * 4);
+  return *reinterpret_cast<const uint16_t *>(row + (size_t)v * 2);
 }
 
 // 16 contiguous elements of a tile as raw 16-byte vectors (bf16: 2 vectors per
@@ -121,7 +131,7 @@ template <int DT>
 __device__ __forceinline__ void load_raw(const DrawRow &r, int e, Raw16<DT> &x) {
   constexpr int n = (DT == SPECDEC_F32) ? 4 : 2;
   constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
-  if (r.vec_ok && e + kPerThread <= r.V) {
+  if (r.vec_ok && e + kPerThread <= r.v1) {
     const uint4 *lp = reinterpret_cast<const uint4 *>(r.lrow + (size_t)e * es);
 #pragma unroll
     for (int k = 0; k < n; ++k) x.l[k] = lp[k];
@@ -131,27 +141,23 @@ __device__ __forceinline__ void load_raw(const DrawRow &r, int e, Raw16<DT> &x) 
       for (int k = 0; k < n; ++k) x.q[k] = qp[k];
     }
   } else {
-    // ragged or unaligned: element by element; beyond V the logit is -inf (weight 0)
+    // ragged or unaligned: element by element; past the slice the logit is -inf (weight 0)
     uint32_t lw[4 * n], qw[4 * n];
 #pragma unroll
     for (int k = 0; k < kPerThread; ++k) {
       const int v = e + k;
-      uint32_t lb, qb = 0;
+      const bool in = v < r.v1;
+      const uint32_t lb = in ? load_bits<DT>(r.lrow, v) : (DT == SPECDEC_F32 ? 0xFF800000u : 0xFF80u);
+      const uint32_t qb = (in && r.use_q) ? load_bits<DT>(r.qrow, v) : 0u;
       if (DT == SPECDEC_F32) {
-        lb = (v < r.V) ? __float_as_uint(load_elem(r.lrow, DT, v)) : 0xFF800000u;
-        if (r.use_q && v < r.V) qb = __float_as_uint(load_elem(r.qrow, DT, v));
         lw[k] = lb;
         qw[k] = qb;
+      } else if (k & 1) {
+        lw[k >> 1] |= lb << 16;
+        qw[k >> 1] |= qb << 16;
       } else {
-        lb = (v < r.V) ? (__float_as_uint(load_elem(r.lrow, DT, v)) >> 16) : 0xFF80u;
-        if (r.use_q && v < r.V) qb = __float_as_uint(load_elem(r.qrow, DT, v)) >> 16;
-        if (k & 1) {
-          lw[k >> 1] |= lb << 16;
-          qw[k >> 1] |= qb << 16;
-        } else {
-          lw[k >> 1] = lb;
-          qw[k >> 1] = qb;
-        }
+        lw[k >> 1] = lb;
+        qw[k >> 1] = qb;
       }
     }
 #pragma unroll
@@ -183,7 +189,7 @@ __device__ __forceinline__ unsigned long long weights16(const DrawRow &r, const 
 #pragma unroll
   for (int k = 0; k < kPerThread; ++k) {
     const float q = r.use_q ? raw_elem<DT>(x.q, k) : 0.0f;
-    w[k] = (e + k < r.V) ? elem_w(r, elem_e(r, raw_elem<DT>(x.l, k)), q) : 0.0f;
+    w[k] = (e + k < r.v1) ? elem_w(r, elem_e(r, raw_elem<DT>(x.l, k)), q) : 0.0f;
     s += w[k];
   }
   return to_fixed40(s);
@@ -201,30 +207,32 @@ struct DrawSmem {
   int found;
 };
 
-// One pass over this CTA's tiles [t0, t1) of the row: per-tile fixed-point
-// totals in smem and the CTA total, published in slot `pass & 1`.
+__device__ __forceinline__ int slice_tiles(const DrawRow &r) { return (r.v1 - r.v0 + kTile - 1) / kTile; }
+
+// One pass over this CTA's slice: per-tile fixed-point totals in smem and the
+// CTA total, published in slot `pass & 1`.
 template <int DT>
-__device__ __forceinline__ void draw_sums(DrawSmem &ds, const DrawRow &r, int t0, int t1,
-                                          int pass) {
+__device__ __forceinline__ void draw_sums(DrawSmem &ds, const DrawRow &r, int pass) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int tb = t0; tb < t1; tb += kBatch) {
+  const int nt = slice_tiles(r);
+  for (int tb = 0; tb < nt; tb += kBatch) {
     Raw16<DT> x[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u)
-      if (tb + u < t1) load_raw<DT>(r, (tb + u) * kTile + tid * kPerThread, x[u]);
+      if (tb + u < nt) load_raw<DT>(r, r.v0 + (tb + u) * kTile + tid * kPerThread, x[u]);
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      if (tb + u < t1) {
+      if (tb + u < nt) {
         float w[kPerThread];
-        unsigned long long f = weights16<DT>(r, x[u], (tb + u) * kTile + tid * kPerThread, w);
+        unsigned long long f = weights16<DT>(r, x[u], r.v0 + (tb + u) * kTile + tid * kPerThread, w);
 #pragma unroll
         for (int d = 16; d >= 1; d >>= 1) f += shfl_xor_u64(f, d);
-        if (lane == 0) ds.warp_tile[tb + u - t0][warp] = f;
+        if (lane == 0) ds.warp_tile[tb + u][warp] = f;
       }
     }
   }
   __syncthreads();
-  for (int i = tid; i < t1 - t0; i += kThreads) {
+  for (int i = tid; i < nt; i += kThreads) {
     unsigned long long s = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) s += ds.warp_tile[i][w];
@@ -233,7 +241,7 @@ __device__ __forceinline__ void draw_sums(DrawSmem &ds, const DrawRow &r, int t0
   __syncthreads();
   if (tid == 0) {
     unsigned long long s = 0;
-    for (int i = 0; i < t1 - t0; ++i) s += ds.tile_tot[i];
+    for (int i = 0; i < nt; ++i) s += ds.tile_tot[i];
     ds.cta_total = s;
     ds.shared_total[pass & 1] = s;
   }
@@ -261,22 +269,23 @@ __device__ __forceinline__ void draw_exchange(DrawSmem &ds, cg::cluster_group &c
   __syncthreads();
 }
 
-// If the crossing of `target` lies in this CTA, find the smallest v with
-// C_v > target (C: prefix sums of the last pass's weights).  Returns v in
-// every thread of that CTA, -1 elsewhere.
+// If the crossing of `target` lies in this CTA's slice, find the smallest v
+// with C_v > target (C: prefix sums of the last pass's weights).  Returns v
+// in every thread of that CTA, -1 elsewhere.
 template <int DT>
-__device__ __forceinline__ int draw_search(DrawSmem &ds, const DrawRow &r, int t0, int t1,
+__device__ __forceinline__ int draw_search(DrawSmem &ds, const DrawRow &r,
                                            unsigned long long target) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nt = slice_tiles(r);
   const unsigned long long pre = ds.prefix;
   const bool mine = (pre <= target) && (target - pre < ds.cta_total);
   if (!mine) return -1;  // uniform across the CTA
   if (tid == 0) {
     unsigned long long run = pre;
-    int tile = t1 - 1;
-    for (int i = 0; i < t1 - t0; ++i) {
+    int tile = nt - 1;
+    for (int i = 0; i < nt; ++i) {
       if (target - run < ds.tile_tot[i]) {
-        tile = t0 + i;
+        tile = i;
         break;
       }
       run += ds.tile_tot[i];
@@ -286,7 +295,7 @@ __device__ __forceinline__ int draw_search(DrawSmem &ds, const DrawRow &r, int t
     ds.found = -1;
   }
   __syncthreads();
-  const int e = ds.tile * kTile + tid * kPerThread;
+  const int e = r.v0 + ds.tile * kTile + tid * kPerThread;
   Raw16<DT> x;
   float w[kPerThread];
   load_raw<DT>(r, e, x);
@@ -319,12 +328,18 @@ __device__ __forceinline__ int draw_search(DrawSmem &ds, const DrawRow &r, int t
   return ds.found;
 }
 
-// Tiles of the row owned by cluster rank `rank`.
-__device__ __forceinline__ void cta_tiles(int V, int rank, int &t0, int &t1) {
-  const int nt = (V + kTile - 1) / kTile;
-  const int tpc = (nt + kG - 1) / kG;
-  t0 = min(nt, rank * tpc);
-  t1 = min(nt, t0 + tpc);
+// This cluster rank's slice of a row of V elements: a multiple of 16 elements
+// long (so every slice starts 32-byte aligned relative to the row).
+__device__ __forceinline__ void cta_slice(int V, int rank, int &v0, int &v1) {
+  int L = (V + kG - 1) / kG;
+  L = (L + 15) & ~15;
+  v0 = min(V, rank * L);
+  v1 = min(V, v0 + L);
+}
+
+__host__ __device__ inline int slice_capacity(int V) {
+  int L = (V + kG - 1) / kG;
+  return (L + 15) & ~15;
 }
 
 }  // namespace fin

@@ -178,8 +178,6 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
   // ---- the walk ------------------------------------------------------------
   // State of the current node in units of its row maximum: P_j = max(0, e - K q) / E,
   // starting from (K, E) = (0, S) with S the merged sum of the stats pass.
-  int t0, t1;
-  cta_tiles(V, rank, t0, t1);
   int cur = 0, nacc = 0, pass = 0;
   float K = 0.0f, E = 0.0f;
   bool rejected_any = false;  // the node has a rejected child (state (K, E) in use)
@@ -187,7 +185,7 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
   bool bonus = false;
   if (tid == 0) sm.path[0] = 0;
   DrawRow r;
-  r.V = V;
+  cta_slice(V, rank, r.v0, r.v1);
   r.c = c;
   r.use_q = false;
   r.K = 0.0f;
@@ -245,7 +243,7 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
       const float Kn = K + E;
       r.K = Kn;
       r.use_q = true;
-      draw_sums<DT>(sm.ds, r, t0, t1, pass);
+      draw_sums<DT>(sm.ds, r, pass);
       draw_exchange(sm.ds, cluster, pass);
       ++pass;
       if (sm.ds.Z > 0) {
@@ -270,13 +268,13 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
     r.use_q = !bonus && K > 0.0f;
     r.K = K;
     if (!(sums_match && r.use_q)) {
-      draw_sums<DT>(sm.ds, r, t0, t1, pass);
+      draw_sums<DT>(sm.ds, r, pass);
       draw_exchange(sm.ds, cluster, pass);
       ++pass;
     }
     const float U = __ldg(p.uniforms + nodebase);
     const unsigned long long target = uniform_target(U, sm.ds.Z);
-    const int v = draw_search<DT>(sm.ds, r, t0, t1, target);
+    const int v = draw_search<DT>(sm.ds, r, target);
     if (tid == 0 && v >= 0) {
       p.final_token[b] = v;
       p.out_tokens[b * D1 + nacc] = v;

@@ -318,11 +318,20 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
   // completes exactly when all kUnit stages of the unit have been read.  The
   // temperature of the warp's next stage is loaded one iteration ahead.
   const long long n_stages_local = n_local * kUnit;
+  const int gamma = p.R - 1;
   auto unit_row = [&](long long c) -> int {
     const long long g = first + (c / kUnit) * stride;
     return (int)(g / upr);
   };
-  float T_next = (warp < n_stages_local) ? __ldg(p.temperature + unit_row(warp) / p.R) : 0.0f;
+  // temperature and drafted token of a row, loaded one iteration ahead
+  auto row_token = [&](int row) -> int {
+    if (p.tokens == nullptr) return -1;
+    const int b = row / p.R, i = row - b * p.R;
+    return (i < gamma) ? __ldg(p.tokens + (long long)b * gamma + i) : -1;
+  };
+  int row_next = (warp < n_stages_local) ? unit_row(warp) : 0;
+  float T_next = (warp < n_stages_local) ? __ldg(p.temperature + row_next / p.R) : 0.0f;
+  int x_next = (warp < n_stages_local) ? row_token(row_next) : -1;
   for (long long c = warp; c < n_stages_local; c += kConsumerWarps) {
     const long long i = c / kUnit;
     const int t = (int)(c - i * kUnit);
@@ -332,8 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
     const uint32_t slot = (uint32_t)(i % kSlots);
     const uint32_t use = (uint32_t)(i / kSlots);
     const float T = T_next;
-    if (c + kConsumerWarps < n_stages_local)
-      T_next = __ldg(p.temperature + unit_row(c + kConsumerWarps) / p.R);
+    const int x = x_next;
+    if (c + kConsumerWarps < n_stages_local) {
+      row_next = unit_row(c + kConsumerWarps);
+      T_next = __ldg(p.temperature + row_next / p.R);
+      x_next = row_token(row_next);
+    }
     const bool real = t < u.nst;
 
     LaneData<DT> d;
@@ -354,6 +367,28 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
     if (!ok) sm.abort_flag = 1;
     const int sbytes = max(0, min(kStageBytes, u.bytes - t * kStageBytes));
     if (ok && real) load_lane<DT>(d, sm.stage[slot] + t * kStageBytes, sbytes / 16, lane);
+    if (ok && real && lane == 0 && x >= 0 && x < p.V) {
+      // gather the drafted token's logit (from this stage, or from global for
+      // an edge element) and its q value
+      const int se0 = u.elem0 + t * (kStageBytes / es);
+      const int sel = sbytes / es;
+      const bool in_stage = x >= se0 && x < se0 + sel;
+      const bool in_edge = (u.j0 + t == 0) && (x < u.head_end || x >= u.tail_begin);
+      if (in_stage || in_edge) {
+        const long long roff = (long long)row * p.V;
+        float lx;
+        if (in_stage) {
+          const uint8_t *src = sm.stage[slot] + t * kStageBytes + (size_t)(x - se0) * es;
+          lx = (DT == SPECDEC_F32) ? *reinterpret_cast<const float *>(src)
+                                   : __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t *>(src)) << 16);
+        } else {
+          lx = load_elem(p.logits, DT, roff + x);
+        }
+        const int b = row / p.R, ri = row - b * p.R;
+        const float qx = load_elem(p.q, DT, ((long long)b * gamma + ri) * p.V + x);
+        p.gather[row] = make_float2(lx, qx);
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[slot]);  // this stage is in registers now
     if (!real) continue;

@@ -88,8 +88,10 @@ def test_argument_checks_before_any_device_work(lib):
     assert vt(N, N, BF16, N, N, N, N, 2, 2000, 1000, 5, N, N, N, N, N, N, N, N, 0, N) == 2
     assert vt(N, N, BF16, N, N, N, N, 2, 64, 1000, 65, N, N, N, N, N, N, N, N, 0, N) == 2
     rs = lib.specdec_row_stats
-    assert rs(N, BF16, N, 0, 9, 1000, N, 0, N) == 0
-    assert rs(N, BF16, N, 2, 9, 1000, N, 0, N) == 1
+    assert rs(N, N, BF16, N, N, 0, 9, 1000, N, 0, N) == 0
+    assert rs(N, N, BF16, N, N, 2, 9, 1000, N, 0, N) == 1
+    # q without draft tokens (or the reverse) is rejected
+    assert rs(d, d, BF16, N, d, 2, 9, 1000, d, 1 << 30, N) == 1
 
 
 def test_binding_refuses_to_run_without_the_library(tmp_path):

@@ -169,7 +169,7 @@ def test_deterministic_and_phase_split_agree(oracle_lib):
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         out = binding.LinearOut.empty(w.B, w.gamma, "cuda")
-        binding.row_stats(logits, temp, ws, stream=s)
+        binding.row_stats(logits, temp, ws, q=q, draft_tokens=toks, stream=s)
         binding.linear_finalize(logits, q, toks, temp, uni, out, ws, stream=s)
     s.synchronize()
     torch.cuda.synchronize()
