@@ -70,6 +70,7 @@ extern "C" {
 #define SPECDEC_ERR_UNSUPPORTED 2 /* sizes beyond the documented limits */
 #define SPECDEC_ERR_WORKSPACE 3   /* workspace missing or too small */
 #define SPECDEC_ERR_CUDA 4        /* a CUDA runtime call or launch failed */
+#define SPECDEC_ERR_STATIC_LIMIT 5 /* sizes need more scratch than specdec_verify_linear_static has */
 
 /* per-request status bits written to row_status[b] */
 #define SPECDEC_ROW_OK 0
@@ -180,6 +181,34 @@ int specdec_verify_tree(const void *logits, const void *q, int dtype,
                         int32_t *out_tokens, int32_t *final_token, uint8_t *is_bonus,
                         int32_t *row_status, float *p_node, void *workspace,
                         size_t workspace_bytes, void *stream);
+
+/*
+ * Linear verify that allocates nothing and takes no workspace.
+ *
+ * No counterpart in the method description: an addition of this library for
+ * callers that cannot allocate device memory for a workspace -- for example a
+ * host runtime that forbids allocation after start-up, or a plug-in interface
+ * whose calls carry only the inputs and outputs.  The scratch lives in a fixed
+ * device array inside the library, SPECDEC_STATIC_SCRATCH_BYTES long, which
+ * every GPU that loads the library holds until the process exits.
+ *
+ * Same arguments and outputs as specdec_verify_linear, without the workspace.
+ * Returns SPECDEC_ERR_STATIC_LIMIT, launching nothing, when
+ * specdec_workspace_size(B, gamma+1, V, dtype) exceeds the array.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before capturing a stream into a
+ * graph.  All calls share the one array: calls whose work overlaps on the GPU
+ * (different streams without ordering, or different host threads) race and
+ * corrupt each other's results; serialise them.  Nothing in the array needs
+ * to start at zero.
+ */
+#define SPECDEC_STATIC_SCRATCH_BYTES (4u << 20)
+int specdec_verify_linear_static(const void *logits, const void *q, int dtype,
+                                 const int32_t *draft_tokens, const float *temperature,
+                                 const float *uniforms, int B, int gamma, int V,
+                                 int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
+                                 uint8_t *is_bonus, int32_t *row_status, float *p_draft,
+                                 void *stream);
 
 /* Phase 2 of the tree form (phase 1 is specdec_row_stats with rows_per_request = N). */
 int specdec_tree_finalize(const void *logits, const void *q, int dtype,

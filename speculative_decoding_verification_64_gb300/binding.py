@@ -49,6 +49,9 @@ _EXPORTS = {
                             [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 +
                             [ctypes.c_void_p] * 8 + [ctypes.c_size_t, ctypes.c_void_p],
                             ctypes.c_int),
+    "specdec_verify_linear_static": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
+                                     [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 +
+                                     [ctypes.c_void_p] * 7, ctypes.c_int),
     "specdec_tree_finalize": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
                               [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 +
                               [ctypes.c_void_p] * 8 + [ctypes.c_size_t, ctypes.c_void_p],

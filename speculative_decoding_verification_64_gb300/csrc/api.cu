@@ -90,6 +90,8 @@ const char *specdec_status_string(int code) {
     case SPECDEC_ERR_UNSUPPORTED: return "sizes beyond the supported limits";
     case SPECDEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case SPECDEC_ERR_CUDA: return "CUDA runtime or launch error";
+    case SPECDEC_ERR_STATIC_LIMIT:
+      return "sizes need more scratch than the fixed array of specdec_verify_linear_static";
     default: break;
   }
   return "unknown status";
