@@ -31,7 +31,8 @@
  *     counter-based generator); the library draws no random numbers;
  *   - the library allocates nothing; scratch lives in a caller-provided
  *     workspace of at least specdec_workspace_size(...) bytes (no
- *     initialisation needed, contents are overwritten);
+ *     initialisation needed: every call writes what it later reads).  Calls
+ *     that share a workspace must not overlap on the GPU;
  *   - `stream` is a cudaStream_t (NULL = legacy default stream); work is
  *     asynchronous and stream-ordered; inputs are read only; outputs are
  *     overwritten entirely;
@@ -130,21 +131,23 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
  * into the workspace as per-stage partials (max, base-2 exponential sum,
  * first arg-max position).  One streaming pass over the logits.
  *   logits        [B, rows_per_request, V], temperature float32 [B]
- *   q, draft_tokens  linear form: [B, rows_per_request-1, V] and int32
- *                 [B, rows_per_request-1]; the pass also gathers each drafted
- *                 token's logit and q value for phase 2.  Both NULL for the
- *                 tree form or for statistics alone.
+ *   q, draft_tokens  linear form: [B, gamma, V] and int32 [B, gamma] with
+ *                 gamma = rows_per_request - 1; the pass then also gathers
+ *                 each drafted token's logit and q value for phase 2.  Both
+ *                 NULL for the tree form or for the statistics alone; one
+ *                 without the other is SPECDEC_ERR_INVALID_ARG.
  */
 int specdec_row_stats(const void *logits, const void *q, int dtype, const int32_t *draft_tokens,
                       const float *temperature, int B, int rows_per_request, int V,
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Phase 2 of the linear form: merge the row statistics in the workspace,
- * run the accept test with early stop (section 15.1.2 step 3) and the
- * correction / bonus draw (step 4).  Same arguments as specdec_verify_linear;
- * the workspace must hold phase 1's result for the same logits, q,
- * draft_tokens, B, gamma, V (phase 1 called with q and draft_tokens).
+ * Phase 2 of the linear form: the accept test with early stop (section
+ * 15.1.2 step 3), the correction / bonus draw (step 4) and every output.
+ * Same arguments as specdec_verify_linear; the workspace must hold phase 1's
+ * result for the same logits, q, draft_tokens, temperature, B, gamma, V
+ * (phase 1 called in its linear form).  Phase 2 leaves that result intact, so
+ * it may run again on it (with other uniforms, for instance).
  */
 int specdec_linear_finalize(const void *logits, const void *q, int dtype,
                             const int32_t *draft_tokens, const float *temperature,

@@ -15,24 +15,36 @@ int elem_bytes(int dtype) { return dtype == SPECDEC_F32 ? 4 : 2; }
 bool dtype_ok(int dtype) { return dtype == SPECDEC_F32 || dtype == SPECDEC_BF16; }
 
 // Workspace regions, each 256-byte aligned: the stage partials of the stats
-// pass, the gathered (logit, q) of every drafted token, one decision record
-// per request, and the fixed-point chunk totals of the draw.
+// pass; for the linear form the gathered (logit, q) of every drafted token,
+// p_i(x~_i), one decision record per request, the fixed-point chunk totals of
+// the draw and two ticket counters per request (zero between calls).
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t part, gather, dec, chunk, total;
+  size_t gather, chunk, draw_cnt, total;
 };
 
+// Stage partials first (the tree form uses only these), then the linear
+// form's gathered values, draw chunk totals and tickets.
 WsLayout workspace_layout(long long B, int R, int V, int dtype) {
   const long long rows = B * (long long)R;
   WsLayout w;
-  w.part = 0;
   w.gather = align256((size_t)rows * (size_t)stages_per_row(V, elem_bytes(dtype)) *
                       sizeof(RowPartial));
-  w.dec = w.gather + align256((size_t)rows * sizeof(float2));
-  w.chunk = w.dec + align256((size_t)B * sizeof(LinearDecision));
-  w.total = w.chunk + align256((size_t)B * draw_chunks(V) * sizeof(unsigned long long));
+  w.chunk = w.gather + align256((size_t)rows * sizeof(float2));
+  w.draw_cnt = w.chunk + align256((size_t)B * draw_chunks(V) * sizeof(unsigned long long));
+  w.total = w.draw_cnt + align256((size_t)B * sizeof(unsigned int));
   return w;
+}
+
+LinearWs linear_ws(void *workspace, long long B, int R, int V, int dtype) {
+  const WsLayout w = workspace_layout(B, R, V, dtype);
+  uint8_t *base = reinterpret_cast<uint8_t *>(workspace);
+  LinearWs ws;
+  ws.gather = reinterpret_cast<float2 *>(base + w.gather);
+  ws.chunk_tot = reinterpret_cast<unsigned long long *>(base + w.chunk);
+  ws.draw_cnt = reinterpret_cast<unsigned int *>(base + w.draw_cnt);
+  return ws;
 }
 
 size_t workspace_bytes_for(long long B, int R, int V, int dtype) {
@@ -61,7 +73,6 @@ int launch_stats(const void *logits, const void *q, int dtype, const int32_t *to
                  cudaStream_t stream) {
   const long long rows = (long long)B * R;
   const int spr = stages_per_row(V, elem_bytes(dtype));
-  const WsLayout w = workspace_layout(B, R, V, dtype);
   RowStatsParams p;
   p.logits = logits;
   p.temperature = temperature;
@@ -71,9 +82,10 @@ int launch_stats(const void *logits, const void *q, int dtype, const int32_t *to
   p.R = R;
   p.V = V;
   p.spr = spr;
-  p.tokens = (q != nullptr) ? tokens : nullptr;
+  p.B = B;
+  p.tokens = tokens;
   p.q = q;
-  p.gather = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(workspace) + w.gather);
+  p.ws = linear_ws(workspace, B, R, V, dtype);
   return cuda_status(launch_row_stats(p, stream));
 }
 
@@ -109,12 +121,15 @@ int specdec_row_stats(const void *logits, const void *q, int dtype, const int32_
   if (st != SPECDEC_OK) return st;
   if (B == 0) return SPECDEC_OK;
   if (!logits || !temperature) return SPECDEC_ERR_INVALID_ARG;
-  if ((q == nullptr) != (draft_tokens == nullptr)) return SPECDEC_ERR_INVALID_ARG;
-  if (q != nullptr && rows_per_request < 2) return SPECDEC_ERR_INVALID_ARG;
+  const int linear = (q != nullptr) + (draft_tokens != nullptr);
+  if (linear == 1) return SPECDEC_ERR_INVALID_ARG;
+  if (linear && (rows_per_request < 2 || rows_per_request - 1 > SPECDEC_MAX_GAMMA))
+    return SPECDEC_ERR_INVALID_ARG;
   st = check_workspace(workspace, workspace_bytes, B, rows_per_request, V, dtype);
   if (st != SPECDEC_OK) return st;
-  return launch_stats(logits, q, dtype, draft_tokens, temperature, B, rows_per_request, V,
-                      workspace, static_cast<cudaStream_t>(stream));
+  return launch_stats(logits, linear ? q : nullptr, dtype, linear ? draft_tokens : nullptr,
+                      temperature, B, rows_per_request, V, workspace,
+                      static_cast<cudaStream_t>(stream));
 }
 
 static int linear_checks(const void *logits, const void *q, int dtype, const int32_t *tokens,
@@ -152,11 +167,7 @@ static int linear_finalize_launch(const void *logits, const void *q, int dtype,
   p.is_bonus = is_bonus;
   p.row_status = row_status;
   p.p_draft = p_draft;
-  const WsLayout w = workspace_layout(B, gamma + 1, V, dtype);
-  uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
-  p.dec = reinterpret_cast<LinearDecision *>(ws + w.dec);
-  p.gather = reinterpret_cast<const float2 *>(ws + w.gather);
-  p.chunk_tot = reinterpret_cast<unsigned long long *>(ws + w.chunk);
+  p.ws = linear_ws(workspace, B, gamma + 1, V, dtype);
   p.dtype = dtype;
   p.B = B;
   p.gamma = gamma;

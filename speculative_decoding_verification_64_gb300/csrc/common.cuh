@@ -41,6 +41,29 @@ inline int stages_per_row(int V, int elem_bytes) {
 // ---------------------------------------------------------------------------
 // kernel parameter blocks
 // ---------------------------------------------------------------------------
+// Per-request decision of the linear accept test, made by the stats pass and
+// read by the draw (phase 2).
+// The outcome of one request's accept test, built in shared memory by every
+// CTA of the draw kernel from the stats pass's partials.
+struct LinearDecision {
+  int32_t k;       // first rejected position (gamma: all accepted)
+  int32_t status;  // SPECDEC_ROW_* bits; nonzero: nothing to draw
+  int32_t greedy;  // T == 0: the final token is `arg`
+  int32_t arg;     // first arg-max of the final row (greedy requests)
+  float M;         // max of the final row
+  float S;         // sum of 2^((l - M) c) over the final row
+  float c;         // log2(e) / T
+  int32_t pad;
+};
+
+// Linear-form workspace records shared by the two phases (device pointers
+// into the caller's workspace).
+struct LinearWs {
+  float2 *gather;                // [B*R] (l_i(x~_i), q_i(x~_i)) of row i < gamma
+  unsigned long long *chunk_tot; // [B, nchunk] fixed-point chunk sums of the draw
+  unsigned int *draw_cnt;        // [B] chunks done (ticket of the draw); the stats pass zeroes it
+};
+
 struct RowStatsParams {
   const void *logits;
   const float *temperature;
@@ -48,27 +71,14 @@ struct RowStatsParams {
   long long stages;  // rows * spr
   int dtype;
   int R, V, spr;     // rows per request, vocabulary, stages per row
+  int B;
   // Linear form only (tokens == nullptr otherwise): row i < R - 1 of request b
-  // scores draft token tokens[b * (R - 1) + i]; the pass stores that token's
-  // logit and its q value in gather[row] (left unwritten if the token is out
-  // of range).
+  // scores draft token tokens[b * (R - 1) + i].  The pass gathers that token's
+  // logit and q value and zeroes the draw kernel's tickets.
   const int32_t *tokens;
   const void *q;
-  float2 *gather;
+  LinearWs ws;
 };
-
-// Per-request decision of the linear accept test, handed from the decide
-// kernel to the draw kernel through the workspace (after the partials).
-struct LinearDecision {
-  int32_t k;       // first rejected position (gamma: all accepted)
-  int32_t status;  // SPECDEC_ROW_* bits; nonzero: nothing to draw
-  int32_t greedy;  // T == 0: final token already written
-  float M;         // max of the final row
-  float S;         // sum of 2^((l - M) c) over the final row
-  float c;         // log2(e) / T
-  int32_t pad[2];
-};
-static_assert(sizeof(LinearDecision) == 32, "LinearDecision is 32 bytes");
 
 struct LinearFinalizeParams {
   const void *logits;
@@ -83,9 +93,7 @@ struct LinearFinalizeParams {
   uint8_t *is_bonus;
   int32_t *row_status;
   float *p_draft;
-  LinearDecision *dec;
-  const float2 *gather;          // (l_i(x~_i), q_i(x~_i)) per row, from the stats pass
-  unsigned long long *chunk_tot; // [B, nchunk] fixed-point chunk sums of the draw
+  LinearWs ws;
   int dtype, B, gamma, V, spr, nchunk;
 };
 
@@ -108,6 +116,8 @@ struct TreeFinalizeParams {
 };
 
 // host launchers (defined in the .cu files)
+// Multiprocessor count of the current device (looked up once per device).
+int device_sm_count();
 cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream);
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream);
 cudaError_t launch_tree_finalize(const TreeFinalizeParams &p, cudaStream_t stream);
@@ -148,10 +158,74 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   return r;
 }
 
+// Merged statistics of one row.
+struct RowStat {
+  float M;    // row max of the raw logits (NaN if the row holds a NaN)
+  float S;    // sum of 2^((l - M) c)
+  int arg;    // first index holding M (greedy rows)
+  int flags;
+};
+
+__device__ __forceinline__ float ex2_approx(float x);
+
+// Merge of two stage partials (each sum is taken relative to its own max).
+__device__ __forceinline__ void merge2(float &m, float &s, int &a, float m2, float s2, int a2,
+                                       float c);
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ void merge2(float &m, float &s, int &a, float m2, float s2, int a2,
+                                       float c) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    a = a2;
+    return;
+  }
+  const float M = fmax_nan(m, m2);
+  const float f1 = ex2_approx((m - M) * c);
+  const float f2 = ex2_approx((m2 - M) * c);
+  a = (m > m2) ? a : (m2 > m) ? a2 : min(a, a2);
+  s = s * f1 + s2 * f2;
+  m = M;
+}
+
+// A usable row: finite max within the logit bound and a finite positive sum.
+__device__ __forceinline__ bool row_usable(const RowStat &r) {
+  return r.M > -INFINITY && r.M <= kMaxLogit && r.S > 0.0f && r.S < INFINITY;
+}
+
+// Merge of all stage partials of one row by one warp: lane j takes partials
+// j, j + 32, ..., then a butterfly merge.  merge2 is symmetric in its operands,
+// so every lane ends with the same, bit-identical result.
+__device__ __forceinline__ RowStat warp_merge_row(const RowPartial *part, long long row, int spr,
+                                                  float c, int lane) {
+  const float4 *pr = reinterpret_cast<const float4 *>(part + row * (long long)spr);
+  float m = -INFINITY, s = 0.0f;
+  int a = 0x7FFFFFFF, fl = 0;
+  for (int j = lane; j < spr; j += 32) {
+    const float4 x = pr[j];
+    fl |= __float_as_int(x.w);
+    merge2(m, s, a, x.x, x.y, __float_as_int(x.z), c);
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, d);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, d);
+    const int a2 = __shfl_xor_sync(0xffffffffu, a, d);
+    merge2(m, s, a, m2, s2, a2, c);
+  }
+  RowStat r;
+  r.M = m;
+  r.S = s;
+  r.arg = a;
+  r.flags = __reduce_or_sync(0xffffffffu, fl);
+  return r;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

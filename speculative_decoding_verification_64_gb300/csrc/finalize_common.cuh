@@ -1,6 +1,5 @@
-// Pieces shared by the linear and tree finalize kernels: merging the stage
-// partials of a row, and the cluster-wide inverse-CDF draw over one
-// vocabulary row.
+// Pieces of the tree finalize kernel: the cluster-wide inverse-CDF draw over
+// one vocabulary row.
 //
 // Draw weights are kept in units of the row maximum: with
 //     e_v = 2^((l_v - M) c),  c = log2(e) / T    (e_v <= 1, e = 1 at the maximum),
@@ -32,61 +31,6 @@ constexpr int kTile = kThreads * kPerThread;
 constexpr int kBatch = 4;             // tiles whose loads are in flight together
 constexpr int kMaxTilesPerCta = ((SPECDEC_MAX_V + kG - 1) / kG + 15 + kTile - 1) / kTile;
 constexpr double kFixedUnit = 0x1p-40;  // value of one unit of the fixed-point sums
-
-struct RowStat {
-  float M;    // row max of the raw logits (NaN if the row holds a NaN)
-  float S;    // sum of 2^((l - M) c)
-  int arg;    // first index holding M (greedy rows)
-  int flags;
-};
-
-// Merge of two stage partials (each sum is taken relative to its own max).
-__device__ __forceinline__ void merge2(float &m, float &s, int &a, float m2, float s2, int a2,
-                                       float c) {
-  if (m2 == -INFINITY) return;
-  if (m == -INFINITY) {
-    m = m2;
-    s = s2;
-    a = a2;
-    return;
-  }
-  const float M = fmax_nan(m, m2);
-  const float f1 = ex2_approx((m - M) * c);
-  const float f2 = ex2_approx((m2 - M) * c);
-  a = (m > m2) ? a : (m2 > m) ? a2 : min(a, a2);
-  s = s * f1 + s2 * f2;
-  m = M;
-}
-
-// Warp-cooperative merge of one row's stage partials; every lane gets the result.
-__device__ __forceinline__ RowStat warp_merge_row(const RowPartial *part, long long row, int spr,
-                                                  float c, int lane) {
-  const RowPartial *pr = part + row * (long long)spr;
-  float m = -INFINITY, s = 0.0f;
-  int a = 0x7FFFFFFF, fl = 0;
-  for (int j = lane; j < spr; j += 32) {
-    const RowPartial x = pr[j];
-    fl |= x.flags;
-    merge2(m, s, a, x.m, x.s, x.arg, c);
-  }
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, d);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, d);
-    const int a2 = __shfl_xor_sync(0xffffffffu, a, d);
-    merge2(m, s, a, m2, s2, a2, c);
-  }
-  RowStat r;
-  r.M = m;
-  r.S = s;
-  r.arg = a;
-  r.flags = __reduce_or_sync(0xffffffffu, fl);
-  return r;
-}
-
-__device__ __forceinline__ bool row_usable(const RowStat &r) {
-  return r.M > -INFINITY && r.M <= kMaxLogit && r.S > 0.0f && r.S < INFINITY;
-}
 
 // p(x) from the merged row statistics (accept tests and the p outputs).
 __device__ __forceinline__ float target_prob(float lx, const RowStat &r, float c) {

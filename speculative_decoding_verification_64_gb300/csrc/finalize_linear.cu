@@ -1,30 +1,33 @@
-// Linear verify, phase 2: accept test with early stop and the final draw
-// ("Chapter 15: Decoding acceleration", section 15.1.2 steps 3 and 4; the
-// bonus draw from the last target row follows section 15.1.3's expected
-// count (1 - a^(g+1)) / (1 - a) of emitted tokens per step).
+// Linear verify, phase 2: the accept test and the final draw ("Chapter 15:
+// Decoding acceleration", section 15.1.2 steps 3 and 4: accept x~_i while
+// u_i <= min(1, p_i(x~_i) / q_i(x~_i)), stop at the first rejection and draw
+// its replacement from max(0, p - q) / Z; the bonus draw from the last target
+// row when every draft is accepted follows section 15.1.3's expected count
+// (1 - a^(g+1)) / (1 - a) of emitted tokens per step).
 //
-// Three short kernels, each fully parallel, so that no request waits on a
-// long chain of dependent steps:
+// One kernel, one CTA per (request, 8192-element chunk of its final row):
 //
-// decide: one CTA per request.  Its warps merge the stage partials of the
-//   request's rows in parallel; warp 0 takes the drafted tokens' logits and q
-//   values the stats pass gathered, runs the accept test, finds the first
-//   rejection k with a ballot and find-first-set, writes the accepted tokens
-//   and counts, and leaves a decision record (k, M, S of the final row).
-//   Greedy requests (T = 0) get their final token (the first arg-max) here.
+// * every CTA merges its request's row partials (16 lanes per row) and runs
+//   the accept test in one warp, lane i testing draft i with the logit and q
+//   value the stats pass gathered; a ballot gives the first rejection k.  All
+//   CTAs of a request compute the same decision bit for bit (same data, same
+//   instruction sequence), which costs a few KB of L2 reads per CTA and needs
+//   no cross-CTA handshake;
+// * the CTA of chunk 0 writes the request's outputs but the final token
+//   (accepted tokens and count, bonus flag, status, p_draft); greedy and
+//   malformed requests are complete with it;
+// * every CTA sums the draw weights of its chunk: with e_v = 2^((l_v - M) c),
+//   the weights are max(0, e_v - S q_v) = S max(0, p - q) after a rejection and
+//   e_v = S p for the bonus draw; each thread sums its 32 contiguous weights in
+//   float32 and the CTA adds the thread sums in 40-bit fixed point;
+// * the last CTA of a request to finish (an atomic ticket that the stats pass
+//   zeroed) scans the chunk totals, finds the chunk holding U * Z, recomputes
+//   that chunk's thread sums (the same arithmetic, the same order), scans
+//   them, and the thread holding the crossing finds the token among its 32
+//   weights.  Integer sums make the crossing exact for the weights computed.
 //
-// draw sums: one CTA per (request, 8192-element chunk of its final row).  With
-//   e_v = 2^((l_v - M) c), the weights are max(0, e_v - S q_v) = S max(0, p - q)
-//   after a rejection and e_v = S p for the bonus draw; each thread sums its 32
-//   contiguous weights in float32, and the CTA adds the thread sums in 40-bit
-//   fixed point into the chunk total.  Requests are taken in reverse order so
-//   the rows the stats pass read last, still in L2, come first.
-//
-// draw search: one CTA per request.  An exclusive scan of the chunk totals
-//   gives Z and the chunk holding U * Z; the CTA recomputes that chunk's thread
-//   sums (the same arithmetic, the same order), scans them, and the thread
-//   holding the crossing finds the token among its 32 weights.  Integer sums
-//   make the crossing exact for the weights the kernels compute.
+// Requests are taken in reverse order so that the rows the stats pass read
+// last, still in L2, come first.
 #include <cfloat>
 
 #include "common.cuh"
@@ -36,144 +39,11 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPerT = 32;                  // contiguous elements per thread
 constexpr int kChunk = kThreads * kPerT;   // elements per chunk (8192)
-constexpr int kMaxRows = SPECDEC_MAX_GAMMA + 1;
+#ifndef SPECDEC_DRAW_MIN_BLOCKS
+#define SPECDEC_DRAW_MIN_BLOCKS 4
+#endif
+constexpr int kMinBlocks = SPECDEC_DRAW_MIN_BLOCKS;  // resident CTAs per SM the registers allow
 static_assert(kChunk == SPECDEC_DRAW_CHUNK, "chunk size shared with the workspace layout");
-
-struct RowStat {
-  float M, S;
-  int arg, flags;
-};
-
-// Merge of two stage partials (each sum is taken relative to its own max).
-__device__ __forceinline__ void merge2(float &m, float &s, int &a, float m2, float s2, int a2,
-                                       float c) {
-  if (m2 == -INFINITY) return;
-  if (m == -INFINITY) {
-    m = m2;
-    s = s2;
-    a = a2;
-    return;
-  }
-  const float M = fmax_nan(m, m2);
-  const float f1 = ex2_approx((m - M) * c);
-  const float f2 = ex2_approx((m2 - M) * c);
-  a = (m > m2) ? a : (m2 > m) ? a2 : min(a, a2);
-  s = s * f1 + s2 * f2;
-  m = M;
-}
-
-__device__ __forceinline__ RowStat warp_merge_row(const RowPartial *part, long long row, int spr,
-                                                  float c, int lane) {
-  const RowPartial *pr = part + row * (long long)spr;
-  float m = -INFINITY, s = 0.0f;
-  int a = 0x7FFFFFFF, fl = 0;
-  for (int j = lane; j < spr; j += 32) {
-    const RowPartial x = pr[j];
-    fl |= x.flags;
-    merge2(m, s, a, x.m, x.s, x.arg, c);
-  }
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, d);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, d);
-    const int a2 = __shfl_xor_sync(0xffffffffu, a, d);
-    merge2(m, s, a, m2, s2, a2, c);
-  }
-  RowStat r;
-  r.M = m;
-  r.S = s;
-  r.arg = a;
-  r.flags = __reduce_or_sync(0xffffffffu, fl);
-  return r;
-}
-
-__device__ __forceinline__ bool row_usable(const RowStat &r) {
-  return r.M > -INFINITY && r.M <= kMaxLogit && r.S > 0.0f && r.S < INFINITY;
-}
-
-template <int DT>
-__global__ void __launch_bounds__(kThreads) linear_decide_kernel(const LinearFinalizeParams p) {
-  __shared__ RowStat rows[kMaxRows];
-  const long long b = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gamma = p.gamma, R = gamma + 1, V = p.V;
-
-  const float T = __ldg(p.temperature + b);
-  const bool greedy = (T == 0.0f);
-  const float c = temperature_scale(T);
-
-  int x = -1;
-  float u = 0.0f;
-  float2 g = make_float2(0.0f, 1.0f);
-  if (warp == 0 && lane < gamma) {
-    x = __ldg(p.tokens + b * gamma + lane);
-    u = __ldg(p.uniforms + b * R + lane);
-    if (x >= 0 && x < V) g = p.gather[b * R + lane];
-  }
-  for (int i = warp; i < R; i += kWarps) {
-    const RowStat r = warp_merge_row(p.part, b * R + i, p.spr, c, lane);
-    if (lane == 0) rows[i] = r;
-  }
-  __syncthreads();
-  if (warp != 0) return;
-
-  int status = temperature_valid(T) ? 0 : SPECDEC_ROW_BAD_TEMP;
-  for (int i = lane; i < R; i += 32) {
-    status |= rows[i].flags;
-    if (!row_usable(rows[i])) status |= SPECDEC_ROW_NONFINITE;
-  }
-  bool acc = true;
-  float pd = 0.0f;
-  if (lane < gamma) {
-    if (x < 0 || x >= V) {
-      status |= SPECDEC_ROW_BAD_TOKEN;
-    } else {
-      const float lx = g.x, qx = g.y;
-      if (!(qx > 0.0f) || qx == INFINITY) status |= SPECDEC_ROW_BAD_Q;
-      if (greedy) {
-        acc = (x == rows[lane].arg);
-        pd = acc ? 1.0f : 0.0f;
-      } else {
-        pd = exp2f((lx - rows[lane].M) * c) / rows[lane].S;
-        // u <= min(1, p/q)  <=>  u q <= p  for q > 0, u < 1 (exact products in float64)
-        acc = ((double)u * (double)qx <= (double)pd);
-      }
-    }
-  }
-  status = __reduce_or_sync(0xffffffffu, status);
-  const unsigned rej = __ballot_sync(0xffffffffu, lane < gamma && !acc);
-  const int k = rej ? (__ffs(rej) - 1) : gamma;
-  if (status) {
-    for (int j = lane; j < R; j += 32) p.out_tokens[b * R + j] = -1;
-    if (p.p_draft && lane < gamma) p.p_draft[b * gamma + lane] = __int_as_float(0x7fc00000);
-  } else {
-    for (int j = lane; j < R; j += 32) {
-      if (j < k) p.out_tokens[b * R + j] = __ldg(p.tokens + b * gamma + j);
-      else if (j > k) p.out_tokens[b * R + j] = -1;
-    }
-    if (p.p_draft && lane < gamma) p.p_draft[b * gamma + lane] = pd;
-  }
-  if (lane == 0) {
-    p.n_accepted[b] = status ? 0 : k;
-    p.is_bonus[b] = (uint8_t)(!status && k == gamma);
-    p.row_status[b] = status;
-    if (status) {
-      p.final_token[b] = -1;
-    } else if (greedy) {
-      p.final_token[b] = rows[k].arg;
-      p.out_tokens[b * R + k] = rows[k].arg;
-    }
-    LinearDecision d;
-    d.k = k;
-    d.status = status;
-    d.greedy = greedy;
-    d.M = rows[k].M;
-    d.S = rows[k].S;
-    d.c = c;
-    d.pad[0] = d.pad[1] = 0;
-    p.dec[b] = d;
-  }
-}
 
 // ---------------------------------------------------------------------------
 // the draw
@@ -206,73 +76,119 @@ __device__ __forceinline__ Draw make_draw(const LinearFinalizeParams &p, long lo
   return w;
 }
 
+// Elements are read 64 bytes (four 16-byte vectors) per array at a time: 32
+// bf16 or 16 float32 values.
 template <int DT>
-__device__ __forceinline__ float bits_to_f(uint32_t v) {
-  return (DT == SPECDEC_F32) ? __uint_as_float(v) : __uint_as_float(v << 16);
-}
+struct Sub {
+  static constexpr int kEs = (DT == SPECDEC_F32) ? 4 : 2;
+  static constexpr int kElems = 64 / kEs;
+  uint4 l[4], q[4];
 
-// The 32 weights of the elements [e, e + 32) (zero at and beyond V) and their
-// float32 sum in index order, as 40-bit fixed point.
-template <int DT>
-__device__ __forceinline__ unsigned long long thread_weights(const Draw &w, int e, float out[kPerT]) {
-  constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
-  constexpr int nvec = kPerT * es / 16;
-  uint32_t lw[kPerT], qw[kPerT];
-  if (w.vec_ok && e + kPerT <= w.V) {
-    uint4 lv[nvec], qv[nvec];
-    const uint4 *lp = reinterpret_cast<const uint4 *>(w.lrow + (size_t)e * es);
+  // the raw bits of element i (a compile-time index after unrolling)
+  __device__ __forceinline__ static uint32_t word(const uint4 (&v)[4], int j) {
+    const uint4 x = v[j >> 2];
+    return (j & 3) == 0 ? x.x : (j & 3) == 1 ? x.y : (j & 3) == 2 ? x.z : x.w;
+  }
+  __device__ __forceinline__ static float value(const uint4 (&v)[4], int i) {
+    if (DT == SPECDEC_F32) return __uint_as_float(word(v, i));
+    const uint32_t w = word(v, i >> 1);
+    return (i & 1) ? bf16_hi(w) : bf16_lo(w);
+  }
+
+  // Elements [e, e + kElems): 16-byte loads when aligned and inside the row,
+  // else element loads with l = -inf, q = 0 beyond V (weight 0 there).
+  __device__ __forceinline__ void load(const Draw &w, int e) {
+    if (w.vec_ok && e + kElems <= w.V) {
+      const uint4 *lp = reinterpret_cast<const uint4 *>(w.lrow + (size_t)e * kEs);
+      const uint4 *qp = reinterpret_cast<const uint4 *>(w.qrow + (size_t)e * kEs);
 #pragma unroll
-    for (int k = 0; k < nvec; ++k) lv[k] = __ldg(lp + k);
-    if (w.use_q) {
-      const uint4 *qp = reinterpret_cast<const uint4 *>(w.qrow + (size_t)e * es);
+      for (int k = 0; k < 4; ++k) l[k] = __ldg(lp + k);
 #pragma unroll
-      for (int k = 0; k < nvec; ++k) qv[k] = __ldg(qp + k);
+      for (int k = 0; k < 4; ++k) q[k] = w.use_q ? __ldg(qp + k) : make_uint4(0u, 0u, 0u, 0u);
+      return;
     }
+    uint32_t lw[16], qw[16];
 #pragma unroll
-    for (int k = 0; k < nvec; ++k) {
-      const uint32_t a[4] = {lv[k].x, lv[k].y, lv[k].z, lv[k].w};
-      const uint32_t bq[4] = {w.use_q ? qv[k].x : 0u, w.use_q ? qv[k].y : 0u,
-                              w.use_q ? qv[k].z : 0u, w.use_q ? qv[k].w : 0u};
+    for (int j = 0; j < 16; ++j) lw[j] = qw[j] = 0u;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        if (DT == SPECDEC_F32) {
-          lw[4 * k + t] = a[t];
-          qw[4 * k + t] = bq[t];
-        } else {
-          lw[8 * k + 2 * t] = a[t] & 0xFFFFu;
-          lw[8 * k + 2 * t + 1] = a[t] >> 16;
-          qw[8 * k + 2 * t] = bq[t] & 0xFFFFu;
-          qw[8 * k + 2 * t + 1] = bq[t] >> 16;
-        }
-      }
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < kPerT; ++k) {
-      const int v = e + k;
+    for (int i = 0; i < kElems; ++i) {
+      const int v = e + i;
       const bool in = v < w.V;
       if (DT == SPECDEC_F32) {
-        lw[k] = in ? __float_as_uint(__ldg(reinterpret_cast<const float *>(w.lrow) + v)) : 0xFF800000u;
-        qw[k] = (in && w.use_q) ? __float_as_uint(__ldg(reinterpret_cast<const float *>(w.qrow) + v)) : 0u;
+        lw[i] = in ? __float_as_uint(__ldg(reinterpret_cast<const float *>(w.lrow) + v)) : 0xFF800000u;
+        qw[i] = (in && w.use_q) ? __float_as_uint(__ldg(reinterpret_cast<const float *>(w.qrow) + v)) : 0u;
       } else {
-        lw[k] = in ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(w.lrow) + v) : 0xFF80u;
-        qw[k] = (in && w.use_q) ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(w.qrow) + v) : 0u;
+        const uint32_t lb = in ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(w.lrow) + v) : 0xFF80u;
+        const uint32_t qb = (in && w.use_q) ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(w.qrow) + v) : 0u;
+        lw[i >> 1] |= (i & 1) ? (lb << 16) : lb;
+        qw[i >> 1] |= (i & 1) ? (qb << 16) : qb;
       }
     }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      l[k] = make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+      q[k] = make_uint4(qw[4 * k], qw[4 * k + 1], qw[4 * k + 2], qw[4 * k + 3]);
+    }
   }
+
+  // weight of element i: e_v, or max(0, e_v - K q_v) after a rejection
+  __device__ __forceinline__ float weight(const Draw &w, int i) const {
+    const float ev = ex2_approx((value(l, i) - w.M) * w.c);
+    return w.use_q ? fmaxf(fmaf(-w.K, value(q, i), ev), 0.0f) : ev;
+  }
+};
+
+// The float32 sum, in index order, of the 32 weights of elements [e, e + 32)
+// (zero at and beyond V), as 40-bit fixed point.
+template <int DT>
+__device__ __forceinline__ unsigned long long thread_sum(const Draw &w, int e) {
+  constexpr int n = Sub<DT>::kElems;
   float s = 0.0f;
 #pragma unroll
-  for (int k = 0; k < kPerT; ++k) {
-    const float ev = ex2_approx((bits_to_f<DT>(lw[k]) - w.M) * w.c);
-    const float x = w.use_q ? fmaxf(fmaf(-w.K, bits_to_f<DT>(qw[k]), ev), 0.0f) : ev;
-    out[k] = (e + k < w.V) ? x : 0.0f;
-    s += out[k];
+  for (int h = 0; h < kPerT / n; ++h) {
+    Sub<DT> x;
+    x.load(w, e + h * n);
+#pragma unroll
+    for (int i = 0; i < n; ++i) s += x.weight(w, i);
   }
   return to_fixed40(s);
 }
 
-__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v,
-                                                            unsigned long long *red) {
+// The element of [e, e + 32) at which base + (running float32 sum, as in
+// thread_sum) first exceeds target.
+template <int DT>
+__device__ __forceinline__ int thread_find(const Draw &w, int e, unsigned long long base,
+                                           unsigned long long target) {
+  constexpr int n = Sub<DT>::kElems;
+  float run = 0.0f;
+#pragma unroll
+  for (int h = 0; h < kPerT / n; ++h) {
+    Sub<DT> x;
+    x.load(w, e + h * n);
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      run += x.weight(w, i);
+      if (base + to_fixed40(run) > target) return e + h * n + i;
+    }
+  }
+  return e + kPerT - 1;
+}
+
+// Shared-memory scratch of the block reductions, two buffers used in turn:
+// a buffer is written again only after a barrier that every reader of its
+// previous contents has passed.
+struct Red {
+  unsigned long long *buf;  // [2][kWarps]
+  int phase;
+  __device__ __forceinline__ unsigned long long *next() {
+    unsigned long long *r = buf + phase * kWarps;
+    phase ^= 1;
+    return r;
+  }
+};
+
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, Red &rr) {
+  unsigned long long *red = rr.next();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) v += shfl_xor_u64(v, d);
@@ -285,9 +201,9 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
 }
 
 // Exclusive block scan of one u64 per thread; also returns the block total.
-__device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long long v,
-                                                               unsigned long long *red,
+__device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long long v, Red &rr,
                                                                unsigned long long &total) {
+  unsigned long long *red = rr.next();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned long long inc = v;
 #pragma unroll
@@ -307,100 +223,277 @@ __device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long lon
   return pre + inc - v;
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kThreads) linear_draw_sums_kernel(const LinearFinalizeParams p) {
-  __shared__ unsigned long long red[kWarps];
-  const long long b = (long long)p.B - 1 - blockIdx.x / p.nchunk;
-  const int chunk = (int)(blockIdx.x % p.nchunk);
-  const LinearDecision d = p.dec[b];
-  if (d.status || d.greedy) return;
-  const Draw w = make_draw<DT>(p, b, d);
-  float out[kPerT];
-  const unsigned long long f = thread_weights<DT>(w, chunk * kChunk + threadIdx.x * kPerT, out);
-  const unsigned long long tot = block_sum_u64(f, red);
-  if (threadIdx.x == 0) p.chunk_tot[b * p.nchunk + chunk] = tot;
+constexpr int kSeg = 16;                     // lanes merging one row
+constexpr int kRowsPerRound = kThreads / kSeg;
+
+__device__ __forceinline__ float4 load_partial(const float4 *pr, int j, int spr, bool active) {
+  return (active && j < spr) ? pr[j] : make_float4(-INFINITY, 0.0f, __int_as_float(0x7FFFFFFF), 0.0f);
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kThreads) linear_draw_search_kernel(const LinearFinalizeParams p) {
-  __shared__ unsigned long long red[kWarps];
-  __shared__ unsigned long long s_base;
-  __shared__ int s_chunk;
-  const long long b = blockIdx.x;
-  const int tid = threadIdx.x;
-  const LinearDecision d = p.dec[b];
-  if (d.status || d.greedy) return;
-  Draw w = make_draw<DT>(p, b, d);
-  const int nch = p.nchunk;
-  float out[kPerT];
+// Merge of one row's partials by a 16-lane segment of a warp (both segments
+// of the warp take part in every shuffle; an idle segment merges nothing).
+// The first two partials of each lane are loaded before any arithmetic, so
+// that rows of up to 32 stages cost one memory round trip.
+__device__ __forceinline__ RowStat segment_merge_row(const RowPartial *part, long long row,
+                                                     bool active, int spr, float c, int sl) {
+  const float4 *pr = reinterpret_cast<const float4 *>(part + row * (long long)spr);
+  const float4 x0 = load_partial(pr, sl, spr, active);
+  const float4 x1 = load_partial(pr, sl + kSeg, spr, active);
+  float m = -INFINITY, s = 0.0f;
+  int a = 0x7FFFFFFF;
+  int fl = __float_as_int(x0.w) | __float_as_int(x1.w);
+  merge2(m, s, a, x0.x, x0.y, __float_as_int(x0.z), c);
+  merge2(m, s, a, x1.x, x1.y, __float_as_int(x1.z), c);
+  if (active) {
+    for (int j = sl + 2 * kSeg; j < spr; j += kSeg) {  // rows of more than 32 stages
+      const float4 x = pr[j];
+      fl |= __float_as_int(x.w);
+      merge2(m, s, a, x.x, x.y, __float_as_int(x.z), c);
+    }
+  }
+#pragma unroll
+  for (int d = kSeg / 2; d >= 1; d >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, d);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, d);
+    const int a2 = __shfl_xor_sync(0xffffffffu, a, d);
+    fl |= __shfl_xor_sync(0xffffffffu, fl, d);
+    merge2(m, s, a, m2, s2, a2, c);
+  }
+  RowStat r;
+  r.M = m;
+  r.S = s;
+  r.arg = a;
+  r.flags = fl;
+  return r;
+}
 
-  // chunk totals (recomputed with the target row's weights if the residual is empty)
-  unsigned long long mine = (tid < nch) ? p.chunk_tot[b * nch + tid] : 0ull;
+// Inputs of one lane's accept test: draft x~_i, its uniform, and the logit
+// and q value the stats pass gathered for it.
+struct DraftIn {
+  int x;
+  float u;
+  float2 g;
+};
+
+__device__ __forceinline__ DraftIn load_draft(const LinearFinalizeParams &p, long long b, int lane) {
+  DraftIn in;
+  in.x = -1;
+  in.u = 0.0f;
+  in.g = make_float2(0.0f, 1.0f);
+  if (lane < p.gamma) {
+    in.x = __ldg(p.tokens + b * p.gamma + lane);
+    in.u = __ldg(p.uniforms + b * (p.gamma + 1) + lane);
+    in.g = __ldg(p.ws.gather + b * (p.gamma + 1) + lane);  // meaningful for a valid x only
+  }
+  return in;
+}
+
+// The accept test of request b by warp 0 from the merged rows rs[0, R):
+// lane i < gamma tests draft i, a ballot gives the first rejection.  Lane
+// i's p_i(x~_i) is returned in pd (NaN for a malformed request).
+__device__ __forceinline__ LinearDecision decide(const LinearFinalizeParams &p, const DraftIn &in,
+                                                 float T, float c, const RowStat *rs, int lane,
+                                                 float &pd) {
+  const int gamma = p.gamma, R = gamma + 1, V = p.V;
+  const bool greedy = (T == 0.0f);
+  RowStat r0, r1;
+  r0.M = r1.M = -INFINITY;
+  r0.S = r1.S = 0.0f;
+  r0.arg = r1.arg = 0x7FFFFFFF;
+  r0.flags = r1.flags = 0;
+  if (lane < R) r0 = rs[lane];
+  if (lane + 32 < R) r1 = rs[lane + 32];
+  int status = temperature_valid(T) ? 0 : SPECDEC_ROW_BAD_TEMP;
+  if (lane < R) status |= r0.flags | (row_usable(r0) ? 0 : SPECDEC_ROW_NONFINITE);
+  if (lane + 32 < R) status |= r1.flags | (row_usable(r1) ? 0 : SPECDEC_ROW_NONFINITE);
+  bool acc = true;
+  pd = 0.0f;
+  if (lane < gamma) {
+    if (in.x < 0 || in.x >= V) {
+      status |= SPECDEC_ROW_BAD_TOKEN;
+    } else {
+      if (!(in.g.y > 0.0f) || in.g.y == INFINITY) status |= SPECDEC_ROW_BAD_Q;
+      if (greedy) {
+        acc = (in.x == r0.arg);
+        pd = acc ? 1.0f : 0.0f;
+      } else {
+        pd = exp2f((in.g.x - r0.M) * c) / r0.S;
+        // u <= min(1, p/q)  <=>  u q <= p  for q > 0, u < 1 (exact products in float64)
+        acc = ((double)in.u * (double)in.g.y <= (double)pd);
+      }
+    }
+  }
+  status = __reduce_or_sync(0xffffffffu, status);
+  if (status) pd = __int_as_float(0x7fc00000);
+  const unsigned rej = __ballot_sync(0xffffffffu, lane < gamma && !acc);
+  const int k = rej ? (__ffs(rej) - 1) : gamma;
+  const bool hi = k >= 32;  // statistics of the final row k, from the lane holding it
+  LinearDecision d;
+  d.k = k;
+  d.status = status;
+  d.greedy = greedy;
+  d.arg = __shfl_sync(0xffffffffu, hi ? r1.arg : r0.arg, k & 31);
+  d.M = __shfl_sync(0xffffffffu, hi ? r1.M : r0.M, k & 31);
+  d.S = __shfl_sync(0xffffffffu, hi ? r1.S : r0.S, k & 31);
+  d.c = c;
+  d.pad = 0;
+  return d;
+}
+
+struct DrawSmem {
+  unsigned long long red[2 * kWarps];
+  unsigned long long base;
+  int chunk, last;
+  RowStat rs[SPECDEC_MAX_GAMMA + 1];
+  LinearDecision dec;
+};
+
+// The accept test of request b by the whole CTA (rows merged by 16-lane
+// segments, the test in warp 0); the owner of chunk 0 also writes every
+// output but a drawn token.  Two barriers; the result is CTA-uniform.
+template <int DT>
+__device__ __forceinline__ LinearDecision request_decision(const LinearFinalizeParams &p,
+                                                           long long b, bool owns_chunk0,
+                                                           DrawSmem &sm) {
+  const int tid = threadIdx.x;
+  const int gamma = p.gamma, R = gamma + 1;
+  const float T = __ldg(p.temperature + b);
+  const DraftIn din = load_draft(p, b, tid);
+  const float c = temperature_scale(T);
+  for (int r0 = 0; r0 < R; r0 += kRowsPerRound) {
+    const int r = r0 + tid / kSeg;
+    if (r0 + (tid / 32) * (32 / kSeg) >= R) continue;  // both segments of this warp idle
+    const RowStat st = segment_merge_row(p.part, b * R + r, r < R, p.spr, c, tid % kSeg);
+    if (r < R && tid % kSeg == 0) sm.rs[r] = st;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    float pd;
+    const LinearDecision dd = decide(p, din, T, c, sm.rs, tid, pd);
+    if (tid == 0) sm.dec = dd;
+    if (owns_chunk0 && p.p_draft && tid < gamma) p.p_draft[b * gamma + tid] = pd;
+  }
+  __syncthreads();
+  const LinearDecision d = sm.dec;
+  if (owns_chunk0) {
+    const int k = d.k;
+    if (tid < R) {
+      int t = -1;
+      if (!d.status) {
+        if (tid < k) t = __ldg(p.tokens + b * gamma + tid);
+        else if (tid == k) t = d.arg;  // greedy; a drawn token is written by the search
+      }
+      if (d.status || tid != k || d.greedy) p.out_tokens[b * R + tid] = t;
+    }
+    if (tid == 0) {
+      p.n_accepted[b] = d.status ? 0 : k;
+      p.is_bonus[b] = (uint8_t)(!d.status && k == gamma);
+      p.row_status[b] = d.status;
+      if (d.status) p.final_token[b] = -1;
+      else if (d.greedy) p.final_token[b] = d.arg;
+    }
+  }
+  return d;
+}
+
+// The token of request b from its chunk totals (all chunks summed): the
+// chunk holding U * Z, then the thread of that chunk, then the element.
+template <int DT>
+__device__ __forceinline__ void request_search(const LinearFinalizeParams &p, long long b, int k,
+                                               Draw w, Red &rr, DrawSmem &sm) {
+  const int tid = threadIdx.x;
+  const int gamma = p.gamma, R = gamma + 1;
+  const int nch = p.nchunk;
+  static_assert(SPECDEC_MAX_V / kChunk <= kThreads, "one chunk total per thread");
+  unsigned long long mine = (tid < nch) ? __ldcg(p.ws.chunk_tot + b * nch + tid) : 0ull;
   unsigned long long Z;
-  unsigned long long pre = block_exscan_u64(mine, red, Z);
+  unsigned long long pre = block_exscan_u64(mine, rr, Z);
   if (Z == 0 && w.use_q) {
     // residual mass 0 (only by rounding): draw from p itself
     w.use_q = false;
-    __syncthreads();
     for (int ch = 0; ch < nch; ++ch) {
-      const unsigned long long f = thread_weights<DT>(w, ch * kChunk + tid * kPerT, out);
-      const unsigned long long t = block_sum_u64(f, red);
+      const unsigned long long t = block_sum_u64(thread_sum<DT>(w, ch * kChunk + tid * kPerT), rr);
       if (tid == ch) mine = t;
-      __syncthreads();
     }
-    pre = block_exscan_u64(mine, red, Z);
+    pre = block_exscan_u64(mine, rr, Z);
   }
-  const float U = __ldg(p.uniforms + b * (p.gamma + 1) + p.gamma);
+  const float U = __ldg(p.uniforms + b * R + gamma);
   const unsigned long long target = uniform_target(U, Z);
-  if (tid == 0) s_chunk = -1;
+  if (tid == 0) {
+    sm.chunk = -1;
+    p.ws.draw_cnt[b] = 0;  // phase 2 may run again on the same phase-1 result
+  }
   __syncthreads();
   if (tid < nch && pre <= target && target - pre < mine) {
-    s_chunk = tid;
-    s_base = pre;
+    sm.chunk = tid;
+    sm.base = pre;
   }
   __syncthreads();
-  const int ch = s_chunk;
+  const int ch = sm.chunk;
+  const unsigned long long base = sm.base;
   if (ch < 0) return;  // no weight at all: unreachable for a usable row
-  const unsigned long long base = s_base;
   const int e = ch * kChunk + tid * kPerT;
-  const unsigned long long f = thread_weights<DT>(w, e, out);
-  __syncthreads();
+  const unsigned long long fe = thread_sum<DT>(w, e);
   unsigned long long ctot;
-  const unsigned long long excl = base + block_exscan_u64(f, red, ctot);
-  if (excl <= target && target - excl < f) {
-    float run = 0.0f;
-    int v = e + kPerT - 1;
-#pragma unroll
-    for (int k = 0; k < kPerT; ++k) {
-      run += out[k];
-      if (excl + to_fixed40(run) > target) {
-        v = e + k;
-        break;
-      }
-    }
+  const unsigned long long excl = base + block_exscan_u64(fe, rr, ctot);
+  if (excl <= target && target - excl < fe) {
+    const int v = thread_find<DT>(w, e, excl, target);
     p.final_token[b] = v;
-    p.out_tokens[b * (p.gamma + 1) + d.k] = v;
+    p.out_tokens[b * R + k] = v;
   }
 }
 
+// Persistent: CTA i takes the items [n i / G, n (i + 1) / G) of the sequence
+// of (request, chunk) pairs, requests in reverse order, so that it decides
+// about one or two requests and sums several chunks of each.  A request's
+// chunks are counted on its ticket once per CTA; the CTA that completes the
+// count runs the search.
 template <int DT>
-cudaError_t launch_dt(const LinearFinalizeParams &p, cudaStream_t stream) {
-  linear_decide_kernel<DT><<<(unsigned)p.B, kThreads, 0, stream>>>(p);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  linear_draw_sums_kernel<DT><<<(unsigned)((long long)p.B * p.nchunk), kThreads, 0, stream>>>(p);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  linear_draw_search_kernel<DT><<<(unsigned)p.B, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+__global__ void __launch_bounds__(kThreads, kMinBlocks) linear_draw_kernel(const LinearFinalizeParams p) {
+  __shared__ DrawSmem sm;
+  const int tid = threadIdx.x;
+  Red rr{sm.red, 0};
+  const long long nch = p.nchunk;
+  const long long n = (long long)p.B * nch;
+  const long long lo = n * blockIdx.x / gridDim.x;
+  const long long hi = n * (blockIdx.x + 1) / gridDim.x;
+  for (long long t0 = lo; t0 < hi;) {
+    const long long rb = t0 / nch;
+    const long long t1 = min(hi, (rb + 1) * nch);
+    const long long b = (long long)p.B - 1 - rb;
+    const int c0 = (int)(t0 - rb * nch), c1 = (int)(t1 - rb * nch);
+    t0 = t1;
+    const LinearDecision d = request_decision<DT>(p, b, c0 == 0, sm);
+    if (d.status || d.greedy) continue;  // nothing to draw
+    const Draw w = make_draw<DT>(p, b, d);
+    for (int ch = c0; ch < c1; ++ch) {
+      const unsigned long long tot = block_sum_u64(thread_sum<DT>(w, ch * kChunk + tid * kPerT), rr);
+      if (tid == 0) p.ws.chunk_tot[b * nch + ch] = tot;
+    }
+    if (tid == 0) {
+      __threadfence();
+      sm.last = atomicAdd(p.ws.draw_cnt + b, (unsigned)(c1 - c0)) + (unsigned)(c1 - c0) == (unsigned)nch;
+    }
+    __syncthreads();
+    if (sm.last) {
+      __threadfence();
+      request_search<DT>(p, b, d.k, w, rr, sm);
+    }
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream) {
   if (p.B <= 0) return cudaSuccess;
-  return p.dtype == SPECDEC_F32 ? launch_dt<SPECDEC_F32>(p, stream)
-                                : launch_dt<SPECDEC_BF16>(p, stream);
+  const long long items = (long long)p.B * p.nchunk;
+  const long long slots = (long long)device_sm_count() * kMinBlocks;
+  const unsigned grid = (unsigned)(items < slots ? items : slots);
+  if (p.dtype == SPECDEC_F32)
+    linear_draw_kernel<SPECDEC_F32><<<grid, kThreads, 0, stream>>>(p);
+  else
+    linear_draw_kernel<SPECDEC_BF16><<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace specdec

@@ -22,7 +22,9 @@
 // arguments (l - m) c with packed fp32x2 add and multiply (l - m is exact for
 // bf16 inputs), one ex2 per element and packed adds,
 // reduces over the warp with shuffles and writes the stage's partial.
-// Consumer warps never wait on each other.  The unaligned edge
+// Consumer warps never wait on each other.  In the linear form the warp whose
+// stage holds a row's drafted token also records that token's logit and q
+// value, so that the accept test needs no second look at the rows.  The unaligned edge
 // elements of a row (< 16 bytes at each end) are read with plain loads by the
 // warp of the row's first stage.  Every wait is bounded in time.
 #include <cfloat>
@@ -306,6 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
           ++use;
         }
       }
+    } else if (p.tokens != nullptr) {
+      // idle lanes: zero the draw kernel's per-request tickets, which that
+      // kernel (launched after this one) counts up from zero
+      for (long long b = (long long)blockIdx.x * 31 + (lane - 1); b < p.B; b += (long long)gridDim.x * 31)
+        p.ws.draw_cnt[b] = 0u;
     }
     return;
   }
@@ -386,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
         }
         const int b = row / p.R, ri = row - b * p.R;
         const float qx = load_elem(p.q, DT, ((long long)b * gamma + ri) * p.V + x);
-        p.gather[row] = make_float2(lx, qx);
+        p.ws.gather[row] = make_float2(lx, qx);
       }
     }
     __syncwarp();
@@ -418,20 +425,6 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
   (void)kPerVec;
 }
 
-int g_sm_count[64];
-
-int sm_count_of_current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (g_sm_count[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-    g_sm_count[dev] = n;
-  }
-  return g_sm_count[dev];
-}
-
 template <int DT>
 cudaError_t launch_dt(const RowStatsParams &p, cudaStream_t stream) {
   static bool attr_set[64] = {};
@@ -446,7 +439,7 @@ cudaError_t launch_dt(const RowStatsParams &p, cudaStream_t stream) {
     attr_set[dev] = true;
   }
   const long long units = p.stages / p.spr * ((p.spr + kUnit - 1) / kUnit);
-  long long grid = sm_count_of_current_device();
+  long long grid = device_sm_count();
   if (grid > units) grid = units;
   row_stats_kernel<DT><<<(unsigned)grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
@@ -458,6 +451,22 @@ cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream) {
   if (p.stages <= 0) return cudaSuccess;
   return p.dtype == SPECDEC_F32 ? launch_dt<SPECDEC_F32>(p, stream)
                                 : launch_dt<SPECDEC_BF16>(p, stream);
+}
+
+namespace {
+int g_sm_count[64];
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
 }
 
 }  // namespace specdec

@@ -92,6 +92,7 @@ def test_argument_checks_before_any_device_work(lib):
     assert rs(N, N, BF16, N, N, 2, 9, 1000, N, 0, N) == 1
     # q without draft tokens (or the reverse) is rejected
     assert rs(d, d, BF16, N, d, 2, 9, 1000, d, 1 << 30, N) == 1
+    assert rs(d, N, BF16, d, d, 2, 9, 1000, d, 1 << 30, N) == 1
 
 
 def test_binding_refuses_to_run_without_the_library(tmp_path):

@@ -2,6 +2,8 @@
 
 Tolerances and the boundary-draw rule are in ``parity.py``.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -176,3 +178,45 @@ def test_deterministic_and_phase_split_agree(oracle_lib):
     for k in ("n_accepted", "out_tokens", "final_token", "is_bonus", "row_status", "p_draft"):
         assert torch.equal(getattr(a, k), getattr(b, k)), k
         assert torch.equal(getattr(a, k), getattr(out, k)), k
+
+
+@pytest.mark.parametrize("fill", [0x00, 0xFF, 0x5A])
+def test_workspace_needs_no_initialisation(oracle_lib, fill):
+    """Any workspace contents before a call give the same results, also when a
+    workspace sized for one shape is reused for another."""
+    import torch
+    from speculative_decoding_verification_64_gb300 import binding
+    big = W.make_workload("linear_b256_g8_v128256_bf16", B=40, V=30011)
+    small = W.make_workload("mixed_b512_g4_v152064_bf16", B=24, V=12347, seed_offset=3)
+    ws = binding.alloc_workspace(big.B, big.gamma + 1, big.V, binding.BF16)
+    for w in (big, small, big):
+        args = binding.linear_inputs_to_device(w)
+        want = binding.verify_linear(*args)
+        ws.fill_(fill)
+        got = binding.verify_linear(*args, workspace=ws)
+        torch.cuda.synchronize()
+        for k in ("n_accepted", "out_tokens", "final_token", "is_bonus", "row_status", "p_draft"):
+            assert torch.equal(getattr(want, k), getattr(got, k)), (w.name, fill, k)
+
+
+def test_phase_two_reruns_on_one_phase_one_result(oracle_lib):
+    """Phase 2 leaves phase 1's result intact: with fresh uniforms it gives what a
+    full call with those uniforms gives, and the oracle agrees."""
+    import torch
+    from speculative_decoding_verification_64_gb300 import binding
+    w = W.make_workload("linear_b256_g8_v128256_bf16", B=20, V=20011)
+    logits, q, toks, temp, uni = binding.linear_inputs_to_device(w)
+    ws = binding.alloc_workspace(w.B, w.gamma + 1, w.V, binding.BF16)
+    binding.row_stats(logits, temp, ws, q=q, draft_tokens=toks)
+    for seed in (1, 2, 3):
+        u2 = W.philox_uniforms(1000 + seed, (w.B, w.gamma + 1))
+        w2 = dataclasses.replace(w, uniforms=u2)
+        uni2 = torch.from_numpy(u2).to("cuda")
+        out = binding.LinearOut.empty(w.B, w.gamma, "cuda")
+        binding.linear_finalize(logits, q, toks, temp, uni2, out, ws)
+        full = binding.verify_linear(logits, q, toks, temp, uni2)
+        torch.cuda.synchronize()
+        for k in ("n_accepted", "out_tokens", "final_token", "is_bonus", "row_status", "p_draft"):
+            assert torch.equal(getattr(out, k), getattr(full, k)), (seed, k)
+        compare_linear(w2, {k: v.cpu().numpy() for k, v in vars(out).items()},
+                       oracle_lib.verify_linear_workload(w2))
