@@ -258,8 +258,12 @@ def run_ours(args, dist):
         inputs = binding.tree_inputs_to_device(w, device)
         gamma = w.N - 1
         units = w.B * (w.N - 1)
-    # two resident input sets, alternated step to step (each > L2 for the bench workloads)
-    sets = [inputs, tuple(t.clone() for t in inputs)]
+    # resident input sets used in turn, enough of them that a step's inputs were
+    # last touched at least 3 x L2 bytes of other inputs ago (two for the
+    # large workloads, many copies of the small ones)
+    set_bytes = sum(t.numel() * t.element_size() for t in inputs)
+    n_sets, l2_note = input_rotation(set_bytes)
+    sets = [inputs] + [tuple(t.clone() for t in inputs) for _ in range(n_sets - 1)]
     dt = binding.dtype_code(inputs[0])
     ws = binding.alloc_workspace(w.B, R, w.V, dt, device)
     out = (binding.LinearOut.empty(w.B, w.gamma, device) if linear
@@ -274,7 +278,7 @@ def run_ours(args, dist):
             binding.row_stats(x[0], x[4], ws, stream=stream)
 
     def step(s):
-        x = sets[s & 1]
+        x = sets[s % n_sets]
         stats(x)
         if linear:
             binding.linear_finalize(*x, out, ws, stream=stream)
@@ -282,7 +286,7 @@ def run_ours(args, dist):
             binding.tree_finalize(*x, w.max_depth, out, ws, stream=stream)
 
     def step_timed(s, e0, e1, e2):
-        x = sets[s & 1]
+        x = sets[s % n_sets]
         e0.record(stream)
         stats(x)
         e1.record(stream)
@@ -358,7 +362,7 @@ def run_ours(args, dist):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic",
-        "config": _config(w, _workload_name(args), linear),
+        "config": _config(w, _workload_name(args), linear, l2_note),
         "requests_per_s": round(dist.sum(w.B, device) * K / (total_ms / 1e3), 1),
         "accepted_tokens_per_s": round(dist.sum(float(out.n_accepted.sum().item() + w.B), device)
                                        * K / (total_ms / 1e3), 1),
@@ -384,6 +388,17 @@ def _splits(lib, B, R, V, dt):
     return max(1, (ws // 16) // (B * R))
 
 
+L2_BYTES = 129_000_000  # GB300 L2
+
+
+def input_rotation(set_bytes: int):
+    """How many resident copies of a step's inputs to use in turn so that a
+    step's inputs were last touched at least 3 x L2 bytes of other inputs ago."""
+    n = max(2, -(-3 * L2_BYTES // set_bytes) + 1)
+    return n, (f"{n} resident input sets used in turn, {set_bytes * n / 1e6:.0f} MB in all; "
+               f"a step's inputs were last touched >= 3 x L2 ago")
+
+
 def _workload_name(args):
     name = args.workload
     if args.batch is not None or args.vocab is not None:
@@ -391,9 +406,16 @@ def _workload_name(args):
     return name
 
 
-def _config(w, name, linear):
-    c = {"workload": name, "B": w.B, "V": w.V, "dtype": w.dtype,
-         "l2": "inputs larger than L2 (two resident input sets alternated)"}
+def _host_set_bytes(w) -> int:
+    """Bytes of one step's inputs as the GPU arm holds them on the device."""
+    arrs = ([w.logits, w.q, w.draft_tokens, w.temperature, w.uniforms]
+            if isinstance(w, W.LinearWorkload)
+            else [w.logits, w.q, w.node_tokens, w.parent, w.temperature, w.uniforms])
+    return int(sum(a.nbytes for a in arrs))
+
+
+def _config(w, name, linear, l2_note):
+    c = {"workload": name, "B": w.B, "V": w.V, "dtype": w.dtype, "l2": l2_note}
     if linear:
         c["gamma"] = w.gamma
         c["greedy_requests"] = int((w.temperature == 0).sum())
@@ -516,7 +538,8 @@ def run_reference(args, dist):
         "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(w, _workload_name(args), linear), "impl": "reference",
+        "config": _config(w, _workload_name(args), linear, input_rotation(_host_set_bytes(w))[1]),
+        "impl": "reference",
         "cpu_baseline": {"value": round(value, 1), "unit": "positions/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": "positions/s", "h2d_bytes_per_step": 0,
