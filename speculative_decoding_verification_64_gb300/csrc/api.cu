@@ -32,7 +32,8 @@ WsLayout workspace_layout(long long B, int R, int V, int dtype) {
   w.gather = align256((size_t)rows * (size_t)stages_per_row(V, elem_bytes(dtype)) *
                       sizeof(RowPartial));
   w.chunk = w.gather + align256((size_t)rows * sizeof(float2));
-  w.draw_cnt = w.chunk + align256((size_t)B * draw_chunks(V) * sizeof(unsigned long long));
+  w.draw_cnt = w.chunk + align256((size_t)B * draw_total_slots(V, elem_bytes(dtype)) *
+                                  sizeof(unsigned long long));
   w.total = w.draw_cnt + align256((size_t)B * sizeof(unsigned int));
   return w;
 }
@@ -174,6 +175,7 @@ static int linear_finalize_launch(const void *logits, const void *q, int dtype,
   p.V = V;
   p.spr = stages_per_row(V, elem_bytes(dtype));
   p.nchunk = draw_chunks(V);
+  p.ntot = draw_total_slots(V, elem_bytes(dtype));
   return cuda_status(launch_linear_finalize(p, stream));
 }
 

@@ -28,10 +28,25 @@ static_assert(sizeof(RowPartial) == 16, "RowPartial is 16 bytes");
 #endif
 constexpr int kStageBytes = SPECDEC_STAGE_BYTES;
 
-// Elements per chunk of the linear draw (one CTA each).
+// Elements per chunk of the linear draw over rows that are not 16-byte aligned.
 #define SPECDEC_DRAW_CHUNK 8192
 
 inline int draw_chunks(int V) { return (V + SPECDEC_DRAW_CHUNK - 1) / SPECDEC_DRAW_CHUNK; }
+
+// Bytes of the final row per consumer stage of the linear draw over aligned
+// rows (bulk copies), and the stage count of a row.
+#define SPECDEC_DRAW_STAGE_BYTES 4096
+
+inline int draw_stages(int V, int elem_bytes) {
+  const long long b = (long long)V * elem_bytes;
+  return (int)((b + SPECDEC_DRAW_STAGE_BYTES - 1) / SPECDEC_DRAW_STAGE_BYTES);
+}
+
+// Fixed-point totals kept per request by either form of the draw.
+inline int draw_total_slots(int V, int elem_bytes) {
+  const int a = draw_chunks(V), b = draw_stages(V, elem_bytes);
+  return a > b ? a : b;
+}
 
 inline int stages_per_row(int V, int elem_bytes) {
   const long long b = (long long)V * elem_bytes;
@@ -41,8 +56,6 @@ inline int stages_per_row(int V, int elem_bytes) {
 // ---------------------------------------------------------------------------
 // kernel parameter blocks
 // ---------------------------------------------------------------------------
-// Per-request decision of the linear accept test, made by the stats pass and
-// read by the draw (phase 2).
 // The outcome of one request's accept test, built in shared memory by every
 // CTA of the draw kernel from the stats pass's partials.
 struct LinearDecision {
@@ -60,7 +73,7 @@ struct LinearDecision {
 // into the caller's workspace).
 struct LinearWs {
   float2 *gather;                // [B*R] (l_i(x~_i), q_i(x~_i)) of row i < gamma
-  unsigned long long *chunk_tot; // [B, nchunk] fixed-point chunk sums of the draw
+  unsigned long long *chunk_tot; // [B, draw_total_slots] fixed-point chunk / stage sums of the draw
   unsigned int *draw_cnt;        // [B] chunks done (ticket of the draw); the stats pass zeroes it
 };
 
@@ -95,6 +108,7 @@ struct LinearFinalizeParams {
   float *p_draft;
   LinearWs ws;
   int dtype, B, gamma, V, spr, nchunk;
+  int ntot;  // draw_total_slots(V, element bytes): row stride of ws.chunk_tot
 };
 
 struct TreeFinalizeParams {

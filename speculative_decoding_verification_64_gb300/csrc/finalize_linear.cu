@@ -405,7 +405,7 @@ __device__ __forceinline__ void request_search(const LinearFinalizeParams &p, lo
   const int gamma = p.gamma, R = gamma + 1;
   const int nch = p.nchunk;
   static_assert(SPECDEC_MAX_V / kChunk <= kThreads, "one chunk total per thread");
-  unsigned long long mine = (tid < nch) ? __ldcg(p.ws.chunk_tot + b * nch + tid) : 0ull;
+  unsigned long long mine = (tid < nch) ? __ldcg(p.ws.chunk_tot + b * p.ntot + tid) : 0ull;
   unsigned long long Z;
   unsigned long long pre = block_exscan_u64(mine, rr, Z);
   if (Z == 0 && w.use_q) {
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) linear_draw_kernel(const
     const Draw w = make_draw<DT>(p, b, d);
     for (int ch = c0; ch < c1; ++ch) {
       const unsigned long long tot = block_sum_u64(thread_sum<DT>(w, ch * kChunk + tid * kPerT), rr);
-      if (tid == 0) p.ws.chunk_tot[b * nch + ch] = tot;
+      if (tid == 0) p.ws.chunk_tot[b * p.ntot + ch] = tot;
     }
     if (tid == 0) {
       __threadfence();
@@ -482,10 +482,464 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) linear_draw_kernel(const
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// The draw over 16-byte aligned rows: bulk copies into shared memory and one
+// warp per 4 KB stage of the final row, after the row-statistics kernel's
+// pattern.  Persistent, one CTA per SM; CTA i takes a contiguous run of the
+// sequence of (request, 16 KB unit) pairs, requests in reverse order.
+//
+// * Head: 16-lane segments merge the partials of every row of the run's
+//   requests (at most kMaxReq), then warp j runs request j's accept test; the
+//   CTA holding a request's first unit writes its outputs.
+// * Pipeline: one producer thread copies each unit's logits (and, after a
+//   rejection, its q values) into a ring of kSlots slots; stage t of a unit
+//   goes to consumer warp (local stage index) mod kWarps.  A lane takes the
+//   16-byte vectors lane, lane + 32, ... of the stage, sums each vector's
+//   weights in float32 in index order and adds the sums as 40-bit fixed
+//   point; the warp's total is the stage total.  Vectors in index order are
+//   therefore the units of the inverse CDF above the float32 level.
+// * Tail: after a barrier, thread 0 adds the run's stage count of each
+//   request to the request's ticket; warp j searches request j if its count
+//   completed the ticket: stage, then vector (in index order), then element.
+// ---------------------------------------------------------------------------
+namespace bulk {
+
+constexpr int kStage = SPECDEC_DRAW_STAGE_BYTES;    // bytes of the final row per stage
+constexpr int kUnitStages = 4;
+constexpr int kUnitBytes = kStage * kUnitStages;    // one bulk copy of logits (+ one of q)
+constexpr int kSlots = 6;
+constexpr int kWarps = 12;                          // consumer warps
+constexpr int kThreads = (kWarps + 1) * 32;         // + the producer warp
+constexpr int kVec = kStage / 16 / 32;              // 16-byte vectors per lane per stage
+constexpr int kMaxReq = 8;                          // requests in one CTA's run
+constexpr unsigned kAbort = 1u << 24;               // ticket increment of a CTA whose wait ran out
+
+struct Smem {
+  alignas(128) uint8_t l[kSlots][kUnitBytes];
+  alignas(128) uint8_t q[kSlots][kUnitBytes];
+  alignas(8) uint64_t full[kSlots];
+  alignas(8) uint64_t empty[kSlots];
+  RowStat rs[kMaxReq][SPECDEC_MAX_GAMMA + 1];
+  LinearDecision dec[kMaxReq];
+  int search[kMaxReq];  // 0: not this CTA's; 1: search; 2: search, but a wait ran out somewhere
+  volatile int abort_flag;
+};
+
+// Weight of element i of a 16-byte vector: 2^((l - M) c), or max(0, that - S q)
+// after a rejection (the same arithmetic as the other form of the draw).
+template <int DT>
+__device__ __forceinline__ float vec_weight(const uint4 &lv, const uint4 &qv, int i,
+                                            const LinearDecision &d, bool use_q) {
+  float l, q;
+  if (DT == SPECDEC_F32) {
+    const uint32_t lw = (i == 0) ? lv.x : (i == 1) ? lv.y : (i == 2) ? lv.z : lv.w;
+    const uint32_t qw = (i == 0) ? qv.x : (i == 1) ? qv.y : (i == 2) ? qv.z : qv.w;
+    l = __uint_as_float(lw);
+    q = __uint_as_float(qw);
+  } else {
+    const int j = i >> 1;
+    const uint32_t lw = (j == 0) ? lv.x : (j == 1) ? lv.y : (j == 2) ? lv.z : lv.w;
+    const uint32_t qw = (j == 0) ? qv.x : (j == 1) ? qv.y : (j == 2) ? qv.z : qv.w;
+    l = (i & 1) ? bf16_hi(lw) : bf16_lo(lw);
+    q = (i & 1) ? bf16_hi(qw) : bf16_lo(qw);
+  }
+  const float ev = ex2_approx((l - d.M) * d.c);
+  return use_q ? fmaxf(fmaf(-d.S, q, ev), 0.0f) : ev;
+}
+
+template <int DT>
+__host__ __device__ constexpr int vec_elems() { return (DT == SPECDEC_F32) ? 4 : 8; }
+
+// float32 sum, in index order, of the weights of one vector
+template <int DT>
+__device__ __forceinline__ float vec_sum(const uint4 &lv, const uint4 &qv, const LinearDecision &d,
+                                         bool use_q) {
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < vec_elems<DT>(); ++i) s += vec_weight<DT>(lv, qv, i, d, use_q);
+  return s;
+}
+
+// the element of a vector at which base + (running sum, as in vec_sum) first exceeds target
+template <int DT>
+__device__ __forceinline__ int vec_find(const uint4 &lv, const uint4 &qv, const LinearDecision &d,
+                                        bool use_q, unsigned long long base,
+                                        unsigned long long target) {
+  float run = 0.0f;
+#pragma unroll
+  for (int i = 0; i < vec_elems<DT>(); ++i) {
+    run += vec_weight<DT>(lv, qv, i, d, use_q);
+    if (base + to_fixed40(run) > target) return i;
+  }
+  return vec_elems<DT>() - 1;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) v += shfl_xor_u64(v, d);
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v, int lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const unsigned long long y = shfl_up_u64(v, d);
+    if (lane >= d) v += y;
+  }
+  return v;
+}
+
+__host__ __device__ constexpr uint32_t kNegInfBits(int dt) { return dt == SPECDEC_F32 ? 0xFF800000u : 0xFF80FF80u; }
+
+// Vectors lane + 32 k of a stage of sbytes bytes (from shared or global
+// memory): -inf logits and zero q past the end, which weigh 0.
+template <int DT>
+__device__ __forceinline__ void load_stage(uint4 (&lv)[kVec], uint4 (&qv)[kVec], const uint8_t *l,
+                                           const uint8_t *q, int sbytes, bool use_q, int lane,
+                                           bool global) {
+  const uint32_t ninf = kNegInfBits(DT);
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) {
+    const int off = (lane + 32 * k) * 16;
+    const bool in = off < sbytes;
+    if (global) {
+      lv[k] = in ? __ldg(reinterpret_cast<const uint4 *>(l + off)) : make_uint4(ninf, ninf, ninf, ninf);
+      qv[k] = (in && use_q) ? __ldg(reinterpret_cast<const uint4 *>(q + off)) : make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      lv[k] = in ? *reinterpret_cast<const uint4 *>(l + off) : make_uint4(ninf, ninf, ninf, ninf);
+      qv[k] = (in && use_q) ? *reinterpret_cast<const uint4 *>(q + off) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+// Per-request view of the run: the request's index b, its row pointers and sizes.
+struct Req {
+  long long b;
+  const uint8_t *lrow, *qrow;
+  int rowbytes, nst;
+};
+
+template <int DT>
+__device__ __forceinline__ Req make_req(const LinearFinalizeParams &p, long long rb, int k) {
+  constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
+  Req r;
+  r.b = (long long)p.B - 1 - rb;
+  const int R = p.gamma + 1;
+  r.rowbytes = p.V * es;
+  r.nst = (r.rowbytes + kStage - 1) / kStage;
+  r.lrow = reinterpret_cast<const uint8_t *>(p.logits) + (size_t)(r.b * R + k) * r.rowbytes;
+  r.qrow = (k < p.gamma)
+               ? reinterpret_cast<const uint8_t *>(p.q) + (size_t)(r.b * p.gamma + k) * r.rowbytes
+               : r.lrow;
+  return r;
+}
+
+// Outputs of request b but a drawn token, by one warp.
+__device__ __forceinline__ void write_outputs_warp(const LinearFinalizeParams &p, long long b,
+                                                   const LinearDecision &d, float pd, int lane) {
+  const int gamma = p.gamma, R = gamma + 1, k = d.k;
+  if (p.p_draft && lane < gamma) p.p_draft[b * gamma + lane] = pd;
+  for (int i = lane; i < R; i += 32) {
+    int t = -1;
+    if (!d.status) {
+      if (i < k) t = __ldg(p.tokens + b * gamma + i);
+      else if (i == k) t = d.arg;
+    }
+    if (d.status || i != k || d.greedy) p.out_tokens[b * R + i] = t;
+  }
+  if (lane == 0) {
+    p.n_accepted[b] = d.status ? 0 : k;
+    p.is_bonus[b] = (uint8_t)(!d.status && k == gamma);
+    p.row_status[b] = d.status;
+    if (d.status) p.final_token[b] = -1;
+    else if (d.greedy) p.final_token[b] = d.arg;
+  }
+}
+
+// The search of one request by one warp (see the header of this section).
+template <int DT>
+__device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const Req &rq,
+                                            LinearDecision d, bool aborted, int lane) {
+  constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
+  const int gamma = p.gamma, R = gamma + 1;
+  const long long b = rq.b;
+  unsigned long long *tot = p.ws.chunk_tot + b * p.ntot;
+  if (lane == 0) p.ws.draw_cnt[b] = 0;  // phase 2 may run again on the same phase-1 result
+  if (aborted) {
+    // a bounded wait ran out in some CTA of this request: report, draw nothing
+    for (int i = lane; i < R; i += 32) p.out_tokens[b * R + i] = -1;
+    if (lane == 0) {
+      p.row_status[b] = SPECDEC_ROW_INTERNAL;
+      p.n_accepted[b] = 0;
+      p.is_bonus[b] = 0;
+      p.final_token[b] = -1;
+    }
+    return;
+  }
+  bool use_q = d.k < gamma;
+  unsigned long long Z = 0;
+  for (int s = lane; s < rq.nst; s += 32) Z += __ldcg(tot + s);
+  Z = warp_sum_u64(Z);
+  if (Z == 0 && use_q) {
+    // residual mass 0 (only by rounding): draw from p itself
+    use_q = false;
+    for (int s = 0; s < rq.nst; ++s) {
+      uint4 lv[kVec], qv[kVec];
+      load_stage<DT>(lv, qv, rq.lrow + (size_t)s * kStage, rq.qrow + (size_t)s * kStage,
+                     min(kStage, rq.rowbytes - s * kStage), false, lane, true);
+      unsigned long long acc = 0;
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) acc += to_fixed40(vec_sum<DT>(lv[k], qv[k], d, false));
+      acc = warp_sum_u64(acc);
+      if (lane == 0) tot[s] = acc;
+      Z += acc;
+    }
+    __syncwarp();
+  }
+  const float U = __ldg(p.uniforms + b * R + gamma);
+  const unsigned long long target = uniform_target(U, Z);
+  // the stage holding the crossing
+  unsigned long long base = 0;
+  int st = -1;
+  for (int s0 = 0; s0 < rq.nst && st < 0; s0 += 32) {
+    const unsigned long long v = (s0 + lane < rq.nst) ? __ldcg(tot + s0 + lane) : 0ull;
+    const unsigned long long incl = warp_incl_scan_u64(v, lane);
+    const unsigned m = __ballot_sync(0xffffffffu, target < base + incl);
+    if (m) {
+      const int ls = __ffs(m) - 1;
+      st = s0 + ls;
+      base += __shfl_sync(0xffffffffu, incl - v, ls);
+    } else {
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  if (st < 0) return;  // no weight at all: unreachable for a usable row
+  // the vector, in index order (vector lane + 32 k), then the element
+  uint4 lv[kVec], qv[kVec];
+  const int off = st * kStage;
+  load_stage<DT>(lv, qv, rq.lrow + off, rq.qrow + off, min(kStage, rq.rowbytes - off), use_q, lane,
+                 true);
+  int kx = -1, lx = -1;               // the crossing vector: lane lx's vector kx
+  unsigned long long vbase = 0;       // fixed-point sum before it (valid in lane lx)
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) {
+    const unsigned long long x = to_fixed40(vec_sum<DT>(lv[k], qv[k], d, use_q));
+    const unsigned long long incl = warp_incl_scan_u64(x, lane);
+    const unsigned m = __ballot_sync(0xffffffffu, target < base + incl);
+    if (kx < 0 && m) {
+      kx = k;
+      lx = __ffs(m) - 1;
+      vbase = base + incl - x;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (kx < 0 || lane != lx) return;
+  uint4 ls = lv[0], qs = qv[0];
+#pragma unroll
+  for (int k = 1; k < kVec; ++k) {
+    if (k == kx) {
+      ls = lv[k];
+      qs = qv[k];
+    }
+  }
+  const int e = vec_find<DT>(ls, qs, d, use_q, vbase, target);
+  const int v = off / es + (lane + 32 * kx) * vec_elems<DT>() + e;
+  p.final_token[b] = v;
+  p.out_tokens[b * R + d.k] = v;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFinalizeParams p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+  constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gamma = p.gamma, R = gamma + 1;
+  const int rowbytes = p.V * es;
+  const int nst = (rowbytes + kStage - 1) / kStage;
+  const int upr = (nst + kUnitStages - 1) / kUnitStages;  // units per row
+  const long long units = (long long)p.B * upr;
+  const long long lo = units * blockIdx.x / gridDim.x;
+  const long long hi = units * (blockIdx.x + 1) / gridDim.x;
+  const long long rb0 = lo / upr;
+  const int nreq = (hi > lo) ? (int)((hi - 1) / upr - rb0 + 1) : 0;  // <= kMaxReq (host check)
+
+  if (tid == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], kUnitStages);  // one arrival per stage of the unit
+    }
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+
+  // ---- head: row merges (16-lane segments over (request, row) pairs) ------
+  const int pairs = nreq * R;
+  for (int base = 0; base < pairs; base += kThreads / kSeg) {
+    if (base + warp * (32 / kSeg) >= pairs) continue;  // both segments of this warp idle
+    const int pr = base + tid / kSeg;
+    const bool active = pr < pairs;
+    const int j = active ? pr / R : 0, r = active ? pr - j * R : 0;
+    const long long b = (long long)p.B - 1 - (rb0 + j);
+    const float c = temperature_scale(__ldg(p.temperature + b));
+    const RowStat st = segment_merge_row(p.part, b * R + r, active, p.spr, c, tid % kSeg);
+    if (active && tid % kSeg == 0) sm.rs[j][r] = st;
+  }
+  __syncthreads();
+  // ---- head: accept tests, warp j for request j ----------------------------
+  if (warp < nreq) {
+    const long long rb = rb0 + warp;
+    const long long b = (long long)p.B - 1 - rb;
+    const float T = __ldg(p.temperature + b);
+    const DraftIn din = load_draft(p, b, lane);
+    float pd;
+    const LinearDecision d = decide(p, din, T, temperature_scale(T), sm.rs[warp], lane, pd);
+    if (lane == 0) sm.dec[warp] = d;
+    if (rb * upr >= lo) write_outputs_warp(p, b, d, pd, lane);  // this CTA holds unit 0
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      long long rb = rb0;
+      int ju = (int)(lo - rb0 * upr);
+      for (long long n = 0; lo + n < hi; ++n) {
+        const uint32_t slot = (uint32_t)(n % kSlots), use = (uint32_t)(n / kSlots);
+        if (use > 0 && !mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1)) {
+          sm.abort_flag = 1;
+          break;
+        }
+        if (sm.abort_flag) break;
+        const LinearDecision d = sm.dec[rb - rb0];
+        if (d.status || d.greedy) {
+          mbar_arrive(&sm.full[slot]);  // nothing to draw: an empty unit
+        } else {
+          const Req rq = make_req<DT>(p, rb, d.k);
+          const bool use_q = d.k < gamma;
+          const int bytes = min(kUnitBytes, rq.rowbytes - ju * kUnitBytes);
+          mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(bytes * (use_q ? 2 : 1)));
+          bulk_copy_g2s(sm.l[slot], rq.lrow + (size_t)ju * kUnitBytes, (uint32_t)bytes, &sm.full[slot]);
+          if (use_q)
+            bulk_copy_g2s(sm.q[slot], rq.qrow + (size_t)ju * kUnitBytes, (uint32_t)bytes, &sm.full[slot]);
+        }
+        if (++ju == upr) {
+          ju = 0;
+          ++rb;
+        }
+      }
+    }
+  } else {
+    // ------------------------------ consumers -----------------------------
+    const long long n_stages_local = (hi - lo) * kUnitStages;
+    for (long long cst = warp; cst < n_stages_local; cst += kWarps) {
+      const long long n = cst / kUnitStages;
+      const int t = (int)(cst - n * kUnitStages);
+      const long long i = lo + n;
+      const long long rb = i / upr;
+      const int ju = (int)(i - rb * upr);
+      const uint32_t slot = (uint32_t)(n % kSlots), use = (uint32_t)(n / kSlots);
+      const LinearDecision d = sm.dec[rb - rb0];
+      const int s = ju * kUnitStages + t;  // stage within the row
+      const bool real = !(d.status || d.greedy) && s < nst;
+      const bool use_q = d.k < gamma;
+      const bool ok = !sm.abort_flag && mbar_wait_bounded(&sm.full[slot], use & 1);
+      if (!ok) sm.abort_flag = 1;
+      uint4 lv[kVec], qv[kVec];
+      const int sbytes = (ok && real) ? min(kStage, rowbytes - s * kStage) : 0;
+      load_stage<DT>(lv, qv, sm.l[slot] + t * kStage, sm.q[slot] + t * kStage, sbytes, use_q, lane,
+                     false);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[slot]);  // this stage is in registers now
+      if (!real || !ok) continue;
+      unsigned long long acc = 0;
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) acc += to_fixed40(vec_sum<DT>(lv[k], qv[k], d, use_q));
+      acc = warp_sum_u64(acc);
+      if (lane == 0) p.ws.chunk_tot[((long long)p.B - 1 - rb) * p.ntot + s] = acc;
+    }
+  }
+  __syncthreads();
+
+  // ---- tail: tickets, then the searches --------------------------------------
+  if (tid == 0) {
+    __threadfence();
+    const unsigned abort_add = sm.abort_flag ? kAbort : 0u;
+    for (int j = 0; j < nreq; ++j) {
+      const LinearDecision d = sm.dec[j];
+      sm.search[j] = 0;
+      if (d.status || d.greedy) continue;
+      const long long rb = rb0 + j;
+      const long long u0 = max(lo, rb * upr), u1 = min(hi, (rb + 1) * upr);
+      const int s0 = (int)(u0 - rb * upr) * kUnitStages;
+      const int s1 = min(nst, (int)(u1 - rb * upr) * kUnitStages);
+      const unsigned add = (unsigned)(s1 - s0) + abort_add;
+      const long long b = (long long)p.B - 1 - rb;
+      const unsigned now = atomicAdd(p.ws.draw_cnt + b, add) + add;
+      if ((now & (kAbort - 1)) == (unsigned)nst) sm.search[j] = (now >= kAbort) ? 2 : 1;
+    }
+  }
+  __syncthreads();
+  if (warp < nreq && sm.search[warp]) {
+    __threadfence();
+    const LinearDecision d = sm.dec[warp];
+    search_warp<DT>(p, make_req<DT>(p, rb0 + warp, d.k), d, sm.search[warp] == 2, lane);
+  }
+}
+
+}  // namespace bulk
+
+}  // namespace
+
+namespace {
+
+// The bulk-copy draw needs 16-byte aligned rows (base pointers and row
+// length) and at most bulk::kMaxReq requests in any CTA's run.
+bool bulk_draw_applies(const LinearFinalizeParams &p, int grid) {
+  const int es = (p.dtype == SPECDEC_F32) ? 4 : 2;
+  const long long rowbytes = (long long)p.V * es;
+  if (rowbytes % 16 != 0) return false;
+  if ((reinterpret_cast<uintptr_t>(p.logits) & 15) || (reinterpret_cast<uintptr_t>(p.q) & 15))
+    return false;
+  const long long nst = (rowbytes + bulk::kStage - 1) / bulk::kStage;
+  const long long upr = (nst + bulk::kUnitStages - 1) / bulk::kUnitStages;
+  const long long units = (long long)p.B * upr;
+  const long long per_cta = (units + grid - 1) / grid;
+  return (per_cta + upr - 1) / upr + 1 <= bulk::kMaxReq;
+}
+
+template <int DT>
+cudaError_t launch_bulk(const LinearFinalizeParams &p, unsigned grid, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const int smem = (int)sizeof(bulk::Smem);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    err = cudaFuncSetAttribute(bulk::draw_bulk_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               smem);
+    if (err != cudaSuccess) return err;
+    attr_set[dev] = true;
+  }
+  bulk::draw_bulk_kernel<DT><<<grid, bulk::kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream) {
   if (p.B <= 0) return cudaSuccess;
+  {
+    const int es = (p.dtype == SPECDEC_F32) ? 4 : 2;
+    const long long nst = ((long long)p.V * es + bulk::kStage - 1) / bulk::kStage;
+    const long long units = (long long)p.B * ((nst + bulk::kUnitStages - 1) / bulk::kUnitStages);
+    const long long sms = device_sm_count();
+    const int grid = (int)(units < sms ? units : sms);
+    if (bulk_draw_applies(p, grid))
+      return (p.dtype == SPECDEC_F32) ? launch_bulk<SPECDEC_F32>(p, (unsigned)grid, stream)
+                                      : launch_bulk<SPECDEC_BF16>(p, (unsigned)grid, stream);
+  }
   const long long items = (long long)p.B * p.nchunk;
   const long long slots = (long long)device_sm_count() * kMinBlocks;
   const unsigned grid = (unsigned)(items < slots ? items : slots);
