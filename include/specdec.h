@@ -87,6 +87,7 @@ extern "C" {
 #define SPECDEC_MAX_TREE_NODES 1024
 #define SPECDEC_MAX_TREE_DEPTH 64
 #define SPECDEC_MAX_V (1 << 21)
+#define SPECDEC_MAX_UNIFORMS (1ll << 40) /* words per specdec_philox_uniforms call */
 
 /* ABI version of the loaded library (SPECDEC_ABI_VERSION at build time). */
 int specdec_abi_version(void);
@@ -221,6 +222,27 @@ int specdec_tree_finalize(const void *logits, const void *q, int dtype,
                           int32_t *out_tokens, int32_t *final_token, uint8_t *is_bonus,
                           int32_t *row_status, float *p_node, void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/*
+ * Uniforms on the device for the accept tests and the final draw (section
+ * 15.1.2 step 3 draws u ~ U(0,1); the other entry points take them as an
+ * input).  Generator: Philox4x64-10 ("Parallel random numbers: as easy as
+ * 1, 2, 3", Salmon, Moraes, Dror, Shaw, SC'11).  Word i of the stream that
+ * starts from `counter` is word i mod 4 of the block for counter
+ * counter + floor(i/4) + 1 under `key` (the counter advances before each
+ * block, as NumPy's Philox bit generator does, so a stream started from that
+ * generator's state continues it word for word); the call writes
+ *     out[j] = ((w_{first_word + j} >> 41) + 0.5) * 2^-23,   j in [0, n),
+ * exact float32 values strictly inside (0, 1).
+ *   key      host pointer, 2 words;  counter  host pointer, 4 words (little-endian)
+ *   out      device pointer, n floats
+ * Returns SPECDEC_ERR_INVALID_ARG for a null pointer, n < 0, or a word range
+ * beyond 2^64; SPECDEC_ERR_UNSUPPORTED for n > SPECDEC_MAX_UNIFORMS.  n = 0 is a
+ * no-op.  Asynchronous on `stream`; key and counter are read before return.
+ */
+int specdec_philox_uniforms(const uint64_t *key, const uint64_t *counter,
+                            unsigned long long first_word, long long n, float *out,
+                            void *stream);
 
 #ifdef __cplusplus
 }

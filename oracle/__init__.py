@@ -65,8 +65,40 @@ def _load():
         lib.specdec_oracle_verify_tree.restype = i
         lib.specdec_oracle_num_threads.argtypes = []
         lib.specdec_oracle_num_threads.restype = i
+        u64 = ctypes.c_uint64
+        lib.specdec_oracle_philox_words.argtypes = [p, p, u64, ctypes.c_int64, p]
+        lib.specdec_oracle_philox_words.restype = None
+        lib.specdec_oracle_philox_uniforms.argtypes = [p, p, u64, ctypes.c_int64, p]
+        lib.specdec_oracle_philox_uniforms.restype = None
         _lib = lib
     return _lib
+
+
+def _u64_array(x, n: int, name: str) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.uint64).reshape(-1))
+    if a.size != n:
+        raise ValueError(f"{name} must hold {n} 64-bit words")
+    return a
+
+
+def philox_words(key, counter, first: int, n: int) -> np.ndarray:
+    """Raw Philox4x64-10 words [first, first + n) of the stream (key, counter)."""
+    k = _u64_array(key, 2, "key")
+    c = _u64_array(counter, 4, "counter")
+    out = np.empty(n, dtype=np.uint64)
+    _load().specdec_oracle_philox_words(k.ctypes.data, c.ctypes.data, int(first), int(n),
+                                        out.ctypes.data)
+    return out
+
+
+def philox_uniforms(key, counter, first: int, n: int) -> np.ndarray:
+    """float32 uniforms ((w >> 41) + 0.5) * 2^-23 of the words [first, first + n)."""
+    k = _u64_array(key, 2, "key")
+    c = _u64_array(counter, 4, "counter")
+    out = np.empty(n, dtype=np.float32)
+    _load().specdec_oracle_philox_uniforms(k.ctypes.data, c.ctypes.data, int(first), int(n),
+                                           out.ctypes.data)
+    return out
 
 
 def num_threads() -> int:

@@ -37,6 +37,13 @@
  *     draws its bonus from its own target row;
  *   - a malformed request gets a status bitmask and sentinel outputs.
  *
+ * The uniforms the method draws (section 15.1.2 step 3: u ~ U(0,1)) are an
+ * input of both sides.  For generating them on the device, the library has a
+ * Philox4x64-10 generator; its statement here (specdec_oracle_philox_*) follows
+ * the generator's published definition (Salmon, Moraes, Dror, Shaw, "Parallel
+ * random numbers: as easy as 1, 2, 3", SC'11) and is pinned against NumPy's
+ * Philox bit generator, an independent implementation of the same definition.
+ *
  * Build: gcc -O2 -fopenmp -shared -fPIC (no fast-math: IEEE double).
  */
 #include <math.h>
@@ -436,4 +443,78 @@ int specdec_oracle_num_threads(void) {
   }
 #endif
   return n;
+}
+
+/* ------------------------------------------------------------------------
+ * Philox4x64-10 (SC'11 paper above).  One round maps the counter block
+ * (x0, x1, x2, x3) with key (k0, k1) to
+ *     (hi(M1 x2) ^ x1 ^ k0,  lo(M1 x2),  hi(M0 x0) ^ x3 ^ k1,  lo(M0 x0))
+ * where hi/lo are the halves of the 128-bit product; the key is bumped by the
+ * Weyl constants (W0, W1) between rounds; ten rounds.  Word i of a stream
+ * that starts from counter c is word i mod 4 of the block for counter
+ * c + floor(i / 4) + 1 (256-bit little-endian words; the counter is advanced
+ * before each block, as NumPy's Philox does).  Uniform: u = ((w >> 41) + 0.5)
+ * * 2^-23, exact in float32, in (0, 1).
+ * ------------------------------------------------------------------------ */
+static const uint64_t kPhiloxM0 = 0xD2E7470EE14C6C93ull;
+static const uint64_t kPhiloxM1 = 0xCA5A826395121157ull;
+static const uint64_t kPhiloxW0 = 0x9E3779B97F4A7C15ull;
+static const uint64_t kPhiloxW1 = 0xBB67AE8584CAA73Bull;
+
+static void philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
+  uint64_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+  uint64_t k0 = key[0], k1 = key[1];
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += kPhiloxW0;
+      k1 += kPhiloxW1;
+    }
+    const unsigned __int128 p0 = (unsigned __int128)kPhiloxM0 * x0;
+    const unsigned __int128 p1 = (unsigned __int128)kPhiloxM1 * x2;
+    const uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+    const uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+    x0 = hi1 ^ x1 ^ k0;
+    x1 = lo1;
+    x2 = hi0 ^ x3 ^ k1;
+    x3 = lo0;
+  }
+  out[0] = x0;
+  out[1] = x1;
+  out[2] = x2;
+  out[3] = x3;
+}
+
+/* counter + add (256-bit, little-endian 64-bit words) */
+static void counter_add(const uint64_t c[4], uint64_t add, uint64_t out[4]) {
+  uint64_t carry = add;
+  for (int i = 0; i < 4; ++i) {
+    const uint64_t v = c[i] + carry;
+    carry = (v < c[i]) ? 1 : 0;
+    out[i] = v;
+  }
+}
+
+/* Raw words [first, first + n) of the stream (key, counter). */
+void specdec_oracle_philox_words(const uint64_t *key, const uint64_t *counter, uint64_t first,
+                                 int64_t n, uint64_t *out) {
+  for (int64_t i = 0; i < n; ++i) {
+    const uint64_t w = first + (uint64_t)i;
+    uint64_t c[4], blk[4];
+    /* block floor(w / 4) uses counter + floor(w / 4) + 1: add in two steps so
+     * that a block index of 2^64 - 1 carries correctly */
+    counter_add(counter, w / 4, c);
+    counter_add(c, 1, c);
+    philox4x64_10(c, key, blk);
+    out[i] = blk[w % 4];
+  }
+}
+
+/* Uniforms of the words [first, first + n). */
+void specdec_oracle_philox_uniforms(const uint64_t *key, const uint64_t *counter, uint64_t first,
+                                    int64_t n, float *out) {
+  for (int64_t i = 0; i < n; ++i) {
+    uint64_t w;
+    specdec_oracle_philox_words(key, counter, first + (uint64_t)i, 1, &w);
+    out[i] = (float)(((double)(w >> 41) + 0.5) * 0x1p-23);
+  }
 }

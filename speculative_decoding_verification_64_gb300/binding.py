@@ -34,6 +34,9 @@ _EXPORTS = {
     "specdec_abi_version": ([], ctypes.c_int),
     "specdec_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "specdec_workspace_size": ([ctypes.c_int] * 4, ctypes.c_size_t),
+    "specdec_philox_uniforms": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_ulonglong,
+                                 ctypes.c_longlong, ctypes.c_void_p, ctypes.c_void_p],
+                                ctypes.c_int),
     "specdec_row_stats": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                            ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
@@ -306,3 +309,20 @@ def tree_inputs_to_device(w, device="cuda"):
     return (to_device(w.logits, device, bf), to_device(w.q, device, bf),
             to_device(w.node_tokens, device), to_device(w.parent, device),
             to_device(w.temperature, device), to_device(w.uniforms, device))
+
+
+def philox_uniforms(key, counter, first_word: int, n: int, device="cuda", stream=None) -> torch.Tensor:
+    """float32 uniforms of the Philox4x64-10 words [first_word, first_word + n) of the
+    stream (key, counter), made on the device (``specdec_philox_uniforms``).  key: 2
+    words, counter: 4 words (e.g. the state of ``numpy.random.Philox(seed)``)."""
+    import numpy as np
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64).reshape(-1))
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint64).reshape(-1))
+    if k.size != 2 or c.size != 4:
+        raise ValueError("key must hold 2 and counter 4 64-bit words")
+    out = torch.empty(int(n), dtype=torch.float32, device=device)
+    rc = load_library().specdec_philox_uniforms(k.ctypes.data, c.ctypes.data, int(first_word),
+                                                int(n), _ptr(out) if n > 0 else None,
+                                                _stream_ptr(stream))
+    _check(rc, "specdec_philox_uniforms")
+    return out

@@ -296,4 +296,23 @@ int specdec_verify_tree(const void *logits, const void *q, int dtype, const int3
                               is_bonus, row_status, p_node, workspace, s);
 }
 
+
+int specdec_philox_uniforms(const uint64_t *key, const uint64_t *counter,
+                            unsigned long long first_word, long long n, float *out,
+                            void *stream) {
+  if (n < 0) return SPECDEC_ERR_INVALID_ARG;
+  if (n == 0) return SPECDEC_OK;
+  if (!key || !counter || !out) return SPECDEC_ERR_INVALID_ARG;
+  if (n > SPECDEC_MAX_UNIFORMS) return SPECDEC_ERR_UNSUPPORTED;
+  if (first_word > ~0ull - (unsigned long long)(n - 1)) return SPECDEC_ERR_INVALID_ARG;
+  PhiloxParams p;
+  p.key[0] = key[0];
+  p.key[1] = key[1];
+  for (int i = 0; i < 4; ++i) p.counter[i] = counter[i];
+  p.first = first_word;
+  p.n = n;
+  p.out = out;
+  return cuda_status(launch_philox_uniforms(p, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

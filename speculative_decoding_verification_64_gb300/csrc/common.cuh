@@ -130,11 +130,21 @@ struct TreeFinalizeParams {
 };
 
 // host launchers (defined in the .cu files)
+// Philox4x64-10 uniforms: words [first, first + n) of the stream (key, counter).
+struct PhiloxParams {
+  uint64_t key[2];
+  uint64_t counter[4];
+  uint64_t first;
+  long long n;
+  float *out;
+};
+
 // Multiprocessor count of the current device (looked up once per device).
 int device_sm_count();
 cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream);
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream);
 cudaError_t launch_tree_finalize(const TreeFinalizeParams &p, cudaStream_t stream);
+cudaError_t launch_philox_uniforms(const PhiloxParams &p, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // device helpers

@@ -109,3 +109,20 @@ def test_oracle_is_not_reachable_from_the_product_package():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "specdec_oracle" not in text, f
+
+
+def test_philox_argument_checks(lib):
+    import numpy as np
+    N = None
+    key = np.zeros(2, dtype=np.uint64)
+    ctr = np.zeros(4, dtype=np.uint64)
+    k, c = key.ctypes.data, ctr.ctypes.data
+    d = ctypes.c_void_p(16)
+    ph = lib.specdec_philox_uniforms
+    assert ph(k, c, 0, 0, N, N) == 0                    # n = 0 is a no-op
+    assert ph(k, c, 0, -1, d, N) == 1                   # n < 0
+    assert ph(N, c, 0, 4, d, N) == 1                    # null key
+    assert ph(k, N, 0, 4, d, N) == 1                    # null counter
+    assert ph(k, c, 0, 4, N, N) == 1                    # null output
+    assert ph(k, c, 2**64 - 3, 4, d, N) == 1            # word range beyond 2^64
+    assert ph(k, c, 0, (1 << 40) + 1, d, N) == 2        # beyond SPECDEC_MAX_UNIFORMS

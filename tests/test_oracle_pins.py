@@ -664,3 +664,46 @@ def test_tree_status_bits(oracle_lib):
                                   w.temperature, w.uniforms, max_depth=1)
     deep = np.array([(np.bincount(np.r_[0, w.parent[b, 1:]]) > 0).sum() > 1 for b in range(6)])
     assert (out2["row_status"][deep] & oracle_lib.ROW_BAD_TREE).all()
+
+
+# --- Philox4x64-10 uniforms (the device generator's oracle) -----------------
+# Pinned against NumPy's Philox bit generator: an independent implementation of
+# the same published generator, whose raw words the oracle must reproduce for
+# any key, counter (including carries across the 64-bit counter words) and
+# starting word.
+
+def _numpy_philox(key, counter):
+    import numpy as np
+    bg = np.random.Philox(0)
+    st = bg.state
+    st["state"]["key"] = np.asarray(key, dtype=np.uint64)
+    st["state"]["counter"] = np.asarray(counter, dtype=np.uint64)
+    st["buffer_pos"] = 4
+    bg.state = st
+    return bg
+
+
+@pytest.mark.parametrize("counter", [
+    [0, 0, 0, 0],
+    [2**64 - 3, 7, 0, 0],                               # carry into word 1
+    [2**64 - 1, 2**64 - 1, 2**64 - 1, 2**64 - 5],       # carries through three words
+    [123456789, 2**63, 5, 2**64 - 1],
+])
+@pytest.mark.parametrize("key", [[0, 0], [2**64 - 1, 1], [0x0123456789ABCDEF, 0xFEDCBA9876543210]])
+def test_philox_words_match_numpy(oracle_lib, key, counter):
+    import numpy as np
+    want = _numpy_philox(key, counter).random_raw(64)
+    for first, n in [(0, 64), (1, 10), (3, 5), (4, 4), (17, 40)]:
+        got = oracle_lib.philox_words(key, counter, first, n)
+        assert np.array_equal(got, want[first:first + n]), (first, n)
+
+
+@pytest.mark.parametrize("seed,shape,offset", [(0, (3, 5), 0), (7, (257,), 6), (2024, (4, 9), 1001)])
+def test_philox_uniforms_match_the_workload_stream(oracle_lib, seed, shape, offset):
+    import numpy as np
+    want = W.philox_uniforms(seed, shape, offset_words=offset).reshape(-1)
+    st = np.random.Philox(seed).state["state"]
+    got = oracle_lib.philox_uniforms(st["key"], st["counter"], offset, want.size)
+    assert got.dtype == np.float32
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    assert (got > 0).all() and (got < 1).all()
