@@ -326,3 +326,4 @@ def philox_uniforms(key, counter, first_word: int, n: int, device="cuda", stream
                                                 _stream_ptr(stream))
     _check(rc, "specdec_philox_uniforms")
     return out
+

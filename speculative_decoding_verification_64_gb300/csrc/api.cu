@@ -49,6 +49,7 @@ LinearWs linear_ws(void *workspace, long long B, int R, int V, int dtype) {
 }
 
 size_t workspace_bytes_for(long long B, int R, int V, int dtype) {
+  if (B <= 0) return 0;  // no requests, no scratch
   return workspace_layout(B, R, V, dtype).total;
 }
 
@@ -149,12 +150,12 @@ static int linear_checks(const void *logits, const void *q, int dtype, const int
   return check_workspace(workspace, workspace_bytes, B, gamma + 1, V, dtype);
 }
 
-static int linear_finalize_launch(const void *logits, const void *q, int dtype,
-                                  const int32_t *tokens, const float *temperature,
-                                  const float *uniforms, int B, int gamma, int V,
-                                  int32_t *n_accepted, int32_t *out_tokens,
-                                  int32_t *final_token, uint8_t *is_bonus, int32_t *row_status,
-                                  float *p_draft, void *workspace, cudaStream_t stream) {
+static LinearFinalizeParams linear_params(const void *logits, const void *q, int dtype,
+                                          const int32_t *tokens, const float *temperature,
+                                          const float *uniforms, int B, int gamma, int V,
+                                          int32_t *n_accepted, int32_t *out_tokens,
+                                          int32_t *final_token, uint8_t *is_bonus,
+                                          int32_t *row_status, float *p_draft, void *workspace) {
   LinearFinalizeParams p;
   p.logits = logits;
   p.q = q;
@@ -176,6 +177,18 @@ static int linear_finalize_launch(const void *logits, const void *q, int dtype,
   p.spr = stages_per_row(V, elem_bytes(dtype));
   p.nchunk = draw_chunks(V);
   p.ntot = draw_total_slots(V, elem_bytes(dtype));
+  return p;
+}
+
+static int linear_finalize_launch(const void *logits, const void *q, int dtype,
+                                  const int32_t *tokens, const float *temperature,
+                                  const float *uniforms, int B, int gamma, int V,
+                                  int32_t *n_accepted, int32_t *out_tokens,
+                                  int32_t *final_token, uint8_t *is_bonus, int32_t *row_status,
+                                  float *p_draft, void *workspace, cudaStream_t stream) {
+  const LinearFinalizeParams p =
+      linear_params(logits, q, dtype, tokens, temperature, uniforms, B, gamma, V, n_accepted,
+                    out_tokens, final_token, is_bonus, row_status, p_draft, workspace);
   return cuda_status(launch_linear_finalize(p, stream));
 }
 

@@ -30,10 +30,12 @@
 // last, still in L2, come first.
 #include <cfloat>
 
-#include "common.cuh"
+#include "draw_common.cuh"
 
 namespace specdec {
 namespace {
+
+using namespace drawc;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
@@ -223,122 +225,7 @@ __device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long lon
   return pre + inc - v;
 }
 
-constexpr int kSeg = 16;                     // lanes merging one row
 constexpr int kRowsPerRound = kThreads / kSeg;
-
-__device__ __forceinline__ float4 load_partial(const float4 *pr, int j, int spr, bool active) {
-  return (active && j < spr) ? pr[j] : make_float4(-INFINITY, 0.0f, __int_as_float(0x7FFFFFFF), 0.0f);
-}
-
-// Merge of one row's partials by a 16-lane segment of a warp (both segments
-// of the warp take part in every shuffle; an idle segment merges nothing).
-// The first two partials of each lane are loaded before any arithmetic, so
-// that rows of up to 32 stages cost one memory round trip.
-__device__ __forceinline__ RowStat segment_merge_row(const RowPartial *part, long long row,
-                                                     bool active, int spr, float c, int sl) {
-  const float4 *pr = reinterpret_cast<const float4 *>(part + row * (long long)spr);
-  const float4 x0 = load_partial(pr, sl, spr, active);
-  const float4 x1 = load_partial(pr, sl + kSeg, spr, active);
-  float m = -INFINITY, s = 0.0f;
-  int a = 0x7FFFFFFF;
-  int fl = __float_as_int(x0.w) | __float_as_int(x1.w);
-  merge2(m, s, a, x0.x, x0.y, __float_as_int(x0.z), c);
-  merge2(m, s, a, x1.x, x1.y, __float_as_int(x1.z), c);
-  if (active) {
-    for (int j = sl + 2 * kSeg; j < spr; j += kSeg) {  // rows of more than 32 stages
-      const float4 x = pr[j];
-      fl |= __float_as_int(x.w);
-      merge2(m, s, a, x.x, x.y, __float_as_int(x.z), c);
-    }
-  }
-#pragma unroll
-  for (int d = kSeg / 2; d >= 1; d >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, d);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, d);
-    const int a2 = __shfl_xor_sync(0xffffffffu, a, d);
-    fl |= __shfl_xor_sync(0xffffffffu, fl, d);
-    merge2(m, s, a, m2, s2, a2, c);
-  }
-  RowStat r;
-  r.M = m;
-  r.S = s;
-  r.arg = a;
-  r.flags = fl;
-  return r;
-}
-
-// Inputs of one lane's accept test: draft x~_i, its uniform, and the logit
-// and q value the stats pass gathered for it.
-struct DraftIn {
-  int x;
-  float u;
-  float2 g;
-};
-
-__device__ __forceinline__ DraftIn load_draft(const LinearFinalizeParams &p, long long b, int lane) {
-  DraftIn in;
-  in.x = -1;
-  in.u = 0.0f;
-  in.g = make_float2(0.0f, 1.0f);
-  if (lane < p.gamma) {
-    in.x = __ldg(p.tokens + b * p.gamma + lane);
-    in.u = __ldg(p.uniforms + b * (p.gamma + 1) + lane);
-    in.g = __ldg(p.ws.gather + b * (p.gamma + 1) + lane);  // meaningful for a valid x only
-  }
-  return in;
-}
-
-// The accept test of request b by warp 0 from the merged rows rs[0, R):
-// lane i < gamma tests draft i, a ballot gives the first rejection.  Lane
-// i's p_i(x~_i) is returned in pd (NaN for a malformed request).
-__device__ __forceinline__ LinearDecision decide(const LinearFinalizeParams &p, const DraftIn &in,
-                                                 float T, float c, const RowStat *rs, int lane,
-                                                 float &pd) {
-  const int gamma = p.gamma, R = gamma + 1, V = p.V;
-  const bool greedy = (T == 0.0f);
-  RowStat r0, r1;
-  r0.M = r1.M = -INFINITY;
-  r0.S = r1.S = 0.0f;
-  r0.arg = r1.arg = 0x7FFFFFFF;
-  r0.flags = r1.flags = 0;
-  if (lane < R) r0 = rs[lane];
-  if (lane + 32 < R) r1 = rs[lane + 32];
-  int status = temperature_valid(T) ? 0 : SPECDEC_ROW_BAD_TEMP;
-  if (lane < R) status |= r0.flags | (row_usable(r0) ? 0 : SPECDEC_ROW_NONFINITE);
-  if (lane + 32 < R) status |= r1.flags | (row_usable(r1) ? 0 : SPECDEC_ROW_NONFINITE);
-  bool acc = true;
-  pd = 0.0f;
-  if (lane < gamma) {
-    if (in.x < 0 || in.x >= V) {
-      status |= SPECDEC_ROW_BAD_TOKEN;
-    } else {
-      if (!(in.g.y > 0.0f) || in.g.y == INFINITY) status |= SPECDEC_ROW_BAD_Q;
-      if (greedy) {
-        acc = (in.x == r0.arg);
-        pd = acc ? 1.0f : 0.0f;
-      } else {
-        pd = exp2f((in.g.x - r0.M) * c) / r0.S;
-        // u <= min(1, p/q)  <=>  u q <= p  for q > 0, u < 1 (exact products in float64)
-        acc = ((double)in.u * (double)in.g.y <= (double)pd);
-      }
-    }
-  }
-  status = __reduce_or_sync(0xffffffffu, status);
-  if (status) pd = __int_as_float(0x7fc00000);
-  const unsigned rej = __ballot_sync(0xffffffffu, lane < gamma && !acc);
-  const int k = rej ? (__ffs(rej) - 1) : gamma;
-  const bool hi = k >= 32;  // statistics of the final row k, from the lane holding it
-  LinearDecision d;
-  d.k = k;
-  d.status = status;
-  d.greedy = greedy;
-  d.arg = __shfl_sync(0xffffffffu, hi ? r1.arg : r0.arg, k & 31);
-  d.M = __shfl_sync(0xffffffffu, hi ? r1.M : r0.M, k & 31);
-  d.S = __shfl_sync(0xffffffffu, hi ? r1.S : r0.S, k & 31);
-  d.c = c;
-  d.pad = 0;
-  return d;
-}
 
 struct DrawSmem {
   unsigned long long red[2 * kWarps];
@@ -505,13 +392,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) linear_draw_kernel(const
 // ---------------------------------------------------------------------------
 namespace bulk {
 
-constexpr int kStage = SPECDEC_DRAW_STAGE_BYTES;    // bytes of the final row per stage
+using namespace drawc;
+
 constexpr int kUnitStages = 4;
 constexpr int kUnitBytes = kStage * kUnitStages;    // one bulk copy of logits (+ one of q)
 constexpr int kSlots = 6;
 constexpr int kWarps = 12;                          // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;         // + the producer warp
-constexpr int kVec = kStage / 16 / 32;              // 16-byte vectors per lane per stage
 constexpr int kMaxReq = 8;                          // requests in one CTA's run
 constexpr unsigned kAbort = 1u << 24;               // ticket increment of a CTA whose wait ran out
 
@@ -525,229 +412,6 @@ struct Smem {
   int search[kMaxReq];  // 0: not this CTA's; 1: search; 2: search, but a wait ran out somewhere
   volatile int abort_flag;
 };
-
-// Weight of element i of a 16-byte vector: 2^((l - M) c), or max(0, that - S q)
-// after a rejection (the same arithmetic as the other form of the draw).
-template <int DT>
-__device__ __forceinline__ float vec_weight(const uint4 &lv, const uint4 &qv, int i,
-                                            const LinearDecision &d, bool use_q) {
-  float l, q;
-  if (DT == SPECDEC_F32) {
-    const uint32_t lw = (i == 0) ? lv.x : (i == 1) ? lv.y : (i == 2) ? lv.z : lv.w;
-    const uint32_t qw = (i == 0) ? qv.x : (i == 1) ? qv.y : (i == 2) ? qv.z : qv.w;
-    l = __uint_as_float(lw);
-    q = __uint_as_float(qw);
-  } else {
-    const int j = i >> 1;
-    const uint32_t lw = (j == 0) ? lv.x : (j == 1) ? lv.y : (j == 2) ? lv.z : lv.w;
-    const uint32_t qw = (j == 0) ? qv.x : (j == 1) ? qv.y : (j == 2) ? qv.z : qv.w;
-    l = (i & 1) ? bf16_hi(lw) : bf16_lo(lw);
-    q = (i & 1) ? bf16_hi(qw) : bf16_lo(qw);
-  }
-  const float ev = ex2_approx((l - d.M) * d.c);
-  return use_q ? fmaxf(fmaf(-d.S, q, ev), 0.0f) : ev;
-}
-
-template <int DT>
-__host__ __device__ constexpr int vec_elems() { return (DT == SPECDEC_F32) ? 4 : 8; }
-
-// float32 sum, in index order, of the weights of one vector
-template <int DT>
-__device__ __forceinline__ float vec_sum(const uint4 &lv, const uint4 &qv, const LinearDecision &d,
-                                         bool use_q) {
-  float s = 0.0f;
-#pragma unroll
-  for (int i = 0; i < vec_elems<DT>(); ++i) s += vec_weight<DT>(lv, qv, i, d, use_q);
-  return s;
-}
-
-// the element of a vector at which base + (running sum, as in vec_sum) first exceeds target
-template <int DT>
-__device__ __forceinline__ int vec_find(const uint4 &lv, const uint4 &qv, const LinearDecision &d,
-                                        bool use_q, unsigned long long base,
-                                        unsigned long long target) {
-  float run = 0.0f;
-#pragma unroll
-  for (int i = 0; i < vec_elems<DT>(); ++i) {
-    run += vec_weight<DT>(lv, qv, i, d, use_q);
-    if (base + to_fixed40(run) > target) return i;
-  }
-  return vec_elems<DT>() - 1;
-}
-
-__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) v += shfl_xor_u64(v, d);
-  return v;
-}
-
-__device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v, int lane) {
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const unsigned long long y = shfl_up_u64(v, d);
-    if (lane >= d) v += y;
-  }
-  return v;
-}
-
-__host__ __device__ constexpr uint32_t kNegInfBits(int dt) { return dt == SPECDEC_F32 ? 0xFF800000u : 0xFF80FF80u; }
-
-// Vectors lane + 32 k of a stage of sbytes bytes (from shared or global
-// memory): -inf logits and zero q past the end, which weigh 0.
-template <int DT>
-__device__ __forceinline__ void load_stage(uint4 (&lv)[kVec], uint4 (&qv)[kVec], const uint8_t *l,
-                                           const uint8_t *q, int sbytes, bool use_q, int lane,
-                                           bool global) {
-  const uint32_t ninf = kNegInfBits(DT);
-#pragma unroll
-  for (int k = 0; k < kVec; ++k) {
-    const int off = (lane + 32 * k) * 16;
-    const bool in = off < sbytes;
-    if (global) {
-      lv[k] = in ? __ldg(reinterpret_cast<const uint4 *>(l + off)) : make_uint4(ninf, ninf, ninf, ninf);
-      qv[k] = (in && use_q) ? __ldg(reinterpret_cast<const uint4 *>(q + off)) : make_uint4(0u, 0u, 0u, 0u);
-    } else {
-      lv[k] = in ? *reinterpret_cast<const uint4 *>(l + off) : make_uint4(ninf, ninf, ninf, ninf);
-      qv[k] = (in && use_q) ? *reinterpret_cast<const uint4 *>(q + off) : make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-}
-
-// Per-request view of the run: the request's index b, its row pointers and sizes.
-struct Req {
-  long long b;
-  const uint8_t *lrow, *qrow;
-  int rowbytes, nst;
-};
-
-template <int DT>
-__device__ __forceinline__ Req make_req(const LinearFinalizeParams &p, long long rb, int k) {
-  constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
-  Req r;
-  r.b = (long long)p.B - 1 - rb;
-  const int R = p.gamma + 1;
-  r.rowbytes = p.V * es;
-  r.nst = (r.rowbytes + kStage - 1) / kStage;
-  r.lrow = reinterpret_cast<const uint8_t *>(p.logits) + (size_t)(r.b * R + k) * r.rowbytes;
-  r.qrow = (k < p.gamma)
-               ? reinterpret_cast<const uint8_t *>(p.q) + (size_t)(r.b * p.gamma + k) * r.rowbytes
-               : r.lrow;
-  return r;
-}
-
-// Outputs of request b but a drawn token, by one warp.
-__device__ __forceinline__ void write_outputs_warp(const LinearFinalizeParams &p, long long b,
-                                                   const LinearDecision &d, float pd, int lane) {
-  const int gamma = p.gamma, R = gamma + 1, k = d.k;
-  if (p.p_draft && lane < gamma) p.p_draft[b * gamma + lane] = pd;
-  for (int i = lane; i < R; i += 32) {
-    int t = -1;
-    if (!d.status) {
-      if (i < k) t = __ldg(p.tokens + b * gamma + i);
-      else if (i == k) t = d.arg;
-    }
-    if (d.status || i != k || d.greedy) p.out_tokens[b * R + i] = t;
-  }
-  if (lane == 0) {
-    p.n_accepted[b] = d.status ? 0 : k;
-    p.is_bonus[b] = (uint8_t)(!d.status && k == gamma);
-    p.row_status[b] = d.status;
-    if (d.status) p.final_token[b] = -1;
-    else if (d.greedy) p.final_token[b] = d.arg;
-  }
-}
-
-// The search of one request by one warp (see the header of this section).
-template <int DT>
-__device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const Req &rq,
-                                            LinearDecision d, bool aborted, int lane) {
-  constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
-  const int gamma = p.gamma, R = gamma + 1;
-  const long long b = rq.b;
-  unsigned long long *tot = p.ws.chunk_tot + b * p.ntot;
-  if (lane == 0) p.ws.draw_cnt[b] = 0;  // phase 2 may run again on the same phase-1 result
-  if (aborted) {
-    // a bounded wait ran out in some CTA of this request: report, draw nothing
-    for (int i = lane; i < R; i += 32) p.out_tokens[b * R + i] = -1;
-    if (lane == 0) {
-      p.row_status[b] = SPECDEC_ROW_INTERNAL;
-      p.n_accepted[b] = 0;
-      p.is_bonus[b] = 0;
-      p.final_token[b] = -1;
-    }
-    return;
-  }
-  bool use_q = d.k < gamma;
-  unsigned long long Z = 0;
-  for (int s = lane; s < rq.nst; s += 32) Z += __ldcg(tot + s);
-  Z = warp_sum_u64(Z);
-  if (Z == 0 && use_q) {
-    // residual mass 0 (only by rounding): draw from p itself
-    use_q = false;
-    for (int s = 0; s < rq.nst; ++s) {
-      uint4 lv[kVec], qv[kVec];
-      load_stage<DT>(lv, qv, rq.lrow + (size_t)s * kStage, rq.qrow + (size_t)s * kStage,
-                     min(kStage, rq.rowbytes - s * kStage), false, lane, true);
-      unsigned long long acc = 0;
-#pragma unroll
-      for (int k = 0; k < kVec; ++k) acc += to_fixed40(vec_sum<DT>(lv[k], qv[k], d, false));
-      acc = warp_sum_u64(acc);
-      if (lane == 0) tot[s] = acc;
-      Z += acc;
-    }
-    __syncwarp();
-  }
-  const float U = __ldg(p.uniforms + b * R + gamma);
-  const unsigned long long target = uniform_target(U, Z);
-  // the stage holding the crossing
-  unsigned long long base = 0;
-  int st = -1;
-  for (int s0 = 0; s0 < rq.nst && st < 0; s0 += 32) {
-    const unsigned long long v = (s0 + lane < rq.nst) ? __ldcg(tot + s0 + lane) : 0ull;
-    const unsigned long long incl = warp_incl_scan_u64(v, lane);
-    const unsigned m = __ballot_sync(0xffffffffu, target < base + incl);
-    if (m) {
-      const int ls = __ffs(m) - 1;
-      st = s0 + ls;
-      base += __shfl_sync(0xffffffffu, incl - v, ls);
-    } else {
-      base += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
-  if (st < 0) return;  // no weight at all: unreachable for a usable row
-  // the vector, in index order (vector lane + 32 k), then the element
-  uint4 lv[kVec], qv[kVec];
-  const int off = st * kStage;
-  load_stage<DT>(lv, qv, rq.lrow + off, rq.qrow + off, min(kStage, rq.rowbytes - off), use_q, lane,
-                 true);
-  int kx = -1, lx = -1;               // the crossing vector: lane lx's vector kx
-  unsigned long long vbase = 0;       // fixed-point sum before it (valid in lane lx)
-#pragma unroll
-  for (int k = 0; k < kVec; ++k) {
-    const unsigned long long x = to_fixed40(vec_sum<DT>(lv[k], qv[k], d, use_q));
-    const unsigned long long incl = warp_incl_scan_u64(x, lane);
-    const unsigned m = __ballot_sync(0xffffffffu, target < base + incl);
-    if (kx < 0 && m) {
-      kx = k;
-      lx = __ffs(m) - 1;
-      vbase = base + incl - x;
-    }
-    base += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (kx < 0 || lane != lx) return;
-  uint4 ls = lv[0], qs = qv[0];
-#pragma unroll
-  for (int k = 1; k < kVec; ++k) {
-    if (k == kx) {
-      ls = lv[k];
-      qs = qv[k];
-    }
-  }
-  const int e = vec_find<DT>(ls, qs, d, use_q, vbase, target);
-  const int v = off / es + (lane + 32 * kx) * vec_elems<DT>() + e;
-  p.final_token[b] = v;
-  p.out_tokens[b * R + d.k] = v;
-}
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFinalizeParams p) {
@@ -884,7 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFina
   if (warp < nreq && sm.search[warp]) {
     __threadfence();
     const LinearDecision d = sm.dec[warp];
-    search_warp<DT>(p, make_req<DT>(p, rb0 + warp, d.k), d, sm.search[warp] == 2, lane);
+    const Req rq = make_req<DT>(p, rb0 + warp, d.k);
+    if (lane == 0) p.ws.draw_cnt[rq.b] = 0;  // phase 2 may run again on the same phase-1 result
+    search_warp<DT>(p, rq, d, sm.search[warp] == 2, lane);
   }
 }
 
