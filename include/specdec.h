@@ -137,10 +137,15 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
  *                 each drafted token's logit and q value for phase 2.  Both
  *                 NULL for the tree form or for the statistics alone; one
  *                 without the other is SPECDEC_ERR_INVALID_ARG.
+ *   flags         0, or SPECDEC_STATS_ENTROPY to keep per stage the sum of
+ *                 p-weighted logit offsets that specdec_row_entropy reads (about
+ *                 one extra fused multiply-add per element; the verify calls
+ *                 run without it).  Other bits: SPECDEC_ERR_INVALID_ARG.
  */
+#define SPECDEC_STATS_ENTROPY 1u /* flag: also the sums specdec_row_entropy needs */
 int specdec_row_stats(const void *logits, const void *q, int dtype, const int32_t *draft_tokens,
                       const float *temperature, int B, int rows_per_request, int V,
-                      void *workspace, size_t workspace_bytes, void *stream);
+                      unsigned flags, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Phase 2 of the linear form: the accept test with early stop (section
@@ -222,6 +227,41 @@ int specdec_tree_finalize(const void *logits, const void *q, int dtype,
                           int32_t *out_tokens, int32_t *final_token, uint8_t *is_bonus,
                           int32_t *row_status, float *p_node, void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/*
+ * Entropy -sum_v p ln p (natural log) of every target row, for policies that
+ * set the draft length from the target's confidence (the adaptive draft
+ * length of the multi-token-prediction section: entropy = -sum p(x) log p(x)).
+ * Reads the workspace of a specdec_row_stats call made with
+ * SPECDEC_STATS_ENTROPY (then phase 2 may run as usual) for the same B,
+ * rows_per_request, V, dtype; temperature float32 [B].
+ *   entropy  float32 [B, rows_per_request]; 0 for greedy rows (T = 0),
+ *            NaN for an invalid temperature, an unusable row, or a workspace
+ *            whose statistics were taken without the flag.
+ * One small launch; the logits are not read again.
+ */
+int specdec_row_entropy(const void *workspace, size_t workspace_bytes, int dtype,
+                        const float *temperature, int B, int rows_per_request, int V,
+                        float *entropy, void *stream);
+
+/*
+ * Log-probability under the target of the path a verify step emitted (the
+ * path-probability passage of the tree section: log P(path) = sum_i log
+ * p(x_i | prefix_i)):
+ *     logprob[b] = sum_{j = 0 .. n_accepted[b]} ln p_{row_j}(out_tokens[b, j])
+ * with row_j = j for the linear form (path_nodes NULL) and
+ * row_j = path_nodes[b, j] for the tree form; out_tokens and path_nodes have
+ * rows of path_len entries (gamma + 1, or max_depth + 1), as the verify calls
+ * write them.  Greedy requests: 0 along arg-maxima, -inf otherwise.  NaN for
+ * a request with a nonzero row_status (row_status may be NULL), an invalid
+ * temperature, an unusable row, or a token or node out of range.  Needs the
+ * logits and the workspace of the same verify call.
+ */
+int specdec_path_logprob(const void *logits, int dtype, const float *temperature,
+                         const int32_t *out_tokens, const int32_t *n_accepted,
+                         const int32_t *path_nodes, const int32_t *row_status, int B,
+                         int rows_per_request, int V, int path_len, const void *workspace,
+                         size_t workspace_bytes, float *logprob, void *stream);
 
 /*
  * Uniforms on the device for the accept tests and the final draw (section

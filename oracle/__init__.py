@@ -65,6 +65,10 @@ def _load():
         lib.specdec_oracle_verify_tree.restype = i
         lib.specdec_oracle_num_threads.argtypes = []
         lib.specdec_oracle_num_threads.restype = i
+        lib.specdec_oracle_row_entropy.argtypes = [p, i, p, i, i, i, p]
+        lib.specdec_oracle_row_entropy.restype = None
+        lib.specdec_oracle_path_logprob.argtypes = [p, i, p, p, p, p, p, i, i, i, i, p]
+        lib.specdec_oracle_path_logprob.restype = None
         u64 = ctypes.c_uint64
         lib.specdec_oracle_philox_words.argtypes = [p, p, u64, ctypes.c_int64, p]
         lib.specdec_oracle_philox_words.restype = None
@@ -98,6 +102,40 @@ def philox_uniforms(key, counter, first: int, n: int) -> np.ndarray:
     out = np.empty(n, dtype=np.float32)
     _load().specdec_oracle_philox_uniforms(k.ctypes.data, c.ctypes.data, int(first), int(n),
                                            out.ctypes.data)
+    return out
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def row_entropy(logits: np.ndarray, dtype: str, temperature: np.ndarray) -> np.ndarray:
+    """float64 [B, R] entropies (natural log) of the target rows of logits [B, R, V]
+    (float32, or uint16 bf16 bits)."""
+    B, R, V = logits.shape
+    lg = np.ascontiguousarray(logits)
+    tp = np.ascontiguousarray(temperature, dtype=np.float32)
+    out = np.empty((B, R), dtype=np.float64)
+    _load().specdec_oracle_row_entropy(lg.ctypes.data, _dtype_code(dtype), tp.ctypes.data,
+                                       B, R, V, out.ctypes.data)
+    return out
+
+
+def path_logprob(logits: np.ndarray, dtype: str, temperature: np.ndarray, out_tokens: np.ndarray,
+                 n_accepted: np.ndarray, path_nodes: Optional[np.ndarray] = None,
+                 row_status: Optional[np.ndarray] = None) -> np.ndarray:
+    """float64 [B] log-probabilities of the emitted paths (see specdec_oracle.c)."""
+    B, R, V = logits.shape
+    lg = np.ascontiguousarray(logits)
+    tp = np.ascontiguousarray(temperature, dtype=np.float32)
+    ot = np.ascontiguousarray(out_tokens, dtype=np.int32)
+    na = np.ascontiguousarray(n_accepted, dtype=np.int32)
+    pn = None if path_nodes is None else np.ascontiguousarray(path_nodes, dtype=np.int32)
+    rs = None if row_status is None else np.ascontiguousarray(row_status, dtype=np.int32)
+    out = np.empty(B, dtype=np.float64)
+    _load().specdec_oracle_path_logprob(lg.ctypes.data, _dtype_code(dtype), tp.ctypes.data,
+                                        ot.ctypes.data, na.ctypes.data, _ptr(pn), _ptr(rs),
+                                        B, R, V, ot.shape[1], out.ctypes.data)
     return out
 
 

@@ -518,3 +518,76 @@ void specdec_oracle_philox_uniforms(const uint64_t *key, const uint64_t *counter
     out[i] = (float)(((double)(w >> 41) + 0.5) * 0x1p-23);
   }
 }
+
+/* ------------------------------------------------------------------------
+ * Per-row entropy and path log-probability (the adaptive-draft-length and
+ * path-probability passages of the same chapter: entropy = -sum p log p of
+ * the target distribution, and log P(path) = sum_i log p(x_i | prefix_i)).
+ * ------------------------------------------------------------------------ */
+
+/* entropy[b * R + i] = -sum_v p log p of target row (b, i), natural log;
+ * 0 for greedy rows (one-hot), NaN for an invalid temperature or an unusable
+ * row. */
+void specdec_oracle_row_entropy(const void *logits, int dtype, const float *temperature, int B,
+                                int R, int V, double *entropy) {
+#pragma omp parallel
+  {
+    double *p = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (long long row = 0; row < (long long)B * R; ++row) {
+      const int b = (int)(row / R);
+      const float T = temperature[b];
+      const size_t off = (size_t)row * (size_t)V;
+      if (!temperature_valid(T) || row_nonfinite(logits, dtype, off, V)) {
+        entropy[row] = NAN;
+        continue;
+      }
+      target_probs(logits, dtype, off, V, (double)T, p);
+      double h = 0.0;
+      for (int v = 0; v < V; ++v)
+        if (p[v] > 0.0) h -= p[v] * log(p[v]);
+      entropy[row] = h;
+    }
+    free(p);
+  }
+}
+
+/* logprob[b] = sum_{j=0..n_accepted[b]} log p_{row_j}(out_tokens[b, j]) with
+ * row_j = j (path_nodes NULL, linear form) or path_nodes[b, j] (tree form);
+ * out_tokens and path_nodes have rows of path_len entries.  NaN for a
+ * request with a nonzero status, an invalid temperature, an unusable row or
+ * a token or node out of range; -inf where a token has probability 0. */
+void specdec_oracle_path_logprob(const void *logits, int dtype, const float *temperature,
+                                 const int32_t *out_tokens, const int32_t *n_accepted,
+                                 const int32_t *path_nodes, const int32_t *row_status, int B,
+                                 int R, int V, int path_len, double *logprob) {
+#pragma omp parallel
+  {
+    double *p = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+      const float T = temperature[b];
+      const int k = n_accepted[b];
+      double s = 0.0;
+      int bad = (row_status && row_status[b] != 0) || !temperature_valid(T) || k < 0 ||
+                k >= path_len;
+      for (int j = 0; !bad && j <= k; ++j) {
+        const int row = path_nodes ? path_nodes[(size_t)b * path_len + j] : j;
+        const int tok = out_tokens[(size_t)b * path_len + j];
+        if (row < 0 || row >= R || tok < 0 || tok >= V) {
+          bad = 1;
+          break;
+        }
+        const size_t off = ((size_t)b * R + (size_t)row) * (size_t)V;
+        if (row_nonfinite(logits, dtype, off, V)) {
+          bad = 1;
+          break;
+        }
+        target_probs(logits, dtype, off, V, (double)T, p);
+        s += log(p[tok]);
+      }
+      logprob[b] = bad ? NAN : s;
+    }
+    free(p);
+  }
+}

@@ -37,9 +37,17 @@ _EXPORTS = {
     "specdec_philox_uniforms": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_ulonglong,
                                  ctypes.c_longlong, ctypes.c_void_p, ctypes.c_void_p],
                                 ctypes.c_int),
+    "specdec_row_entropy": ([ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
+                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                             ctypes.c_void_p], ctypes.c_int),
+    "specdec_path_logprob": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                              ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "specdec_row_stats": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+                           ctypes.c_uint, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p],
+                          ctypes.c_int),
     "specdec_verify_linear": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
                               [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 +
                               [ctypes.c_void_p] * 7 + [ctypes.c_size_t, ctypes.c_void_p],
@@ -206,16 +214,20 @@ def verify_linear(logits: torch.Tensor, q: torch.Tensor, draft_tokens: torch.Ten
     return out
 
 
+STATS_ENTROPY = 1
+
+
 def row_stats(logits: torch.Tensor, temperature: torch.Tensor, workspace: torch.Tensor,
               q: Optional[torch.Tensor] = None, draft_tokens: Optional[torch.Tensor] = None,
-              stream=None) -> None:
+              entropy: bool = False, stream=None) -> None:
     """Phase 1 only (``specdec_row_stats``): logits [B, R, V] -> stage partials in the
     workspace.  For the linear form pass q and draft_tokens too (phase 2 needs the
-    drafted tokens' logits and q values, gathered here)."""
+    drafted tokens' logits and q values, gathered here).  ``entropy`` keeps the sums
+    ``row_entropy`` reads."""
     B, R, V = logits.shape
     rc = load_library().specdec_row_stats(
         _ptr(logits), _ptr(q), dtype_code(logits), _ptr(draft_tokens), _ptr(temperature), B, R, V,
-        _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+        STATS_ENTROPY if entropy else 0, _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     _check(rc, "specdec_row_stats")
 
 
@@ -327,3 +339,31 @@ def philox_uniforms(key, counter, first_word: int, n: int, device="cuda", stream
     _check(rc, "specdec_philox_uniforms")
     return out
 
+
+
+def row_entropy(logits: torch.Tensor, temperature: torch.Tensor, workspace: torch.Tensor,
+                stream=None) -> torch.Tensor:
+    """Entropies [B, R] of the target rows of ``logits`` from the workspace of a
+    ``row_stats(..., entropy=True)`` call on those logits (``specdec_row_entropy``)."""
+    B, R, V = logits.shape
+    out = torch.empty((B, R), dtype=torch.float32, device=logits.device)
+    rc = load_library().specdec_row_entropy(_ptr(workspace), workspace.numel(), dtype_code(logits),
+                                            _ptr(temperature), B, R, V, _ptr(out),
+                                            _stream_ptr(stream))
+    _check(rc, "specdec_row_entropy")
+    return out
+
+
+def path_logprob(logits: torch.Tensor, temperature: torch.Tensor, out_tokens: torch.Tensor,
+                 n_accepted: torch.Tensor, workspace: torch.Tensor,
+                 path_nodes: Optional[torch.Tensor] = None,
+                 row_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Log-probabilities [B] of the emitted paths (``specdec_path_logprob``)."""
+    B, R, V = logits.shape
+    out = torch.empty(B, dtype=torch.float32, device=logits.device)
+    rc = load_library().specdec_path_logprob(
+        _ptr(logits), dtype_code(logits), _ptr(temperature), _ptr(out_tokens), _ptr(n_accepted),
+        _ptr(path_nodes), _ptr(row_status), B, R, V, out_tokens.shape[1], _ptr(workspace),
+        workspace.numel(), _ptr(out), _stream_ptr(stream))
+    _check(rc, "specdec_path_logprob")
+    return out

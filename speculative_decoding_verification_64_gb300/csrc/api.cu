@@ -72,7 +72,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPECDEC_OK : SPECDEC_
 
 int launch_stats(const void *logits, const void *q, int dtype, const int32_t *tokens,
                  const float *temperature, int B, int R, int V, void *workspace,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, bool entropy = false) {
   const long long rows = (long long)B * R;
   const int spr = stages_per_row(V, elem_bytes(dtype));
   RowStatsParams p;
@@ -85,6 +85,7 @@ int launch_stats(const void *logits, const void *q, int dtype, const int32_t *to
   p.V = V;
   p.spr = spr;
   p.B = B;
+  p.entropy = entropy ? 1 : 0;
   p.tokens = tokens;
   p.q = q;
   p.ws = linear_ws(workspace, B, R, V, dtype);
@@ -118,7 +119,8 @@ size_t specdec_workspace_size(int B, int rows_per_request, int V, int dtype) {
 
 int specdec_row_stats(const void *logits, const void *q, int dtype, const int32_t *draft_tokens,
                       const float *temperature, int B, int rows_per_request, int V,
-                      void *workspace, size_t workspace_bytes, void *stream) {
+                      unsigned flags, void *workspace, size_t workspace_bytes, void *stream) {
+  if (flags & ~(unsigned)SPECDEC_STATS_ENTROPY) return SPECDEC_ERR_INVALID_ARG;
   int st = check_sizes(B, rows_per_request, V, dtype);
   if (st != SPECDEC_OK) return st;
   if (B == 0) return SPECDEC_OK;
@@ -131,7 +133,7 @@ int specdec_row_stats(const void *logits, const void *q, int dtype, const int32_
   if (st != SPECDEC_OK) return st;
   return launch_stats(logits, linear ? q : nullptr, dtype, linear ? draft_tokens : nullptr,
                       temperature, B, rows_per_request, V, workspace,
-                      static_cast<cudaStream_t>(stream));
+                      static_cast<cudaStream_t>(stream), (flags & SPECDEC_STATS_ENTROPY) != 0);
 }
 
 static int linear_checks(const void *logits, const void *q, int dtype, const int32_t *tokens,
@@ -326,6 +328,51 @@ int specdec_philox_uniforms(const uint64_t *key, const uint64_t *counter,
   p.n = n;
   p.out = out;
   return cuda_status(launch_philox_uniforms(p, static_cast<cudaStream_t>(stream)));
+}
+
+int specdec_row_entropy(const void *workspace, size_t workspace_bytes, int dtype,
+                        const float *temperature, int B, int rows_per_request, int V,
+                        float *entropy, void *stream) {
+  int st = check_sizes(B, rows_per_request, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  if (B == 0) return SPECDEC_OK;
+  if (!temperature || !entropy) return SPECDEC_ERR_INVALID_ARG;
+  st = check_workspace(workspace, workspace_bytes, B, rows_per_request, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  return cuda_status(launch_row_entropy(reinterpret_cast<const RowPartial *>(workspace),
+                                        temperature, B, rows_per_request,
+                                        stages_per_row(V, elem_bytes(dtype)), entropy,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int specdec_path_logprob(const void *logits, int dtype, const float *temperature,
+                         const int32_t *out_tokens, const int32_t *n_accepted,
+                         const int32_t *path_nodes, const int32_t *row_status, int B,
+                         int rows_per_request, int V, int path_len, const void *workspace,
+                         size_t workspace_bytes, float *logprob, void *stream) {
+  int st = check_sizes(B, rows_per_request, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  if (B == 0) return SPECDEC_OK;
+  if (!logits || !temperature || !out_tokens || !n_accepted || !logprob || path_len < 1)
+    return SPECDEC_ERR_INVALID_ARG;
+  st = check_workspace(workspace, workspace_bytes, B, rows_per_request, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  PathLogprobParams p;
+  p.logits = logits;
+  p.part = reinterpret_cast<const RowPartial *>(workspace);
+  p.temperature = temperature;
+  p.out_tokens = out_tokens;
+  p.n_accepted = n_accepted;
+  p.path_nodes = path_nodes;
+  p.row_status = row_status;
+  p.logprob = logprob;
+  p.dtype = dtype;
+  p.B = B;
+  p.R = rows_per_request;
+  p.V = V;
+  p.spr = stages_per_row(V, elem_bytes(dtype));
+  p.path_len = path_len;
+  return cuda_status(launch_path_logprob(p, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

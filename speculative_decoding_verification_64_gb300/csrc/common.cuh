@@ -16,7 +16,9 @@ namespace specdec {
 struct RowPartial {
   float m;        // max of the raw logits in the stage (NaN if one is NaN, -inf if none finite)
   float s;        // sum over the stage of 2^((l - m) c), c = log2(e) / T
-  int32_t arg;    // first index holding m (greedy rows only; else INT_MAX)
+  int32_t arg;    // greedy rows: first index holding m; other rows: INT_MAX, or (stats
+                  // pass with SPECDEC_STATS_ENTROPY) the float bits of the stage's
+                  // sum of 2^((l - m) c) (l - m), for the row entropy
   int32_t flags;  // SPECDEC_ROW_INTERNAL when a bounded wait ran out
 };
 static_assert(sizeof(RowPartial) == 16, "RowPartial is 16 bytes");
@@ -85,6 +87,7 @@ struct RowStatsParams {
   int dtype;
   int R, V, spr;     // rows per request, vocabulary, stages per row
   int B;
+  int entropy;       // also the entropy sums of non-greedy rows (in RowPartial::arg)
   // Linear form only (tokens == nullptr otherwise): row i < R - 1 of request b
   // scores draft token tokens[b * (R - 1) + i].  The pass gathers that token's
   // logit and q value and zeroes the draw kernel's tickets.
@@ -139,12 +142,28 @@ struct PhiloxParams {
   float *out;
 };
 
+// Path log-probability of a verify step's outputs (see row_extras.cu).
+struct PathLogprobParams {
+  const void *logits;
+  const RowPartial *part;
+  const float *temperature;
+  const int32_t *out_tokens;   // [B, path_len]
+  const int32_t *n_accepted;   // [B]
+  const int32_t *path_nodes;   // [B, path_len] (tree form) or NULL (linear form: row j = j)
+  const int32_t *row_status;   // [B] or NULL
+  float *logprob;              // [B]
+  int dtype, B, R, V, spr, path_len;
+};
+
 // Multiprocessor count of the current device (looked up once per device).
 int device_sm_count();
 cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream);
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream);
 cudaError_t launch_tree_finalize(const TreeFinalizeParams &p, cudaStream_t stream);
 cudaError_t launch_philox_uniforms(const PhiloxParams &p, cudaStream_t stream);
+cudaError_t launch_row_entropy(const RowPartial *part, const float *temperature, int B, int R,
+                               int spr, float *entropy, cudaStream_t stream);
+cudaError_t launch_path_logprob(const PathLogprobParams &p, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // device helpers

@@ -44,7 +44,8 @@ struct StatsSmem {
   volatile int abort_flag;
 };
 
-template <int DT>
+// kA: also the entropy sums of non-greedy rows (SPECDEC_STATS_ENTROPY).
+template <int DT, bool kA>
 __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   StatsSmem &sm = *reinterpret_cast<StatsSmem *>(smem_raw);
@@ -203,7 +204,13 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
         r.arg = warp_min(first_idx);
         r.s = (wm == -INFINITY) ? 0.0f : 1.0f;
       } else if (wm != -INFINITY) {
-        r.s = warp_sum(lane_sum<DT>(d, temperature_scale(T), wm));
+        if (kA) {
+          float a;
+          r.s = warp_sum(lane_sum_a<DT>(d, temperature_scale(T), wm, a));
+          r.arg = __float_as_int(warp_sum(a));  // sum of e (l - m); arg is for greedy rows only
+        } else {
+          r.s = warp_sum(lane_sum<DT>(d, temperature_scale(T), wm));
+        }
       }
     }
     if (lane == 0) p.part[(long long)row * p.spr + u.j0 + t] = r;
@@ -211,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
   (void)kPerVec;
 }
 
-template <int DT>
+template <int DT, bool kA>
 cudaError_t launch_dt(const RowStatsParams &p, cudaStream_t stream) {
   static bool attr_set[64] = {};
   int dev = 0;
@@ -219,7 +226,7 @@ cudaError_t launch_dt(const RowStatsParams &p, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   const int smem = (int)sizeof(StatsSmem);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    err = cudaFuncSetAttribute(row_stats_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(row_stats_kernel<DT, kA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                smem);
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
@@ -227,7 +234,7 @@ cudaError_t launch_dt(const RowStatsParams &p, cudaStream_t stream) {
   const long long units = p.stages / p.spr * ((p.spr + kUnit - 1) / kUnit);
   long long grid = device_sm_count();
   if (grid > units) grid = units;
-  row_stats_kernel<DT><<<(unsigned)grid, kThreads, smem, stream>>>(p);
+  row_stats_kernel<DT, kA><<<(unsigned)grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -235,8 +242,11 @@ cudaError_t launch_dt(const RowStatsParams &p, cudaStream_t stream) {
 
 cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream) {
   if (p.stages <= 0) return cudaSuccess;
-  return p.dtype == SPECDEC_F32 ? launch_dt<SPECDEC_F32>(p, stream)
-                                : launch_dt<SPECDEC_BF16>(p, stream);
+  if (p.entropy)
+    return p.dtype == SPECDEC_F32 ? launch_dt<SPECDEC_F32, true>(p, stream)
+                                  : launch_dt<SPECDEC_BF16, true>(p, stream);
+  return p.dtype == SPECDEC_F32 ? launch_dt<SPECDEC_F32, false>(p, stream)
+                                : launch_dt<SPECDEC_BF16, false>(p, stream);
 }
 
 namespace {

@@ -212,6 +212,86 @@ __device__ __forceinline__ float lane_sum(const LaneData<DT> &d, float c, float 
   return (acc0.x + acc0.y) + e;
 }
 
+// -inf logits (masked tokens) become the most negative finite value before the
+// sums below: their weight is 0 either way, and 0 * (l - m) stays 0.
+__device__ __forceinline__ uint32_t bf16x2_floor_finite(uint32_t w) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0xFF7FFF7Fu));
+  return r;
+}
+
+// Over the lane's elements (packed fp32x2 math): the sum of e = 2^((l - m) c),
+// returned, and in `a` the sum of e (l - m) (every term <= 0), from which the
+// row's entropy follows: H = ln S - A / (T S) for the merged S and A.
+template <int DT>
+__device__ __forceinline__ float lane_sum_a(const LaneData<DT> &d, float c, float m, float &a) {
+  const float2 cc = make_float2(c, c);
+  const float2 nm = make_float2(-m, -m);
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
+  float2 aa0 = acc0, aa1 = acc0;
+#pragma unroll
+  for (int k = 0; k < kVecPerLane; ++k) {
+    const uint4 w = d.v[k];
+    if (DT == SPECDEC_F32) {
+      const float2 d0 = __fadd2_rn(make_float2(fmaxf(__uint_as_float(w.x), -FLT_MAX),
+                                               fmaxf(__uint_as_float(w.y), -FLT_MAX)), nm);
+      const float2 d1 = __fadd2_rn(make_float2(fmaxf(__uint_as_float(w.z), -FLT_MAX),
+                                               fmaxf(__uint_as_float(w.w), -FLT_MAX)), nm);
+      float2 x0 = __fmul2_rn(d0, cc), x1 = __fmul2_rn(d1, cc);
+      x0.x = ex2_approx(x0.x);
+      x0.y = ex2_approx(x0.y);
+      x1.x = ex2_approx(x1.x);
+      x1.y = ex2_approx(x1.y);
+      if (k & 1) {
+        acc2 = __fadd2_rn(acc2, x0);
+        acc3 = __fadd2_rn(acc3, x1);
+      } else {
+        acc0 = __fadd2_rn(acc0, x0);
+        acc1 = __fadd2_rn(acc1, x1);
+      }
+      aa0 = __ffma2_rn(x0, d0, aa0);
+      aa1 = __ffma2_rn(x1, d1, aa1);
+    } else {
+      const uint32_t wx = bf16x2_floor_finite(w.x), wy = bf16x2_floor_finite(w.y);
+      const uint32_t wz = bf16x2_floor_finite(w.z), ww = bf16x2_floor_finite(w.w);
+      const float2 d0 = __fadd2_rn(make_float2(bf16_lo(wx), bf16_hi(wx)), nm);
+      const float2 d1 = __fadd2_rn(make_float2(bf16_lo(wy), bf16_hi(wy)), nm);
+      const float2 d2 = __fadd2_rn(make_float2(bf16_lo(wz), bf16_hi(wz)), nm);
+      const float2 d3 = __fadd2_rn(make_float2(bf16_lo(ww), bf16_hi(ww)), nm);
+      float2 x0 = __fmul2_rn(d0, cc), x1 = __fmul2_rn(d1, cc);
+      float2 x2 = __fmul2_rn(d2, cc), x3 = __fmul2_rn(d3, cc);
+      x0.x = ex2_approx(x0.x);
+      x0.y = ex2_approx(x0.y);
+      x1.x = ex2_approx(x1.x);
+      x1.y = ex2_approx(x1.y);
+      x2.x = ex2_approx(x2.x);
+      x2.y = ex2_approx(x2.y);
+      x3.x = ex2_approx(x3.x);
+      x3.y = ex2_approx(x3.y);
+      acc0 = __fadd2_rn(acc0, x0);
+      acc1 = __fadd2_rn(acc1, x1);
+      acc2 = __fadd2_rn(acc2, x2);
+      acc3 = __fadd2_rn(acc3, x3);
+      aa0 = __ffma2_rn(x0, d0, aa0);
+      aa1 = __ffma2_rn(x1, d1, aa1);
+      aa0 = __ffma2_rn(x2, d2, aa0);
+      aa1 = __ffma2_rn(x3, d3, aa1);
+    }
+  }
+  acc0 = __fadd2_rn(acc0, acc1);
+  acc2 = __fadd2_rn(acc2, acc3);
+  acc0 = __fadd2_rn(acc0, acc2);
+  aa0 = __fadd2_rn(aa0, aa1);
+  float e = 0.0f, ae = 0.0f;
+  if (d.edge != -INFINITY) {
+    const float de = d.edge - m;
+    e = ex2_approx(de * c);
+    ae = e * de;
+  }
+  a = (aa0.x + aa0.y) + ae;
+  return (acc0.x + acc0.y) + e;
+}
+
 // First index (in the row) of a lane element equal to wm, INT_MAX if none.
 // Fully unrolled so the stage stays in registers.
 template <int DT>

@@ -88,11 +88,13 @@ def test_argument_checks_before_any_device_work(lib):
     assert vt(N, N, BF16, N, N, N, N, 2, 2000, 1000, 5, N, N, N, N, N, N, N, N, 0, N) == 2
     assert vt(N, N, BF16, N, N, N, N, 2, 64, 1000, 65, N, N, N, N, N, N, N, N, 0, N) == 2
     rs = lib.specdec_row_stats
-    assert rs(N, N, BF16, N, N, 0, 9, 1000, N, 0, N) == 0
-    assert rs(N, N, BF16, N, N, 2, 9, 1000, N, 0, N) == 1
+    assert rs(N, N, BF16, N, N, 0, 9, 1000, 0, N, 0, N) == 0
+    assert rs(N, N, BF16, N, N, 2, 9, 1000, 0, N, 0, N) == 1
     # q without draft tokens (or the reverse) is rejected
-    assert rs(d, d, BF16, N, d, 2, 9, 1000, d, 1 << 30, N) == 1
-    assert rs(d, N, BF16, d, d, 2, 9, 1000, d, 1 << 30, N) == 1
+    assert rs(d, d, BF16, N, d, 2, 9, 1000, 0, d, 1 << 30, N) == 1
+    assert rs(d, N, BF16, d, d, 2, 9, 1000, 0, d, 1 << 30, N) == 1
+    # unknown flag bits
+    assert rs(d, N, BF16, N, d, 2, 9, 1000, 2, d, 1 << 30, N) == 1
 
 
 def test_binding_refuses_to_run_without_the_library(tmp_path):
@@ -126,3 +128,19 @@ def test_philox_argument_checks(lib):
     assert ph(k, c, 0, 4, N, N) == 1                    # null output
     assert ph(k, c, 2**64 - 3, 4, d, N) == 1            # word range beyond 2^64
     assert ph(k, c, 0, (1 << 40) + 1, d, N) == 2        # beyond SPECDEC_MAX_UNIFORMS
+
+
+def test_entropy_and_path_logprob_argument_checks(lib):
+    from speculative_decoding_verification_64_gb300.binding import BF16
+    N = None
+    d = ctypes.c_void_p(16)
+    en = lib.specdec_row_entropy
+    assert en(N, 0, BF16, N, 0, 9, 1000, N, N) == 0               # B = 0
+    assert en(d, 1 << 30, BF16, N, 2, 9, 1000, d, N) == 1         # no temperature
+    assert en(d, 8, BF16, d, 2, 9, 1000, d, N) == 3               # workspace too small
+    assert en(d, 1 << 30, 7, d, 2, 9, 1000, d, N) == 1            # dtype
+    pl = lib.specdec_path_logprob
+    assert pl(N, BF16, N, N, N, N, N, 0, 9, 1000, 9, N, 0, N, N) == 0
+    assert pl(d, BF16, d, d, d, N, N, 2, 9, 1000, 0, d, 1 << 30, d, N) == 1   # path_len 0
+    assert pl(d, BF16, d, N, d, N, N, 2, 9, 1000, 9, d, 1 << 30, d, N) == 1   # no tokens
+    assert pl(d, BF16, d, d, d, N, N, 2, 9, 1000, 9, d, 8, d, N) == 3         # workspace

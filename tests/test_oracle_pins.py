@@ -707,3 +707,77 @@ def test_philox_uniforms_match_the_workload_stream(oracle_lib, seed, shape, offs
     assert got.dtype == np.float32
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
     assert (got > 0).all() and (got < 1).all()
+
+
+# --- per-row entropy and path log-probability -------------------------------
+
+def test_entropy_of_a_uniform_row_is_log_v(oracle_lib):
+    for V in (1, 2, 7, 1000):
+        lg = np.zeros((1, 2, V), dtype=np.float32)
+        h = oracle_lib.row_entropy(lg, "f32", np.array([0.9], dtype=np.float32))
+        assert np.allclose(h, math.log(V), atol=1e-12, rtol=0)
+
+
+def test_entropy_matches_scipy_and_the_binary_closed_form(oracle_lib):
+    rng = np.random.default_rng(5)
+    lg = (rng.normal(size=(3, 4, 500)) * 2).astype(np.float32)
+    T = np.array([1.0, 0.37, 2.5], dtype=np.float32)
+    h = oracle_lib.row_entropy(lg, "f32", T)
+    for b in range(3):
+        for i in range(4):
+            p = special.softmax(lg[b, i].astype(np.float64) / float(T[b]))
+            assert abs(h[b, i] - stats.entropy(p)) < 1e-10
+    # two tokens, logits (0, x): binary entropy of sigmoid(x / T)
+    for x, t in ((0.0, 1.0), (1.5, 0.5), (-3.0, 2.0)):
+        lg2 = np.array([[[0.0, x]]], dtype=np.float32)
+        s = 1.0 / (1.0 + math.exp(-x / t))
+        want = -(s * math.log(s) + (1 - s) * math.log(1 - s))
+        got = oracle_lib.row_entropy(lg2, "f32", np.array([t], dtype=np.float32))[0, 0]
+        assert abs(got - want) < 1e-12
+
+
+def test_entropy_special_rows(oracle_lib):
+    lg = np.zeros((4, 1, 6), dtype=np.float32)
+    lg[1, 0, :3] = -np.inf                  # masked half: uniform over the rest
+    lg[2, 0, 2] = np.nan
+    T = np.array([0.0, 1.0, 1.0, -1.0], dtype=np.float32)
+    h = oracle_lib.row_entropy(lg, "f32", T)[:, 0]
+    assert h[0] == 0.0                      # greedy: one-hot
+    assert abs(h[1] - math.log(3)) < 1e-12
+    assert np.isnan(h[2]) and np.isnan(h[3])
+
+
+def test_path_logprob_matches_log_softmax(oracle_lib):
+    rng = np.random.default_rng(6)
+    B, R, V = 5, 4, 300
+    lg = (rng.normal(size=(B, R, V)) * 2).astype(np.float32)
+    T = np.array([1.0, 0.6, 1.7, 1.0, 0.8], dtype=np.float32)
+    toks = rng.integers(0, V, size=(B, R)).astype(np.int32)
+    nacc = np.array([0, 1, 3, 2, 3], dtype=np.int32)
+    got = oracle_lib.path_logprob(lg, "f32", T, toks, nacc)
+    for b in range(B):
+        want = sum(special.log_softmax(lg[b, j].astype(np.float64) / float(T[b]))[toks[b, j]]
+                   for j in range(nacc[b] + 1))
+        assert abs(got[b] - want) < 1e-10
+    # tree form: rows named by the path, here the nodes 0, 2, 3
+    nodes = np.tile(np.array([[0, 2, 3, -1]], dtype=np.int32), (B, 1))
+    nacc2 = np.full(B, 2, dtype=np.int32)
+    got2 = oracle_lib.path_logprob(lg, "f32", T, toks, nacc2, path_nodes=nodes)
+    for b in range(B):
+        want = sum(special.log_softmax(lg[b, r].astype(np.float64) / float(T[b]))[toks[b, j]]
+                   for j, r in enumerate((0, 2, 3)))
+        assert abs(got2[b] - want) < 1e-10
+
+
+def test_path_logprob_special_cases(oracle_lib):
+    lg = np.zeros((4, 2, 5), dtype=np.float32)
+    lg[:, :, 3] = 1.0                       # argmax 3 in every row
+    T = np.array([0.0, 0.0, 1.0, 1.0], dtype=np.float32)
+    toks = np.array([[3, 3], [3, 1], [3, 9], [3, 3]], dtype=np.int32)
+    nacc = np.array([1, 1, 1, 1], dtype=np.int32)
+    status = np.array([0, 0, 0, 2], dtype=np.int32)
+    got = oracle_lib.path_logprob(lg, "f32", T, toks, nacc, row_status=status)
+    assert got[0] == 0.0                    # greedy path of arg-maxima
+    assert got[1] == -np.inf                # greedy path through a non-maximum
+    assert np.isnan(got[2])                 # token out of range
+    assert np.isnan(got[3])                 # malformed request
