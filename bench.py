@@ -56,6 +56,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="skip timing the step replayed from CUDA graphs (reported beside the "
+                         "eager value, never instead of it)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (a smaller case for profiling; not a bench line)")
     ap.add_argument("--vocab", type=int, default=None,
@@ -351,6 +354,41 @@ def run_ours(args, dist):
                 "peak_kind": peak_kind, "traffic": traffic,
                 "algorithmic_bytes_per_launch": int(k_bytes), "avg_launch_us": round(k1_ms * 1e3, 2)}
 
+    # ---- the same steps replayed from CUDA graphs (launch-bound sizes) ----
+    graph = None
+    if args.graph:
+        # a serving loop replays one graph on fixed buffers: up to 4 graphs here
+        # (fewer than the eager rotation leaves the small inputs warm in L2)
+        n_graphs = min(n_sets, 4)
+        graphs = []
+        for i in range(n_graphs):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                x = sets[i]
+                if linear:
+                    binding.row_stats(x[0], x[3], ws, q=x[1], draft_tokens=x[2])
+                    binding.linear_finalize(*x, out, ws)
+                else:
+                    binding.row_stats(x[0], x[4], ws)
+                    binding.tree_finalize(*x, w.max_depth, out, ws)
+            graphs.append(g)
+        for s_ in range(max(args.warmup, 3)):
+            graphs[s_ % n_graphs].replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        dist.barrier()
+        torch.cuda.synchronize()
+        g0.record()
+        for s_ in range(K):
+            graphs[s_ % n_graphs].replay()
+        g1.record()
+        torch.cuda.synchronize()
+        g_ms = dist.max(g0.elapsed_time(g1), device)
+        graph = {"ms_per_step": round(g_ms / K, 5),
+                 "value": round(dist.sum(units, device) * K / (g_ms / 1e3), 1),
+                 "unit": "positions/s", "graphs": n_graphs, "l2_warm": n_graphs < n_sets}
+
     # ---- e2e: pinned host buffers through the public verify call ----
     e2e = run_e2e(args, w, linear, device, stream, dist, units)
 
@@ -384,6 +422,7 @@ def run_ours(args, dist):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": kernels * K,
+        "graph": graph,
         "clocks": clocks,
     }
     if dist.rank == 0:
