@@ -56,6 +56,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--topk", type=int, default=0,
+                    help="linear workloads: time specdec_verify_linear_topk (the top-k residual "
+                         "approximation) with this many candidates instead of the exact step")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="skip timing the step replayed from CUDA graphs (reported beside the "
                          "eager value, never instead of it)")
@@ -295,17 +298,26 @@ def run_ours(args, dist):
         else:
             binding.tree_finalize(*x, w.max_depth, out, ws, stream=stream)
 
+    topk = args.topk if linear else 0
+
     def step(s):
         x = sets[s % n_sets]
+        if topk:
+            binding.verify_linear_topk(*x, topk, out=out, workspace=ws, stream=stream)
+            return
         stats(x)
         finalize(x)
 
     def step_timed(s, e0, e1, e2):
         x = sets[s % n_sets]
         e0.record(stream)
-        stats(x)
-        e1.record(stream)
-        finalize(x)
+        if topk:  # one call: the stats pass and the top-k draw, timed together
+            binding.verify_linear_topk(*x, topk, out=out, workspace=ws, stream=stream)
+            e1.record(stream)
+        else:
+            stats(x)
+            e1.record(stream)
+            finalize(x)
         e2.record(stream)
 
     for s in range(max(args.warmup, 3)):
@@ -338,17 +350,22 @@ def run_ours(args, dist):
     value = dist.sum(units, device) * K / (total_ms / 1e3)
 
     # rejected requests in the last step: their q row is part of the algorithmic bytes
+    # (the top-k approximation reads none of it)
     nb = out.is_bonus.cpu().numpy()
-    rejected = float((nb == 0).sum())
+    rejected = 0.0 if topk else float((nb == 0).sum())
     ab = algorithmic_bytes(w, rejected)
     gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
 
     # roofline of the dominant kernel (row statistics)
     spr = -(-w.V * es // 8192)
-    kname, k_bytes = "row_stats_kernel", ab["logits"] + w.B * R * spr * 16
+    if topk:  # both launches of the call, timed together
+        kname, k_bytes = "row_stats_kernel + topk_draw_kernel", ab["total"]
+        traffic = None
+    else:
+        kname, k_bytes = "row_stats_kernel", ab["logits"] + w.B * R * spr * 16
+        traffic = ncu_traffic(_workload_name(args), kname)
     k_gbs = k_bytes / (k1_ms / 1e3) / 1e9
-    traffic = ncu_traffic(_workload_name(args), kname)
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(k_gbs, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(k_gbs / peak, 4),
                 "peak_kind": peak_kind, "traffic": traffic,
@@ -356,7 +373,7 @@ def run_ours(args, dist):
 
     # ---- the same steps replayed from CUDA graphs (launch-bound sizes) ----
     graph = None
-    if args.graph:
+    if args.graph and not topk:
         # a serving loop replays one graph on fixed buffers: up to 4 graphs here
         # (fewer than the eager rotation leaves the small inputs warm in L2)
         n_graphs = min(n_sets, 4)
@@ -409,7 +426,7 @@ def run_ours(args, dist):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic",
-        "config": _config(w, _workload_name(args), linear, l2_note),
+        "config": _config(w, _workload_name(args), linear, l2_note, topk),
         "requests_per_s": round(dist.sum(w.B, device) * K / (total_ms / 1e3), 1),
         "accepted_tokens_per_s": round(dist.sum(float(out.n_accepted.sum().item() + w.B), device)
                                        * K / (total_ms / 1e3), 1),
@@ -417,7 +434,8 @@ def run_ours(args, dist):
         "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
         "frac_of_measured_hbm": round(gbs / peak, 4),
         "algorithmic_bytes_per_step": int(ab["total"]),
-        "phase_us": {"row_stats": round(k1_ms * 1e3, 2), "finalize": round(k2_ms * 1e3, 2)},
+        "phase_us": ({"verify_topk": round(k1_ms * 1e3, 2)} if topk else
+                     {"row_stats": round(k1_ms * 1e3, 2), "finalize": round(k2_ms * 1e3, 2)}),
         "roofline": roofline,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -456,8 +474,10 @@ def _host_set_bytes(w) -> int:
     return int(sum(a.nbytes for a in arrs))
 
 
-def _config(w, name, linear, l2_note):
+def _config(w, name, linear, l2_note, topk=0):
     c = {"workload": name, "B": w.B, "V": w.V, "dtype": w.dtype, "l2": l2_note}
+    if topk:
+        c["topk_residual"] = topk  # the approximate correction draw, not the exact method
     if linear:
         c["gamma"] = w.gamma
         c["greedy_requests"] = int((w.temperature == 0).sum())

@@ -88,6 +88,7 @@ extern "C" {
 #define SPECDEC_MAX_TREE_DEPTH 64
 #define SPECDEC_MAX_V (1 << 21)
 #define SPECDEC_MAX_UNIFORMS (1ll << 40) /* words per specdec_philox_uniforms call */
+#define SPECDEC_MAX_TOPK 1024            /* candidates of specdec_verify_linear_topk */
 
 /* ABI version of the loaded library (SPECDEC_ABI_VERSION at build time). */
 int specdec_abi_version(void);
@@ -227,6 +228,28 @@ int specdec_tree_finalize(const void *logits, const void *q, int dtype,
                           int32_t *out_tokens, int32_t *final_token, uint8_t *is_bonus,
                           int32_t *row_status, float *p_node, void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/*
+ * The linear step with the top-k residual: an APPROXIMATION of step 4 after
+ * the implementation note of section 15.1.2 (precompute the residual
+ * probabilities of the top-k candidates instead of the whole vocabulary).
+ * At a rejection at row k the correction token is drawn from max(0, p - q)
+ * restricted to the topk tokens of largest p_k (ties to the lower index) and
+ * renormalised; if that mass is 0, from p_k restricted to the candidates.
+ * The q row is then read at topk tokens only.  The law of the emitted token
+ * is no longer exactly p: its total-variation distance from the exact step's
+ * law is the residual mass outside the candidates over the residual mass
+ * (the oracle reports it per request).  The accept test, the bonus draw and
+ * the greedy rows are exact.  Same arguments and outputs as
+ * specdec_verify_linear plus topk in [1, SPECDEC_MAX_TOPK] (values above V
+ * act as V, which is the exact step); same workspace size.
+ */
+int specdec_verify_linear_topk(const void *logits, const void *q, int dtype,
+                               const int32_t *draft_tokens, const float *temperature,
+                               const float *uniforms, int B, int gamma, int V, int topk,
+                               int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
+                               uint8_t *is_bonus, int32_t *row_status, float *p_draft,
+                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Entropy -sum_v p ln p (natural log) of every target row, for policies that

@@ -65,6 +65,9 @@ def _load():
         lib.specdec_oracle_verify_tree.restype = i
         lib.specdec_oracle_num_threads.argtypes = []
         lib.specdec_oracle_num_threads.restype = i
+        lib.specdec_oracle_verify_linear_topk.argtypes = [p, p, i, p, p, p, i, i, i, i,
+                                                          p, p, p, p, p, p, p, p, p]
+        lib.specdec_oracle_verify_linear_topk.restype = i
         lib.specdec_oracle_row_entropy.argtypes = [p, i, p, i, i, i, p]
         lib.specdec_oracle_row_entropy.restype = None
         lib.specdec_oracle_path_logprob.argtypes = [p, i, p, p, p, p, p, i, i, i, i, p]
@@ -103,10 +106,6 @@ def philox_uniforms(key, counter, first: int, n: int) -> np.ndarray:
     _load().specdec_oracle_philox_uniforms(k.ctypes.data, c.ctypes.data, int(first), int(n),
                                            out.ctypes.data)
     return out
-
-
-def _ptr(a):
-    return None if a is None else a.ctypes.data
 
 
 def row_entropy(logits: np.ndarray, dtype: str, temperature: np.ndarray) -> np.ndarray:
@@ -191,6 +190,40 @@ def verify_linear(logits, q, dtype, draft_tokens, temperature, uniforms,
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return out
+
+
+def verify_linear_topk(logits, q, dtype, draft_tokens, temperature, uniforms, topk: int) -> dict:
+    """The linear step with the top-k residual (see specdec_oracle.c): the same
+    outputs as ``verify_linear`` plus p_draft, ratio, final_margin and tv [B] (total
+    variation between the exact residual law and the top-k one; NaN where no
+    residual draw happened)."""
+    lib = _load()
+    logits = _storage(logits, dtype)
+    q = _storage(q, dtype)
+    B, R, V = logits.shape
+    gamma = R - 1
+    toks = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, gamma)
+    temp = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
+    uni = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, R)
+    out = dict(
+        n_accepted=np.empty(B, np.int32), out_tokens=np.empty((B, R), np.int32),
+        final_token=np.empty(B, np.int32), is_bonus=np.empty(B, np.uint8),
+        row_status=np.empty(B, np.int32), p_draft=np.empty((B, gamma)),
+        ratio=np.empty((B, gamma)), final_margin=np.empty(B), tv=np.empty(B))
+    rc = lib.specdec_oracle_verify_linear_topk(
+        _ptr(logits), _ptr(q), _dtype_code(dtype), _ptr(toks), _ptr(temp), _ptr(uni),
+        B, gamma, V, int(topk), _ptr(out["n_accepted"]), _ptr(out["out_tokens"]),
+        _ptr(out["final_token"]), _ptr(out["is_bonus"]), _ptr(out["row_status"]),
+        _ptr(out["p_draft"]), _ptr(out["ratio"]), _ptr(out["final_margin"]), _ptr(out["tv"]))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def verify_linear_topk_workload(w, topk: int) -> dict:
+    """Top-k residual oracle on a ``workloads.LinearWorkload``."""
+    return verify_linear_topk(w.logits, w.q, w.dtype, w.draft_tokens, w.temperature,
+                              w.uniforms, topk)
 
 
 def verify_tree(logits, q, dtype, node_tokens, parent, temperature, uniforms,

@@ -167,6 +167,39 @@ static int cdf_draw(const double *w, int V, double U, double *margin) {
  *   final_margin [B]      distance of U*Z to the nearest CDF boundary / Z;
  *   row_diag [B, gamma, 2] per drafted row: sum_x min(p,q), sum_x max(0,p-q).
  * Returns 0, or -1 on a bad argument. */
+/* Candidate set of the top-k residual (the chapter's implementation note:
+ * precompute the residual probabilities of the top-k candidates instead of
+ * the whole vocabulary): the k tokens of largest target probability, ties to
+ * the lower index.  in_k[v] = 1 for them. */
+static const double *g_sort_p; /* comparator context (one sort per thread at a time) */
+#pragma omp threadprivate(g_sort_p)
+static int by_p_desc(const void *a, const void *b) {
+  const int i = *(const int *)a, j = *(const int *)b;
+  if (g_sort_p[i] > g_sort_p[j]) return -1;
+  if (g_sort_p[i] < g_sort_p[j]) return 1;
+  return (i > j) - (i < j);
+}
+
+static void topk_candidates(const double *p, int V, int k, unsigned char *in_k) {
+  int *idx = (int *)malloc(sizeof(int) * (size_t)V);
+  for (int v = 0; v < V; ++v) {
+    idx[v] = v;
+    in_k[v] = 0;
+  }
+  g_sort_p = p;
+  qsort(idx, (size_t)V, sizeof(int), by_p_desc);
+  for (int j = 0; j < k && j < V; ++j) in_k[idx[j]] = 1;
+  free(idx);
+}
+
+static int verify_linear_impl(const void *logits, const void *q, int dtype,
+                              const int32_t *draft_tokens, const float *temperature,
+                              const float *uniforms, int B, int gamma, int V, int topk,
+                              int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
+                              uint8_t *is_bonus, int32_t *row_status, double *p_draft,
+                              double *ratio, double *final_margin, double *row_diag,
+                              double *tv);
+
 int specdec_oracle_verify_linear(const void *logits, const void *q, int dtype,
                                  const int32_t *draft_tokens, const float *temperature,
                                  const float *uniforms, int B, int gamma, int V,
@@ -174,6 +207,39 @@ int specdec_oracle_verify_linear(const void *logits, const void *q, int dtype,
                                  int32_t *final_token, uint8_t *is_bonus,
                                  int32_t *row_status, double *p_draft, double *ratio,
                                  double *final_margin, double *row_diag) {
+  return verify_linear_impl(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
+                            0, n_accepted, out_tokens, final_token, is_bonus, row_status,
+                            p_draft, ratio, final_margin, row_diag, NULL);
+}
+
+/* The linear step with the top-k residual (an approximation: the law of the
+ * correction token is no longer max(0, p - q) / Z).  At a rejection the
+ * residual is restricted to the top-k candidates of p and renormalised; if
+ * it has no mass there, the draw uses p restricted to the candidates.  The
+ * bonus draw is unchanged.  tv[b] (NULL to skip) = total-variation distance
+ * between the exact residual law and the one drawn from = 1 - Z_K / Z for a
+ * rejected request whose exact residual has mass (Z_K the residual mass on
+ * the candidates), else NaN. */
+int specdec_oracle_verify_linear_topk(const void *logits, const void *q, int dtype,
+                                      const int32_t *draft_tokens, const float *temperature,
+                                      const float *uniforms, int B, int gamma, int V, int topk,
+                                      int32_t *n_accepted, int32_t *out_tokens,
+                                      int32_t *final_token, uint8_t *is_bonus,
+                                      int32_t *row_status, double *p_draft, double *ratio,
+                                      double *final_margin, double *tv) {
+  if (topk < 1) return -1;
+  return verify_linear_impl(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
+                            topk, n_accepted, out_tokens, final_token, is_bonus, row_status,
+                            p_draft, ratio, final_margin, NULL, tv);
+}
+
+static int verify_linear_impl(const void *logits, const void *q, int dtype,
+                              const int32_t *draft_tokens, const float *temperature,
+                              const float *uniforms, int B, int gamma, int V, int topk,
+                              int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
+                              uint8_t *is_bonus, int32_t *row_status, double *p_draft,
+                              double *ratio, double *final_margin, double *row_diag,
+                              double *tv) {
   if (B < 0 || gamma < 1 || V < 1 || (dtype != OR_DT_F32 && dtype != OR_DT_BF16)) return -1;
   const int R = gamma + 1;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -205,6 +271,7 @@ int specdec_oracle_verify_linear(const void *logits, const void *q, int dtype,
       if (p_draft) for (int i = 0; i < gamma; ++i) p_draft[(size_t)b * gamma + i] = NAN;
       if (ratio) for (int i = 0; i < gamma; ++i) ratio[(size_t)b * gamma + i] = NAN;
       if (final_margin) final_margin[b] = NAN;
+      if (tv) tv[b] = NAN;
       continue;
     }
 
@@ -250,14 +317,29 @@ int specdec_oracle_verify_linear(const void *logits, const void *q, int dtype,
     /* step 4: residual at the rejected row, or the bonus row */
     const double *Pk = P + (size_t)k * V;
     double Z = 0.0;
+    if (tv) tv[b] = NAN;
     if (k < gamma) {
       for (int v = 0; v < V; ++v) {
         double d = Pk[v] - load_elem(q, dtype, qbase + (size_t)k * V + v);
         w[v] = d > 0.0 ? d : 0.0;
         Z += w[v];
       }
-      if (!(Z > 0.0))
+      if (topk > 0) {
+        /* top-k residual: keep the candidates' weights only */
+        unsigned char *in_k = (unsigned char *)malloc((size_t)V);
+        topk_candidates(Pk, V, topk, in_k);
+        double ZK = 0.0;
+        for (int v = 0; v < V; ++v) {
+          if (!in_k[v]) w[v] = 0.0;
+          ZK += w[v];
+        }
+        if (tv && Z > 0.0) tv[b] = 1.0 - ZK / Z;
+        if (!(ZK > 0.0))
+          for (int v = 0; v < V; ++v) w[v] = in_k[v] ? Pk[v] : 0.0;
+        free(in_k);
+      } else if (!(Z > 0.0)) {
         for (int v = 0; v < V; ++v) w[v] = Pk[v];
+      }
     } else {
       for (int v = 0; v < V; ++v) w[v] = Pk[v];
     }

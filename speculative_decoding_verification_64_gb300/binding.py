@@ -44,6 +44,12 @@ _EXPORTS = {
                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                               ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "specdec_verify_linear_topk": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                    ctypes.c_void_p], ctypes.c_int),
     "specdec_row_stats": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                            ctypes.c_uint, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p],
@@ -215,6 +221,22 @@ def verify_linear(logits: torch.Tensor, q: torch.Tensor, draft_tokens: torch.Ten
 
 
 STATS_ENTROPY = 1
+
+
+def verify_linear_topk(logits: torch.Tensor, q: torch.Tensor, draft_tokens: torch.Tensor,
+                       temperature: torch.Tensor, uniforms: torch.Tensor, topk: int,
+                       out: Optional[LinearOut] = None, workspace: Optional[torch.Tensor] = None,
+                       stream=None) -> LinearOut:
+    """Linear verify with the top-k residual approximation (``specdec_verify_linear_topk``)."""
+    B, gamma, V, dt, out, ws = _linear_args(logits, q, draft_tokens, temperature, uniforms,
+                                            out, workspace)
+    rc = load_library().specdec_verify_linear_topk(
+        _ptr(logits), _ptr(q), dt, _ptr(draft_tokens), _ptr(temperature), _ptr(uniforms),
+        B, gamma, V, int(topk), _ptr(out.n_accepted), _ptr(out.out_tokens),
+        _ptr(out.final_token), _ptr(out.is_bonus), _ptr(out.row_status), _ptr(out.p_draft),
+        _ptr(ws), ws.numel(), _stream_ptr(stream))
+    _check(rc, "specdec_verify_linear_topk")
+    return out
 
 
 def row_stats(logits: torch.Tensor, temperature: torch.Tensor, workspace: torch.Tensor,

@@ -375,4 +375,25 @@ int specdec_path_logprob(const void *logits, int dtype, const float *temperature
   return cuda_status(launch_path_logprob(p, static_cast<cudaStream_t>(stream)));
 }
 
+int specdec_verify_linear_topk(const void *logits, const void *q, int dtype,
+                               const int32_t *draft_tokens, const float *temperature,
+                               const float *uniforms, int B, int gamma, int V, int topk,
+                               int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
+                               uint8_t *is_bonus, int32_t *row_status, float *p_draft,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+  if (topk < 1) return SPECDEC_ERR_INVALID_ARG;
+  if (topk > SPECDEC_MAX_TOPK) return SPECDEC_ERR_UNSUPPORTED;
+  int st = linear_checks(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
+                         n_accepted, out_tokens, final_token, is_bonus, row_status, workspace,
+                         workspace_bytes);
+  if (st != SPECDEC_OK || B == 0) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = launch_stats(logits, q, dtype, draft_tokens, temperature, B, gamma + 1, V, workspace, s);
+  if (st != SPECDEC_OK) return st;
+  const LinearFinalizeParams p =
+      linear_params(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
+                    n_accepted, out_tokens, final_token, is_bonus, row_status, p_draft, workspace);
+  return cuda_status(launch_linear_topk(p, topk, s));
+}
+
 }  // extern "C"

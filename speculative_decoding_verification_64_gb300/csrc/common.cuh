@@ -159,6 +159,7 @@ struct PathLogprobParams {
 int device_sm_count();
 cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream);
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream);
+cudaError_t launch_linear_topk(const LinearFinalizeParams &p, int topk, cudaStream_t stream);
 cudaError_t launch_tree_finalize(const TreeFinalizeParams &p, cudaStream_t stream);
 cudaError_t launch_philox_uniforms(const PhiloxParams &p, cudaStream_t stream);
 cudaError_t launch_row_entropy(const RowPartial *part, const float *temperature, int B, int R,

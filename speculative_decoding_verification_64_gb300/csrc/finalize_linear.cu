@@ -592,7 +592,313 @@ cudaError_t launch_bulk(const LinearFinalizeParams &p, unsigned grid, cudaStream
   return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------------------
+// The linear draw with the top-k residual: an approximation of step 4 after
+// the chapter's implementation note (precompute the residual probabilities of
+// the top-k candidates instead of the whole vocabulary).  At a rejection the
+// residual max(0, p - q) is restricted to the k tokens of largest p (ties to
+// the lower index) and renormalised; with no mass there, p restricted to the
+// candidates.  The bonus draw is exact.  One CTA per request:
+//   * the accept test as in the chunked draw;
+//   * candidates: radix select of the k-th largest logit key (8 bits a pass:
+//     two passes for bf16, four for float32), then a collection pass in index
+//     order (block scans of the per-thread counts, ties at the threshold to
+//     the lower index);
+//   * weights of the candidates only (q is gathered at k tokens, never read
+//     as a row), each as 40-bit fixed point; inverse CDF in index order.
+// ---------------------------------------------------------------------------
+namespace topk {
+
+struct Smem {
+  DrawSmem d;
+  unsigned int hist[kWarps][256];  // per-warp digit counts
+  unsigned int prefix;             // key bits fixed so far
+  int need;                        // candidates still to place among keys with that prefix
+  int eq_total;                    // keys equal to the threshold
+  unsigned int n_cand;
+  unsigned int taken;
+  int cand[SPECDEC_MAX_TOPK];
+  unsigned long long w[SPECDEC_MAX_TOPK];
+  unsigned long long red[2 * kWarps];
+};
+
+// Order-preserving unsigned key of a logit's bits (bf16: 16 bits; float32: 32).
+template <int DT>
+__device__ __forceinline__ uint32_t order_key_bits(uint32_t b) {
+  if (DT == SPECDEC_F32) return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+}
+
+// The keys of the elements of "vector" vi of a row (16 bytes: 8 bf16 or 4
+// float32 elements), `in` clear past V.  16-byte loads when the row is
+// aligned, else element loads.
+template <int DT>
+struct VecKeys {
+  static constexpr int kN = (DT == SPECDEC_F32) ? 4 : 8;
+  uint32_t key[kN];
+  bool in[kN];
+  __device__ __forceinline__ void load(const uint8_t *row, bool aligned, int vi, int V, bool valid) {
+    constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    const int v0 = vi * kN;
+    if (valid && aligned && v0 + kN <= V) {
+      const uint4 x = __ldg(reinterpret_cast<const uint4 *>(row) + vi);
+      w[0] = x.x;
+      w[1] = x.y;
+      w[2] = x.z;
+      w[3] = x.w;
+#pragma unroll
+      for (int e = 0; e < kN; ++e) in[e] = true;
+    } else {
+#pragma unroll
+      for (int e = 0; e < kN; ++e) {
+        const int v = v0 + e;
+        in[e] = valid && v < V;
+        uint32_t bits = 0;
+        if (in[e]) {
+          bits = (DT == SPECDEC_F32) ? __ldg(reinterpret_cast<const uint32_t *>(row) + v)
+                                     : (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(row) + v);
+        }
+        if (DT == SPECDEC_F32) w[e] = bits;
+        else w[e >> 1] |= bits << (16 * (e & 1));
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < kN; ++e) {
+      const uint32_t bits = (DT == SPECDEC_F32) ? w[e] : ((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+      key[e] = order_key_bits<DT>(bits);
+    }
+    (void)es;
+  }
+};
+
+// Exclusive block scan of one 32-bit count per thread (in thread order).
+__device__ __forceinline__ unsigned block_exscan_u32(unsigned v, unsigned long long *red,
+                                                    unsigned &total) {
+  unsigned long long tot64;
+  Red rr{red, 0};
+  const unsigned long long e = block_exscan_u64(v, rr, tot64);
+  total = (unsigned)tot64;
+  __syncthreads();
+  return (unsigned)e;
+}
+
+// One radix pass: counts of digit (key >> shift) & 255 over the keys whose
+// bits above the digit equal those of `prefix`; then the digit holding the
+// need-th largest of them is fixed.  Warp-aggregated atomics (a warp adds
+// once per distinct digit).
+template <int DT>
+__device__ __forceinline__ void radix_pass(const uint8_t *row, bool aligned, int V, int shift,
+                                           Smem &sm) {
+  constexpr int kN = VecKeys<DT>::kN;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < kWarps * 256; i += kThreads) (&sm.hist[0][0])[i] = 0u;
+  __syncthreads();
+  const uint32_t prefix = sm.prefix;
+  const uint32_t hi_mask = (shift + 8 >= 32) ? 0u : (0xFFFFFFFFu << (shift + 8));
+  const int nvec = (V + kN - 1) / kN;
+  constexpr int kU = 4;  // vectors in flight per lane
+  for (int base = warp * 32; base < nvec; base += kU * kThreads) {
+    VecKeys<DT> vk[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int vi = base + u * kThreads + lane;
+      vk[u].load(row, aligned, vi, V, vi < nvec);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+#pragma unroll
+      for (int e = 0; e < kN; ++e) {
+        const bool match = vk[u].in[e] && (vk[u].key[e] & hi_mask) == (prefix & hi_mask);
+        const uint32_t bin = match ? ((vk[u].key[e] >> shift) & 0xFFu) : (256u + lane);
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (match && lane == __ffs(peers) - 1)
+          atomicAdd(&sm.hist[warp][bin], (unsigned)__popc(peers));
+      }
+    }
+  }
+  __syncthreads();
+  {
+    unsigned t = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t += sm.hist[w][tid];
+    __syncthreads();
+    sm.hist[0][tid] = t;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int need = sm.need, dgt = 255;
+    for (; dgt > 0; --dgt) {
+      if ((int)sm.hist[0][dgt] >= need) break;
+      need -= (int)sm.hist[0][dgt];
+    }
+    sm.need = need;
+    sm.eq_total = (int)sm.hist[0][dgt];
+    sm.prefix = prefix | ((uint32_t)dgt << shift);
+  }
+  __syncthreads();
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) topk_draw_kernel(const LinearFinalizeParams p, int topk) {
+  __shared__ Smem sm;
+  constexpr int kBits = (DT == SPECDEC_F32) ? 32 : 16;
+  constexpr int kN = VecKeys<DT>::kN;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long b = blockIdx.x;
+  const int gamma = p.gamma, R = gamma + 1, V = p.V;
+  const LinearDecision d = request_decision<DT>(p, b, true, sm.d);
+  if (d.status || d.greedy) return;
+  const int k = d.k;
+  if (k == gamma) {
+    // bonus draw: exact, this CTA alone (chunk totals, then the search)
+    Red rr{sm.d.red, 0};
+    const Draw w = make_draw<DT>(p, b, d);
+    for (int ch = 0; ch < p.nchunk; ++ch) {
+      const unsigned long long t = block_sum_u64(thread_sum<DT>(w, ch * kChunk + tid * kPerT), rr);
+      if (tid == 0) p.ws.chunk_tot[b * p.ntot + ch] = t;
+    }
+    __syncthreads();
+    request_search<DT>(p, b, k, w, rr, sm.d);
+    return;
+  }
+  constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
+  const uint8_t *lrow = reinterpret_cast<const uint8_t *>(p.logits) + (size_t)(b * R + k) * V * es;
+  const uint8_t *qrow = reinterpret_cast<const uint8_t *>(p.q) + (size_t)(b * gamma + k) * V * es;
+  const bool aligned = (reinterpret_cast<uintptr_t>(lrow) & 15) == 0;
+  const int K = min(topk, V);
+  // ---- radix select of the K-th largest key --------------------------------
+  if (tid == 0) {
+    sm.prefix = 0;
+    sm.need = K;
+    sm.n_cand = 0;
+    sm.taken = 0;
+  }
+  __syncthreads();
+  for (int shift = kBits - 8; shift >= 0; shift -= 8) radix_pass<DT>(lrow, aligned, V, shift, sm);
+  const uint32_t thr = sm.prefix;      // the K-th largest key
+  const int need_eq = sm.need;          // how many keys equal to it are candidates
+  const bool all_eq = need_eq == sm.eq_total;
+  // ---- candidates: keys above the threshold (and every tie when all are needed) --
+  const int nvec = (V + kN - 1) / kN;
+  constexpr int kU = 4;
+  for (int base = warp * 32; base < nvec; base += kU * kThreads) {
+    VecKeys<DT> vk[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int vi = base + u * kThreads + lane;
+      vk[u].load(lrow, aligned, vi, V, vi < nvec);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+#pragma unroll
+      for (int e = 0; e < kN; ++e) {
+        if (vk[u].in[e] && (vk[u].key[e] > thr || (all_eq && vk[u].key[e] == thr))) {
+          const unsigned pos = atomicAdd(&sm.n_cand, 1u);
+          sm.cand[pos] = (base + u * kThreads + lane) * kN + e;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (!all_eq) {
+    // only the first need_eq ties (by index): rounds of kThreads vectors in order
+    const unsigned start = sm.n_cand;
+    for (int base = 0; base < nvec; base += kThreads) {
+      VecKeys<DT> vk;
+      vk.load(lrow, aligned, base + tid, V, base + tid < nvec);
+      unsigned c = 0;
+#pragma unroll
+      for (int e = 0; e < kN; ++e) c += (vk.in[e] && vk.key[e] == thr) ? 1u : 0u;
+      unsigned round_total;
+      const unsigned pre = block_exscan_u32(c, sm.red, round_total);
+      unsigned rank = sm.taken + pre;
+#pragma unroll
+      for (int e = 0; e < kN; ++e) {
+        if (vk.in[e] && vk.key[e] == thr) {
+          if (rank < (unsigned)need_eq) sm.cand[start + rank] = (base + tid) * kN + e;
+          ++rank;
+        }
+      }
+      __syncthreads();
+      if (tid == 0) sm.taken += round_total;
+      __syncthreads();
+      if (sm.taken >= (unsigned)need_eq) break;
+    }
+  }
+  __syncthreads();
+  // ---- candidates in index order: bitonic sort of K (padded to a power of two) --
+  int n2 = 1;
+  while (n2 < K) n2 <<= 1;
+  for (int j = K + tid; j < n2; j += kThreads) sm.cand[j] = 0x7FFFFFFF;
+  __syncthreads();
+  for (int size = 2; size <= n2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < n2; i += kThreads) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const int a = sm.cand[i], c = sm.cand[j];
+          const bool up = (i & size) == 0;
+          if ((a > c) == up) {
+            sm.cand[i] = c;
+            sm.cand[j] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // ---- candidate weights and the draw ------------------------------------------
+  unsigned long long zk = 0;
+  for (int j = tid; j < K; j += kThreads) {
+    const int v = sm.cand[j];
+    const float lv = load_elem(lrow, DT, v), qv = load_elem(qrow, DT, v);
+    const float ev = ex2_approx((lv - d.M) * d.c);
+    const unsigned long long f = to_fixed40(fmaxf(fmaf(-d.S, qv, ev), 0.0f));
+    sm.w[j] = f;
+    zk += f;
+  }
+  Red rr{sm.red, 0};
+  const unsigned long long Zr = block_sum_u64(zk, rr);
+  __syncthreads();
+  if (Zr == 0) {  // no residual mass on the candidates: p on them
+    for (int j = tid; j < K; j += kThreads) {
+      const float lv = load_elem(lrow, DT, sm.cand[j]);
+      sm.w[j] = to_fixed40(ex2_approx((lv - d.M) * d.c));
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    unsigned long long Z = 0;
+    for (int j = 0; j < K; ++j) Z += sm.w[j];
+    const unsigned long long target = uniform_target(__ldg(p.uniforms + b * R + gamma), Z);
+    int tok = sm.cand[K - 1];
+    unsigned long long run = 0;
+    for (int j = 0; j < K; ++j) {
+      run += sm.w[j];
+      if (run > target) {
+        tok = sm.cand[j];
+        break;
+      }
+    }
+    p.final_token[b] = tok;
+    p.out_tokens[b * R + k] = tok;
+  }
+}
+
+}  // namespace topk
+
 }  // namespace
+
+cudaError_t launch_linear_topk(const LinearFinalizeParams &p, int topk, cudaStream_t stream) {
+  if (p.B <= 0) return cudaSuccess;
+  if (p.dtype == SPECDEC_F32)
+    topk::topk_draw_kernel<SPECDEC_F32><<<(unsigned)p.B, kThreads, 0, stream>>>(p, topk);
+  else
+    topk::topk_draw_kernel<SPECDEC_BF16><<<(unsigned)p.B, kThreads, 0, stream>>>(p, topk);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream) {
   if (p.B <= 0) return cudaSuccess;

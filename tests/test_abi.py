@@ -144,3 +144,13 @@ def test_entropy_and_path_logprob_argument_checks(lib):
     assert pl(d, BF16, d, d, d, N, N, 2, 9, 1000, 0, d, 1 << 30, d, N) == 1   # path_len 0
     assert pl(d, BF16, d, N, d, N, N, 2, 9, 1000, 9, d, 1 << 30, d, N) == 1   # no tokens
     assert pl(d, BF16, d, d, d, N, N, 2, 9, 1000, 9, d, 8, d, N) == 3         # workspace
+
+
+def test_topk_argument_checks(lib):
+    from speculative_decoding_verification_64_gb300.binding import BF16
+    N = None
+    vt = lib.specdec_verify_linear_topk
+    assert vt(N, N, BF16, N, N, N, 0, 8, 1000, 16, N, N, N, N, N, N, N, 0, N) == 0   # B = 0
+    assert vt(N, N, BF16, N, N, N, 4, 8, 1000, 0, N, N, N, N, N, N, N, 0, N) == 1    # topk < 1
+    assert vt(N, N, BF16, N, N, N, 4, 8, 1000, 1025, N, N, N, N, N, N, N, 0, N) == 2  # > max
+    assert vt(N, N, BF16, N, N, N, 4, 8, 1000, 16, N, N, N, N, N, N, N, 0, N) == 1   # nulls

@@ -1,0 +1,60 @@
+"""The top-k residual approximation (specdec_verify_linear_topk) against its
+float64 oracle statement, and its distance from the exact step."""
+import numpy as np
+import pytest
+
+from parity import compare_linear
+from speculative_decoding_verification_64_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+KEYS = ("n_accepted", "out_tokens", "final_token", "is_bonus", "row_status", "p_draft")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    from speculative_decoding_verification_64_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def gpu_topk(w, topk):
+    import torch
+    from speculative_decoding_verification_64_gb300 import binding
+    out = binding.verify_linear_topk(*binding.linear_inputs_to_device(w), topk)
+    torch.cuda.synchronize()
+    return {k: getattr(out, k).cpu().numpy() for k in KEYS}
+
+
+@pytest.mark.parametrize("name,B,V,topk", [
+    ("linear_b256_g8_v128256_bf16", 32, 128256, 32),
+    ("linear_b256_g8_v128256_bf16", 32, 128256, 1024),
+    ("mixed_b512_g4_v152064_bf16", 48, 20011, 64),     # greedy rows, several temperatures
+    ("linear_b64_g5_v32000_bf16", 24, None, 8),
+    ("linear_b1_g4_v32000_f32", 24, None, 100),          # float32 keys: four radix passes
+])
+def test_topk_parity(oracle_lib, name, B, V, topk):
+    w = W.make_workload(name, B=B, V=V)
+    g = gpu_topk(w, topk)
+    o = oracle_lib.verify_linear_topk_workload(w, topk)
+    rep = compare_linear(w, g, o)
+    tv = o["tv"][np.isfinite(o["tv"])]
+    print(name, topk, rep, "mean TV %.3g max TV %.3g over %d corrections"
+          % (tv.mean() if tv.size else 0, tv.max() if tv.size else 0, tv.size))
+
+
+def test_topk_with_the_whole_vocabulary_is_the_exact_step(oracle_lib):
+    w = W.make_workload("linear_b64_g5_v32000_bf16", B=16, V=700)
+    g = gpu_topk(w, 1024)
+    compare_linear(w, g, oracle_lib.verify_linear_workload(w))
+
+
+def test_topk_ties_small_vocabularies_and_statuses(oracle_lib):
+    w = W.make_linear("normal2_tq08", B=12, gamma=3, V=300, dtype="bf16", seed=41)
+    w.logits[:, :, 10:40] = w.logits[0, 0, 7]      # ties among large logits
+    w.logits[2, 1, 5] = 0x7FC0                     # NaN: malformed
+    w.temperature[3] = 0.0                         # greedy
+    for topk in (1, 5, 31, 300):
+        g = gpu_topk(w, topk)
+        compare_linear(w, g, oracle_lib.verify_linear_topk_workload(w, topk))

@@ -781,3 +781,70 @@ def test_path_logprob_special_cases(oracle_lib):
     assert got[1] == -np.inf                # greedy path through a non-maximum
     assert np.isnan(got[2])                 # token out of range
     assert np.isnan(got[3])                 # malformed request
+
+
+# --- top-k residual (an approximate mode of the correction draw) -------------
+
+def test_topk_residual_with_every_token_is_the_exact_step(oracle_lib):
+    w = W.make_workload("linear_b64_g5_v32000_bf16", B=12, V=3001)
+    exact = oracle_lib.verify_linear_workload(w)
+    approx = oracle_lib.verify_linear_topk_workload(w, topk=w.V)
+    for k in ("n_accepted", "out_tokens", "final_token", "is_bonus", "row_status"):
+        assert np.array_equal(exact[k], approx[k]), k
+    assert np.nanmax(np.abs(approx["tv"])) < 1e-12
+
+
+def test_topk_tv_is_the_mass_outside_the_candidates(oracle_lib):
+    w = W.make_workload("linear_b256_g8_v128256_bf16", B=10, V=4000)
+    K = 16
+    got = oracle_lib.verify_linear_topk_workload(w, topk=K)
+    logits = W.decode(w.logits, w.dtype).astype(np.float64)
+    qd = W.decode(w.q, w.dtype).astype(np.float64)
+    for b in range(w.B):
+        k = got["n_accepted"][b]
+        if got["row_status"][b] or k == w.gamma:
+            assert np.isnan(got["tv"][b])
+            continue
+        p = special.softmax(logits[b, k] / float(w.temperature[b]))
+        r = np.maximum(p - qd[b, k], 0.0)
+        cand = np.lexsort((np.arange(w.V), -p))[:K]          # largest p, ties to the lower index
+        assert abs(got["tv"][b] - (1.0 - r[cand].sum() / r.sum())) < 1e-12
+        assert got["final_token"][b] in set(cand.tolist())
+
+
+def test_topk_candidates_break_ties_by_index(oracle_lib):
+    # p ties on tokens 1, 2, 3; q puts no mass there, so every residual draw is a candidate
+    lg = np.array([[[0.0, 2.0, 2.0, 2.0, 1.0], [0.0] * 5]], dtype=np.float32)
+    q = np.array([[[0.97, 0.0, 0.0, 0.0, 0.03]]], dtype=np.float32)
+    toks = np.array([[0]], dtype=np.int32)
+    seen = set()
+    for u1 in np.linspace(0.01, 0.99, 41):
+        uni = np.array([[0.9999, u1]], dtype=np.float32)        # reject draft 0
+        out = oracle_lib.verify_linear_topk(lg, q, "f32", toks, np.array([1.0], np.float32), uni, 2)
+        seen.add(int(out["final_token"][0]))
+    assert seen == {1, 2}
+
+
+def test_topk_law_by_monte_carlo(oracle_lib):
+    """gamma = 1: the first emitted token has law min(p, q) + Z * r_K / Z_K."""
+    rng = np.random.default_rng(9)
+    V, K, n = 6, 2, 200_000
+    lg = rng.normal(size=V).astype(np.float32)
+    p = special.softmax(lg.astype(np.float64))
+    qv = rng.dirichlet(np.ones(V)).astype(np.float32)
+    qd = qv.astype(np.float64)
+    toks = rng.choice(V, size=n, p=qd / qd.sum()).astype(np.int32)
+    logits = np.broadcast_to(np.stack([lg, lg])[None], (n, 2, V)).copy()
+    q = np.broadcast_to(qv[None, None], (n, 1, V)).copy()
+    uni = W.philox_uniforms(77, (n, 2))
+    out = oracle_lib.verify_linear_topk(logits, q, "f32", toks[:, None],
+                                        np.ones(n, np.float32), uni, K)
+    first = out["out_tokens"][:, 0]
+    r = np.maximum(p - qd, 0.0)
+    cand = np.argsort(-p, kind="stable")[:K]
+    rk = np.zeros(V)
+    rk[cand] = r[cand]
+    law = np.minimum(p, qd) + r.sum() * rk / rk.sum()
+    freq = np.bincount(first, minlength=V) / n
+    se = np.sqrt(law * (1 - law) / n)
+    assert (np.abs(freq - law) <= 5 * se + 1e-9).all()
