@@ -58,3 +58,22 @@ def test_topk_ties_small_vocabularies_and_statuses(oracle_lib):
     for topk in (1, 5, 31, 300):
         g = gpu_topk(w, topk)
         compare_linear(w, g, oracle_lib.verify_linear_topk_workload(w, topk))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_topk_rows_without_a_usable_sample_threshold(oracle_lib, dtype):
+    """Rows whose candidate count a sampled threshold cannot bound: constant rows
+    (every key ties), and rows whose large logits sit on a regular comb of
+    positions (a strided sample sees mostly them, so its estimate keeps too few
+    candidates).  Both take the full radix select; results stay the oracle's."""
+    V = 20011
+    w = W.make_linear("normal2_tq08", B=10, gamma=3, V=V, dtype=dtype, seed=57)
+    x = W.decode(w.logits, dtype)
+    x[0:3] = 0.25                                   # constant rows: all ties
+    comb = np.arange(V)[(np.arange(V) % 40) < 8]    # every fifth 16-byte vector of bf16
+    rng = np.random.default_rng(5)
+    x[3:7][:, :, comb] = 6.0 + rng.standard_normal((4, 4, comb.size))
+    w.logits = W.encode(x, dtype)
+    for topk in (7, 300, 1024):
+        g = gpu_topk(w, topk)
+        compare_linear(w, g, oracle_lib.verify_linear_topk_workload(w, topk))
