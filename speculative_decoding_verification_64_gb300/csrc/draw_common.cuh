@@ -291,8 +291,17 @@ __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const
     return;
   }
   bool use_q = d.k < gamma;
-  unsigned long long Z = 0;
-  for (int s = lane; s < rq.nst; s += 32) Z += __ldcg(tot + s);
+  const float U = __ldg(p.uniforms + b * R + gamma);
+  // rows of at most 64 stages keep their stage totals in registers (two per lane)
+  const bool cached = rq.nst <= 64;
+  unsigned long long c0 = 0, c1 = 0, Z = 0;
+  if (cached) {
+    c0 = (lane < rq.nst) ? __ldcg(tot + lane) : 0ull;
+    c1 = (lane + 32 < rq.nst) ? __ldcg(tot + lane + 32) : 0ull;
+    Z = c0 + c1;
+  } else {
+    for (int s = lane; s < rq.nst; s += 32) Z += __ldcg(tot + s);
+  }
   Z = warp_sum_u64(Z);
   if (Z == 0 && use_q) {
     // residual mass 0 (only by rounding): draw from p itself
@@ -309,14 +318,18 @@ __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const
       Z += acc;
     }
     __syncwarp();
+    if (cached) {
+      c0 = (lane < rq.nst) ? __ldcg(tot + lane) : 0ull;
+      c1 = (lane + 32 < rq.nst) ? __ldcg(tot + lane + 32) : 0ull;
+    }
   }
-  const float U = __ldg(p.uniforms + b * R + gamma);
   const unsigned long long target = uniform_target(U, Z);
   // the stage holding the crossing
   unsigned long long base = 0;
   int st = -1;
   for (int s0 = 0; s0 < rq.nst && st < 0; s0 += 32) {
-    const unsigned long long v = (s0 + lane < rq.nst) ? __ldcg(tot + s0 + lane) : 0ull;
+    const unsigned long long v = cached ? (s0 == 0 ? c0 : c1)
+                                        : ((s0 + lane < rq.nst) ? __ldcg(tot + s0 + lane) : 0ull);
     const unsigned long long incl = warp_incl_scan_u64(v, lane);
     const unsigned m = __ballot_sync(0xffffffffu, target < base + incl);
     if (m) {

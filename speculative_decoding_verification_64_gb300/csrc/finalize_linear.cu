@@ -339,6 +339,7 @@ __device__ __forceinline__ void request_search(const LinearFinalizeParams &p, lo
 // count runs the search.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) linear_draw_kernel(const LinearFinalizeParams p) {
+  pdl_wait();
   __shared__ DrawSmem sm;
   const int tid = threadIdx.x;
   Red rr{sm.red, 0};
@@ -417,6 +418,7 @@ struct Smem {
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFinalizeParams p) {
+  pdl_wait();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
   constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
@@ -441,6 +443,15 @@ __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFina
   }
 
   // ---- head: row merges (16-lane segments over (request, row) pairs) ------
+  // warp j, which runs request j's accept test, loads its inputs first so that
+  // their round trip overlaps the merges
+  DraftIn din;
+  float Tj = 0.0f;
+  if (warp < nreq) {
+    const long long b = (long long)p.B - 1 - (rb0 + warp);
+    Tj = __ldg(p.temperature + b);
+    din = load_draft(p, b, lane);
+  }
   const int pairs = nreq * R;
   for (int base = 0; base < pairs; base += kThreads / kSeg) {
     if (base + warp * (32 / kSeg) >= pairs) continue;  // both segments of this warp idle
@@ -457,10 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFina
   if (warp < nreq) {
     const long long rb = rb0 + warp;
     const long long b = (long long)p.B - 1 - rb;
-    const float T = __ldg(p.temperature + b);
-    const DraftIn din = load_draft(p, b, lane);
     float pd;
-    const LinearDecision d = decide(p, din, T, temperature_scale(T), sm.rs[warp], lane, pd);
+    const LinearDecision d = decide(p, din, Tj, temperature_scale(Tj), sm.rs[warp], lane, pd);
     if (lane == 0) sm.dec[warp] = d;
     if (rb * upr >= lo) write_outputs_warp(p, b, d, pd, lane);  // this CTA holds unit 0
   }
@@ -528,14 +537,14 @@ __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFina
   }
   __syncthreads();
 
-  // ---- tail: tickets, then the searches --------------------------------------
-  if (tid == 0) {
+  // ---- tail: tickets (thread j for request j), then the searches -------------
+  if (tid < nreq) {
     __threadfence();
     const unsigned abort_add = sm.abort_flag ? kAbort : 0u;
-    for (int j = 0; j < nreq; ++j) {
-      const LinearDecision d = sm.dec[j];
-      sm.search[j] = 0;
-      if (d.status || d.greedy) continue;
+    const int j = tid;
+    const LinearDecision d = sm.dec[j];
+    sm.search[j] = 0;
+    if (!(d.status || d.greedy)) {
       const long long rb = rb0 + j;
       const long long u0 = max(lo, rb * upr), u1 = min(hi, (rb + 1) * upr);
       const int s0 = (int)(u0 - rb * upr) * kUnitStages;
@@ -590,8 +599,7 @@ cudaError_t launch_bulk(const LinearFinalizeParams &p, unsigned grid, cudaStream
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
-  bulk::draw_bulk_kernel<DT><<<grid, bulk::kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(bulk::draw_bulk_kernel<DT>, dim3(grid), dim3(bulk::kThreads), (size_t)smem, stream, p);
 }
 
 
@@ -1224,6 +1232,7 @@ __device__ __forceinline__ void bonus_draw(const LinearFinalizeParams &p, long l
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 2) topk_draw_kernel(const LinearFinalizeParams p, int topk) {
+  pdl_wait();
   __shared__ Smem sm;
   const int tid = threadIdx.x;
   const long long b = blockIdx.x;
@@ -1254,10 +1263,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_draw_kernel(const LinearFina
 cudaError_t launch_linear_topk(const LinearFinalizeParams &p, int topk, cudaStream_t stream) {
   if (p.B <= 0) return cudaSuccess;
   if (p.dtype == SPECDEC_F32)
-    topk::topk_draw_kernel<SPECDEC_F32><<<(unsigned)p.B, kThreads, 0, stream>>>(p, topk);
-  else
-    topk::topk_draw_kernel<SPECDEC_BF16><<<(unsigned)p.B, kThreads, 0, stream>>>(p, topk);
-  return cudaGetLastError();
+    return launch_pdl(topk::topk_draw_kernel<SPECDEC_F32>, dim3((unsigned)p.B), dim3(kThreads), 0, stream, p, topk);
+  return launch_pdl(topk::topk_draw_kernel<SPECDEC_BF16>, dim3((unsigned)p.B), dim3(kThreads), 0, stream, p, topk);
 }
 
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream) {
@@ -1276,10 +1283,8 @@ cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t s
   const long long slots = (long long)device_sm_count() * kMinBlocks;
   const unsigned grid = (unsigned)(items < slots ? items : slots);
   if (p.dtype == SPECDEC_F32)
-    linear_draw_kernel<SPECDEC_F32><<<grid, kThreads, 0, stream>>>(p);
-  else
-    linear_draw_kernel<SPECDEC_BF16><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+    return launch_pdl(linear_draw_kernel<SPECDEC_F32>, dim3(grid), dim3(kThreads), 0, stream, p);
+  return launch_pdl(linear_draw_kernel<SPECDEC_BF16>, dim3(grid), dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace specdec

@@ -302,6 +302,8 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
 
 }  // namespace
 
+// A plain launch: with programmatic dependent launch the cluster grid's
+// replays in a CUDA graph measured 11 us slower per step (B=32, N=64).
 cudaError_t launch_tree_finalize(const TreeFinalizeParams &p, cudaStream_t stream) {
   if (p.B <= 0) return cudaSuccess;
   if (p.dtype == SPECDEC_F32)

@@ -47,6 +47,7 @@ struct StatsSmem {
 // kA: also the entropy sums of non-greedy rows (SPECDEC_STATS_ENTROPY).
 template <int DT, bool kA>
 __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsParams p) {
+  pdl_launch_dependents();  // phase 2 waits for this grid's completion itself
   extern __shared__ __align__(128) uint8_t smem_raw[];
   StatsSmem &sm = *reinterpret_cast<StatsSmem *>(smem_raw);
   constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
