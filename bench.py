@@ -288,8 +288,10 @@ def run_ours(args, dist):
         else:
             binding.row_stats(x[0], x[4], ws, stream=stream)
 
-    # one step = the two launches of the public verify call, issued as its
-    # phases so that each kernel is timed on its own
+    # one step = one public verify call (its two launches).  Every
+    # PHASE_EVERY-th timed step is issued as the call's two phases instead,
+    # with events around each, for the per-kernel times; the events cost the
+    # step a few microseconds, so they are kept off the other steps.
     kernels = 2
 
     def finalize(x):
@@ -300,19 +302,26 @@ def run_ours(args, dist):
 
     topk = args.topk if linear else 0
 
-    def step(s):
-        x = sets[s % n_sets]
+    def verify(x, on=stream):
         if topk:
-            binding.verify_linear_topk(*x, topk, out=out, workspace=ws, stream=stream)
-            return
-        stats(x)
-        finalize(x)
+            binding.verify_linear_topk(*x, topk, out=out, workspace=ws, stream=on)
+        elif linear:
+            binding.verify_linear(*x, out=out, workspace=ws, stream=on)
+        else:
+            binding.verify_tree(*x, w.max_depth, out=out, workspace=ws, stream=on)
 
-    def step_timed(s, e0, e1, e2):
+    def step(s):
+        verify(sets[s % n_sets])
+
+    def step_timed(s, ph):
         x = sets[s % n_sets]
+        if ph is None:
+            verify(x)
+            return
+        e0, e1, e2 = ph
         e0.record(stream)
         if topk:  # one call: the stats pass and the top-k draw, timed together
-            binding.verify_linear_topk(*x, topk, out=out, workspace=ws, stream=stream)
+            verify(x)
             e1.record(stream)
         else:
             stats(x)
@@ -325,7 +334,10 @@ def run_ours(args, dist):
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] if s % PHASE_EVERY == 0 else None
+          for s in range(K)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dist.local_rank) if dist.rank == 0 else None
     if sampler:
         sampler.start()
@@ -334,17 +346,19 @@ def run_ours(args, dist):
     torch.cuda.synchronize()
     if sampler:
         sampler.mark("begin")
+    t_begin.record(stream)
     for s in range(K):
-        step_timed(s, *ev[s])
+        step_timed(s, ev[s])
+    t_end.record(stream)
     torch.cuda.synchronize()
     if sampler:
         sampler.mark("end")
     dist.barrier()
     clocks = sampler.stop() if sampler else None
 
-    total_ms = ev[0][0].elapsed_time(ev[-1][2])
-    k1_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
-    k2_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    total_ms = t_begin.elapsed_time(t_end)
+    k1_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev if e is not None]))
+    k2_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev if e is not None]))
     total_ms = dist.max(total_ms, device)
     ms_per_step = total_ms / K
     value = dist.sum(units, device) * K / (total_ms / 1e3)
@@ -381,13 +395,7 @@ def run_ours(args, dist):
         for i in range(n_graphs):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                x = sets[i]
-                if linear:
-                    binding.row_stats(x[0], x[3], ws, q=x[1], draft_tokens=x[2])
-                    binding.linear_finalize(*x, out, ws)
-                else:
-                    binding.row_stats(x[0], x[4], ws)
-                    binding.tree_finalize(*x, w.max_depth, out, ws)
+                verify(sets[i], on=None)
             graphs.append(g)
         for s_ in range(max(args.warmup, 3)):
             graphs[s_ % n_graphs].replay()
@@ -449,6 +457,8 @@ def run_ours(args, dist):
 
 
 L2_BYTES = 129_000_000  # GB300 L2
+PHASE_EVERY = 32        # timed steps per step issued as two phases with events
+E2E_COPY_STREAMS = 4    # streams the e2e host-to-device copies are split over
 
 
 def input_rotation(set_bytes: int):
@@ -504,27 +514,51 @@ def run_e2e(args, w, linear, device, stream, dist, units):
     else:
         host_in = [pinned(w.logits, bf), pinned(w.q, bf), pinned(w.node_tokens),
                    pinned(w.parent), pinned(w.temperature), pinned(w.uniforms)]
-    dev_in = [torch.empty_like(t, device=device) for t in host_in]
+    # two device copies of the inputs: step i+1's copies run while step i
+    # verifies; each copy is split over E2E_COPY_STREAMS streams (several copy
+    # engines), and a set is overwritten only after the verify that read it
+    dev_sets = [[torch.empty_like(t, device=device) for t in host_in] for _ in range(2)]
     out = (binding.LinearOut.empty(w.B, w.gamma, device) if linear
            else binding.TreeOut.empty(w.B, w.N, w.max_depth, device))
-    ws = binding.alloc_workspace(w.B, w.rows, w.V, binding.dtype_code(dev_in[0]), device)
+    ws = binding.alloc_workspace(w.B, w.rows, w.V, binding.dtype_code(dev_sets[0][0]), device)
     out_fields = [f for f in vars(out) if getattr(out, f) is not None]
     host_out = {f: torch.empty_like(getattr(out, f), device="cpu").pin_memory() for f in out_fields}
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    copy_streams = [torch.cuda.Stream(device) for _ in range(E2E_COPY_STREAMS)]
+    read_done = [None, None]  # event: the last verify that read set j has run
 
-    def one():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
+    def one(i, start=None):
+        j = i % 2
+        dev_in = dev_sets[j]
+        ready = []
+        for c, cs in enumerate(copy_streams):
+            if start is not None:
+                cs.wait_event(start)
+            if read_done[j] is not None:
+                cs.wait_event(read_done[j])
+            with torch.cuda.stream(cs):
+                for d, h in zip(dev_in, host_in):
+                    n = d.numel()
+                    lo, hi = n * c // len(copy_streams), n * (c + 1) // len(copy_streams)
+                    if hi > lo:
+                        d.view(-1)[lo:hi].copy_(h.view(-1)[lo:hi], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(cs)
+            ready.append(ev)
+        for ev in ready:
+            stream.wait_event(ev)
         if linear:
             binding.verify_linear(*dev_in, out=out, workspace=ws, stream=stream)
         else:
             binding.verify_tree(*dev_in, w.max_depth, out=out, workspace=ws, stream=stream)
+        read_done[j] = torch.cuda.Event()
+        read_done[j].record(stream)
         for f in out_fields:
             host_out[f].copy_(getattr(out, f), non_blocking=True)
 
-    for _ in range(2):
-        one()
+    for i in range(2):
+        one(i)
     torch.cuda.synchronize()
     n = max(1, min(args.e2e_steps, args.steps))
     e0 = torch.cuda.Event(enable_timing=True)
@@ -532,14 +566,16 @@ def run_e2e(args, w, linear, device, stream, dist, units):
     dist.barrier()
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(n):
-        one()
+    for i in range(n):
+        one(i, start=e0 if i < 2 else None)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = dist.max(e0.elapsed_time(e1), device)
     val = dist.sum(units, device) * n / (ms / 1e3)
     return {"value": round(val, 1), "unit": "positions/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": round(ms / n, 4)}
+            "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": round(ms / n, 4),
+            "h2d_gbs": round(h2d * n / (ms / 1e3) / 1e9, 1), "copy_streams": E2E_COPY_STREAMS,
+            "pipelined": "step i+1's copies overlap step i's verify (two device input sets)"}
 
 
 # ----------------------------------------------------------------------------
