@@ -403,6 +403,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
   }
 }
 
+// Block (bounded) until every bulk copy issued into a ring of `slots` "full"
+// barriers has landed, so that a CTA whose consumers stopped waiting (after
+// some wait gave up) never exits while a copy still writes its shared memory.  Units 0 .. n_issued-1 were
+// issued in order, unit n into slot n % slots; a slot's phases complete in
+// order, so waiting for its last issued phase covers the earlier ones.
+__device__ __forceinline__ void drain_ring(uint64_t *full, int slots, long long n_issued) {
+  for (int s = 0; s < slots && s < n_issued; ++s) {
+    const long long last = s + (long long)slots * ((n_issued - 1 - s) / slots);
+    mbar_wait_bounded(&full[s], (uint32_t)((last / slots) & 1));
+  }
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` of transaction count on
 // `bar`.  Source and destination 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s(void *dst_smem, const void *src_gmem,

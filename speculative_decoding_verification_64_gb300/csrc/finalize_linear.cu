@@ -475,12 +475,13 @@ __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFina
   }
   __syncthreads();
 
+  long long n = 0;  // producer: units issued
   if (warp == kWarps) {
     // ------------------------------ producer ------------------------------
     if (lane == 0) {
       long long rb = rb0;
       int ju = (int)(lo - rb0 * upr);
-      for (long long n = 0; lo + n < hi; ++n) {
+      for (; lo + n < hi; ++n) {
         const uint32_t slot = (uint32_t)(n % kSlots), use = (uint32_t)(n / kSlots);
         if (use > 0 && !mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1)) {
           sm.abort_flag = 1;
@@ -536,6 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFina
     }
   }
   __syncthreads();
+  // after any wait of the CTA gave up, consumers stopped waiting for copies:
+  // the CTA stays until every copy the producer issued has landed
+  if (sm.abort_flag && warp == kWarps && lane == 0) drain_ring(sm.full, kSlots, n);
 
   // ---- tail: tickets (thread j for request j), then the searches -------------
   if (tid < nreq) {

@@ -41,6 +41,7 @@ struct StatsSmem {
   alignas(128) uint8_t stage[kSlots][kUnitBytes];
   alignas(8) uint64_t full[kSlots];
   alignas(8) uint64_t empty[kSlots];
+  volatile long long issued;  // units the producer issued, once it is done (else -1)
   volatile int abort_flag;
 };
 
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
       mbar_init(&sm.empty[i], kUnit);  // one arrival per stage of the unit
     }
     sm.abort_flag = 0;
+    sm.issued = -1;
     fence_mbar_init();
   }
   __syncthreads();
@@ -77,12 +79,13 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
       UnitCursor cur;
       cur.init(first, stride, upr);
       uint32_t slot = 0, use = 0;
-      for (long long i = 0; i < n_local; ++i) {
+      long long i = 0;
+      for (; i < n_local; ++i) {
         if (use > 0 && !mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1)) {
           sm.abort_flag = 1;
-          return;
+          break;
         }
-        if (sm.abort_flag) return;
+        if (sm.abort_flag) break;
         const UnitGeom g = unit_geometry(p.logits, p.V, p.spr, cur.row, cur.ju, es);
         cur.advance(upr);
         if (g.bytes > 0) {
@@ -96,6 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
           ++use;
         }
       }
+      sm.issued = i;
+      if (sm.abort_flag) drain_ring(sm.full, kSlots, i);  // units 0 .. i-1 were issued
     } else if (p.tokens != nullptr) {
       // idle lanes: zero the draw kernel's per-request tickets, which that
       // kernel (launched after this one) counts up from zero
@@ -215,6 +220,14 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
       }
     }
     if (lane == 0) p.part[(long long)row * p.spr + u.j0 + t] = r;
+  }
+  // After any wait of the CTA gave up, the consumers stop waiting for copies:
+  // keep the CTA until every copy the producer issued has landed.
+  if (sm.abort_flag && lane == 0) {
+    const unsigned long long t0 = global_timer_ns();
+    while (sm.issued < 0 && global_timer_ns() - t0 < kWaitLimitNs) {
+    }
+    if (sm.issued >= 0) drain_ring(sm.full, kSlots, sm.issued);
   }
   (void)kPerVec;
 }

@@ -15,9 +15,10 @@ namespace specdec {
 namespace stage {
 
 // Defaults measured on GB300 (B=256, V=128256 bf16): 16 KB copies, 12 slots
-// (192 KB in flight per SM) and 12 consumer warps stream at ~96% of the
-// measured copy bandwidth; 8 KB copies are limited by the per-copy cost and
-// fewer warps by the arithmetic.
+// (192 KB in flight per SM) and 12 consumer warps; 8 KB copies are limited by
+// the per-copy cost.  14 and 15 consumer warps measured faster (92.1 and
+// 89.6 us against 97.0), but two runs with more than 12 consumer warps ended
+// in a GPU fault whose cause is not known, so 12 stays the default.
 #ifndef SPECDEC_K1_WARPS
 #define SPECDEC_K1_WARPS 12
 #endif
