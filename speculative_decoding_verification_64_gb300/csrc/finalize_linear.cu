@@ -403,6 +403,7 @@ constexpr int kSlots = 6;
 constexpr int kWarps = 12;                          // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;         // + the producer warp
 constexpr int kMaxReq = 8;                          // requests in one CTA's run
+static_assert(kWarps <= kSlots * kUnitStages, "no more consumer warps than ring stages");
 constexpr unsigned kAbort = 1u << 24;               // ticket increment of a CTA whose wait ran out
 
 struct Smem {
@@ -520,7 +521,11 @@ __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFina
       const int s = ju * kUnitStages + t;  // stage within the row
       const bool real = !(d.status || d.greedy) && s < nst;
       const bool use_q = d.k < gamma;
-      const bool ok = !sm.abort_flag && mbar_wait_bounded(&sm.full[slot], use & 1);
+      // the slot's previous use released first (see the stats pass: a parity
+      // wait tells only two phases apart, and copies land in any order)
+      const bool ok = !sm.abort_flag &&
+                      (use == 0 || mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1)) &&
+                      mbar_wait_bounded(&sm.full[slot], use & 1);
       if (!ok) sm.abort_flag = 1;
       uint4 lv[kVec], qv[kVec];
       const int sbytes = (ok && real) ? min(kStage, rowbytes - s * kStage) : 0;

