@@ -72,6 +72,8 @@ def _load():
         lib.specdec_oracle_row_entropy.restype = None
         lib.specdec_oracle_path_logprob.argtypes = [p, i, p, p, p, p, p, i, i, i, i, p]
         lib.specdec_oracle_path_logprob.restype = None
+        lib.specdec_oracle_row_alpha.argtypes = [p, p, i, p, i, i, i, p]
+        lib.specdec_oracle_row_alpha.restype = None
         u64 = ctypes.c_uint64
         lib.specdec_oracle_philox_words.argtypes = [p, p, u64, ctypes.c_int64, p]
         lib.specdec_oracle_philox_words.restype = None
@@ -117,6 +119,22 @@ def row_entropy(logits: np.ndarray, dtype: str, temperature: np.ndarray) -> np.n
     out = np.empty((B, R), dtype=np.float64)
     _load().specdec_oracle_row_entropy(lg.ctypes.data, _dtype_code(dtype), tp.ctypes.data,
                                        B, R, V, out.ctypes.data)
+    return out
+
+
+def row_alpha(logits: np.ndarray, q: np.ndarray, dtype: str, temperature: np.ndarray) -> np.ndarray:
+    """float64 [B, gamma]: sum_v min(p_i(v), q_i(v)) of the drafted rows i < gamma, the
+    acceptance probability of one draft from q_i (logits [B, gamma+1, V], q [B, gamma, V],
+    float32 or uint16 bf16 bits)."""
+    B, R, V = logits.shape
+    gamma = R - 1
+    assert q.shape == (B, gamma, V)
+    lg = np.ascontiguousarray(logits)
+    qq = np.ascontiguousarray(q)
+    tp = np.ascontiguousarray(temperature, dtype=np.float32)
+    out = np.empty((B, gamma), dtype=np.float64)
+    _load().specdec_oracle_row_alpha(lg.ctypes.data, qq.ctypes.data, _dtype_code(dtype),
+                                     tp.ctypes.data, B, gamma, V, out.ctypes.data)
     return out
 
 

@@ -634,6 +634,42 @@ void specdec_oracle_row_entropy(const void *logits, int dtype, const float *temp
   }
 }
 
+/* alpha[b * gamma + i] = sum_v min(p_i(v), q_i(v)) for the drafted rows
+ * i < gamma of request b: the probability that the speculative sampling test
+ * accepts one token drawn from q_i (the first term of Lemma 1 in "Chapter 15:
+ * Decoding acceleration", section 15.1.2), the per-position acceptance rate
+ * the chapter's adaptive draft length averages.  p_i as in the verify step
+ * (one-hot at the first arg-max for a greedy row); q_i as stored, not
+ * renormalised.  NaN for an invalid temperature or an unusable target row. */
+void specdec_oracle_row_alpha(const void *logits, const void *q, int dtype,
+                              const float *temperature, int B, int gamma, int V,
+                              double *alpha) {
+  const int R = gamma + 1;
+#pragma omp parallel
+  {
+    double *p = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (long long j = 0; j < (long long)B * gamma; ++j) {
+      const int b = (int)(j / gamma), i = (int)(j % gamma);
+      const float T = temperature[b];
+      const size_t loff = ((size_t)b * R + (size_t)i) * (size_t)V;
+      const size_t qoff = (size_t)j * (size_t)V;
+      if (!temperature_valid(T) || row_nonfinite(logits, dtype, loff, V)) {
+        alpha[j] = NAN;
+        continue;
+      }
+      target_probs(logits, dtype, loff, V, (double)T, p);
+      double a = 0.0;
+      for (int v = 0; v < V; ++v) {
+        const double qv = load_elem(q, dtype, qoff + (size_t)v);
+        a += (p[v] < qv) ? p[v] : qv;
+      }
+      alpha[j] = a;
+    }
+    free(p);
+  }
+}
+
 /* logprob[b] = sum_{j=0..n_accepted[b]} log p_{row_j}(out_tokens[b, j]) with
  * row_j = j (path_nodes NULL, linear form) or path_nodes[b, j] (tree form);
  * out_tokens and path_nodes have rows of path_len entries.  NaN for a

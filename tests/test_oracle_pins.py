@@ -848,3 +848,74 @@ def test_topk_law_by_monte_carlo(oracle_lib):
     freq = np.bincount(first, minlength=V) / n
     se = np.sqrt(law * (1 - law) / n)
     assert (np.abs(freq - law) <= 5 * se + 1e-9).all()
+
+
+# ----------------------------------------------------------------------------
+# per-position acceptance rate alpha = sum_v min(p, q)
+# ----------------------------------------------------------------------------
+
+def test_alpha_matches_the_absolute_difference_form(oracle_lib):
+    """sum min(p, q) = (sum p + sum q - sum |p - q|) / 2 for any nonnegative
+    rows, with p from scipy's softmax and q as stored (not summing to 1)."""
+    rng = np.random.default_rng(11)
+    B, gamma, V = 3, 4, 700
+    lg = (rng.normal(size=(B, gamma + 1, V)) * 2).astype(np.float32)
+    q = rng.dirichlet(np.ones(V), size=(B, gamma)).astype(np.float32) * 1.03
+    T = np.array([1.0, 0.45, 2.2], dtype=np.float32)
+    a = oracle_lib.row_alpha(lg, q, "f32", T)
+    for b in range(B):
+        for i in range(gamma):
+            p = special.softmax(lg[b, i].astype(np.float64) / float(T[b]))
+            qd = q[b, i].astype(np.float64)
+            want = 0.5 * (p.sum() + qd.sum() - np.abs(p - qd).sum())
+            assert abs(a[b, i] - want) < 1e-12
+
+
+def test_alpha_special_rows(oracle_lib):
+    V = 8
+    lg = np.zeros((4, 2, V), dtype=np.float32)
+    q = np.zeros((4, 1, V), dtype=np.float32)
+    # q = p: alpha 1 (uniform rows)
+    q[0, 0] = 1.0 / V
+    # disjoint supports: p on tokens 0..3 (-inf elsewhere), q on 4..7
+    lg[1, 0, 4:] = -np.inf
+    q[1, 0, 4:] = 0.25
+    # greedy row: p one-hot at the first arg-max (token 2), alpha = q(2)
+    lg[2, 0] = [0, 1, 3, 3, 0, 0, 0, 0]
+    q[2, 0] = np.linspace(0.05, 0.2, V)
+    # invalid temperature: NaN
+    q[3, 0] = 1.0 / V
+    T = np.array([1.0, 0.7, 0.0, -1.0], dtype=np.float32)
+    a = oracle_lib.row_alpha(lg, q, "f32", T)[:, 0]
+    assert abs(a[0] - 1.0) < 1e-12
+    assert a[1] == 0.0
+    assert a[2] == np.float64(q[2, 0, 2])
+    assert np.isnan(a[3])
+
+
+def test_alpha_is_the_first_draft_acceptance_rate(oracle_lib):
+    """Monte Carlo through the verify step itself: a draft drawn from q is
+    accepted with probability sum min(p, q)."""
+    rng = np.random.default_rng(12)
+    V, n = 9, 100_000
+    lg = (rng.normal(size=V) * 1.5).astype(np.float32)
+    qv = rng.dirichlet(np.ones(V)).astype(np.float32)
+    qd = qv.astype(np.float64)
+    toks = rng.choice(V, size=n, p=qd / qd.sum()).astype(np.int32)
+    logits = np.broadcast_to(np.stack([lg, lg])[None], (n, 2, V)).copy()
+    q = np.broadcast_to(qv[None, None], (n, 1, V)).copy()
+    T = np.full(n, 0.8, np.float32)
+    out = oracle_lib.verify_linear(logits, q, "f32", toks[:, None], T, W.philox_uniforms(78, (n, 2)),
+                                   diagnostics=False)
+    freq = float((out["n_accepted"] == 1).mean())
+    a = float(oracle_lib.row_alpha(logits[:1], q[:1], "f32", T[:1])[0, 0])
+    assert abs(freq - a) <= 5 * math.sqrt(a * (1 - a) / n)
+
+
+def test_alpha_agrees_with_the_verify_diagnostics(oracle_lib):
+    w = W.make_workload("mixed_b512_g4_v152064_bf16", B=6, V=900)
+    a = oracle_lib.row_alpha(w.logits, w.q, w.dtype, w.temperature)
+    d = oracle_lib.verify_linear_workload(w)["row_diag"][..., 0]
+    ok = np.isfinite(a)
+    assert ok.any()
+    assert np.allclose(a[ok], d[ok], rtol=0, atol=1e-12)
