@@ -287,6 +287,24 @@ int specdec_path_logprob(const void *logits, int dtype, const float *temperature
                          size_t workspace_bytes, float *logprob, void *stream);
 
 /*
+ * Acceptance rate of every drafted position: alpha[b, i] = sum_v
+ * min(p_i(v), q_i(v)), the probability that the test of section 15.1.2
+ * accepts one token drawn from q_i (the first term of Lemma 1; the chapter's
+ * sliding-window draft length averages these rates).  p_i as in the verify
+ * step (greedy rows: one-hot at the first arg-max, so alpha = min(1,
+ * q_i(argmax))); q_i as stored.  Reads the logits and q of a linear verify
+ * call and the workspace of its specdec_row_stats pass (any flags) for the
+ * same B, gamma, V, dtype; a second pass over the drafted logits and q rows
+ * (2 * B * gamma * V * elem bytes), so opt-in.
+ *   logits [B, gamma+1, V], q [B, gamma, V], temperature float32 [B]
+ *   alpha  float32 [B, gamma]; NaN for an invalid temperature or an
+ *          unusable target row
+ */
+int specdec_row_alpha(const void *logits, const void *q, int dtype, const float *temperature,
+                      int B, int gamma, int V, const void *workspace, size_t workspace_bytes,
+                      float *alpha, void *stream);
+
+/*
  * Uniforms on the device for the accept tests and the final draw (section
  * 15.1.2 step 3 draws u ~ U(0,1); the other entry points take them as an
  * input).  Generator: Philox4x64-10 ("Parallel random numbers: as easy as

@@ -40,6 +40,9 @@ _EXPORTS = {
     "specdec_row_entropy": ([ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                              ctypes.c_void_p], ctypes.c_int),
+    "specdec_row_alpha": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                           ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "specdec_path_logprob": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
@@ -373,6 +376,21 @@ def row_entropy(logits: torch.Tensor, temperature: torch.Tensor, workspace: torc
                                             _ptr(temperature), B, R, V, _ptr(out),
                                             _stream_ptr(stream))
     _check(rc, "specdec_row_entropy")
+    return out
+
+
+def row_alpha(logits: torch.Tensor, q: torch.Tensor, temperature: torch.Tensor,
+              workspace: torch.Tensor, stream=None) -> torch.Tensor:
+    """Acceptance rates [B, gamma], sum_v min(p_i, q_i) of every drafted row, from the
+    logits [B, gamma+1, V], q [B, gamma, V] and the workspace of a ``row_stats`` call on
+    those logits (``specdec_row_alpha``)."""
+    B, R, V = logits.shape
+    gamma = R - 1
+    out = torch.empty((B, gamma), dtype=torch.float32, device=logits.device)
+    rc = load_library().specdec_row_alpha(_ptr(logits), _ptr(q), dtype_code(logits),
+                                          _ptr(temperature), B, gamma, V, _ptr(workspace),
+                                          workspace.numel(), _ptr(out), _stream_ptr(stream))
+    _check(rc, "specdec_row_alpha")
     return out
 
 

@@ -6,6 +6,13 @@
 
 #include "common.cuh"
 
+namespace specdec {
+// row_extras.cu: sum_v min(p_i, q_i) of every drafted row
+cudaError_t launch_row_alpha(const void *logits, const void *q, int dtype, const RowPartial *part,
+                             const float *temperature, int B, int gamma, int V, int spr,
+                             float *alpha, cudaStream_t stream);
+}  // namespace specdec
+
 using namespace specdec;
 
 namespace {
@@ -343,6 +350,21 @@ int specdec_row_entropy(const void *workspace, size_t workspace_bytes, int dtype
                                         temperature, B, rows_per_request,
                                         stages_per_row(V, elem_bytes(dtype)), entropy,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+int specdec_row_alpha(const void *logits, const void *q, int dtype, const float *temperature,
+                      int B, int gamma, int V, const void *workspace, size_t workspace_bytes,
+                      float *alpha, void *stream) {
+  if (gamma < 1 || gamma > SPECDEC_MAX_GAMMA) return SPECDEC_ERR_INVALID_ARG;
+  int st = check_sizes(B, gamma + 1, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  if (B == 0) return SPECDEC_OK;
+  if (!logits || !q || !temperature || !alpha) return SPECDEC_ERR_INVALID_ARG;
+  st = check_workspace(workspace, workspace_bytes, B, gamma + 1, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  return cuda_status(launch_row_alpha(logits, q, dtype, reinterpret_cast<const RowPartial *>(workspace),
+                                      temperature, B, gamma, V, stages_per_row(V, elem_bytes(dtype)),
+                                      alpha, static_cast<cudaStream_t>(stream)));
 }
 
 int specdec_path_logprob(const void *logits, int dtype, const float *temperature,

@@ -154,3 +154,17 @@ def test_topk_argument_checks(lib):
     assert vt(N, N, BF16, N, N, N, 4, 8, 1000, 0, N, N, N, N, N, N, N, 0, N) == 1    # topk < 1
     assert vt(N, N, BF16, N, N, N, 4, 8, 1000, 1025, N, N, N, N, N, N, N, 0, N) == 2  # > max
     assert vt(N, N, BF16, N, N, N, 4, 8, 1000, 16, N, N, N, N, N, N, N, 0, N) == 1   # nulls
+
+
+def test_row_alpha_argument_checks(lib):
+    from speculative_decoding_verification_64_gb300.binding import BF16
+    N = None
+    d = ctypes.c_void_p(16)
+    ra = lib.specdec_row_alpha
+    assert ra(N, N, BF16, N, 0, 8, 1000, N, 0, N, N) == 0               # B = 0
+    assert ra(d, d, BF16, d, 2, 0, 1000, d, 1 << 30, d, N) == 1         # gamma 0
+    assert ra(d, d, BF16, d, 2, 33, 1000, d, 1 << 30, d, N) == 1        # gamma above the maximum
+    assert ra(d, N, BF16, d, 2, 8, 1000, d, 1 << 30, d, N) == 1         # no q
+    assert ra(d, d, BF16, d, 2, 8, 1000, d, 1 << 30, N, N) == 1         # no output
+    assert ra(d, d, BF16, d, 2, 8, 1000, d, 8, d, N) == 3               # workspace too small
+    assert ra(d, d, 7, d, 2, 8, 1000, d, 1 << 30, d, N) == 1            # dtype
