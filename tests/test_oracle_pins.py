@@ -919,3 +919,28 @@ def test_alpha_agrees_with_the_verify_diagnostics(oracle_lib):
     ok = np.isfinite(a)
     assert ok.any()
     assert np.allclose(a[ok], d[ok], rtol=0, atol=1e-12)
+
+
+def test_cascade_of_two_verify_levels_emits_the_target_law(oracle_lib):
+    """Multi-level speculation: level 1 verifies drafts from d against m, and
+    its emitted token, drafted from m, is verified against p; the cascade's
+    token follows p (Monte Carlo)."""
+    rng = np.random.default_rng(22)
+    V, n = 5, 200_000
+    d = rng.dirichlet(np.ones(V)).astype(np.float32)
+    lm = (rng.normal(size=V) * 1.3).astype(np.float32)
+    lp = (rng.normal(size=V) * 1.3).astype(np.float32)
+    m = special.softmax(lm.astype(np.float64))
+    p = special.softmax(lp.astype(np.float64))
+    dd = d.astype(np.float64)
+    T = np.ones(n, np.float32)
+    x = rng.choice(V, size=(n, 2), p=dd / dd.sum()).astype(np.int32)
+    o1 = oracle_lib.verify_linear(tile(np.stack([lm] * 3), n), tile(np.stack([d] * 2), n), "f32", x, T,
+                                  W.philox_uniforms(201, (n, 3)), diagnostics=False)
+    y0 = np.ascontiguousarray(o1["out_tokens"][:, :1])
+    o2 = oracle_lib.verify_linear(tile(np.stack([lp, lp]), n), tile(m.astype(np.float32)[None], n), "f32",
+                                  y0, T, W.philox_uniforms(202, (n, 2)), diagnostics=False)
+    for tok, law in ((y0[:, 0], m), (o2["out_tokens"][:, 0], p)):
+        freq = np.bincount(tok, minlength=V) / n
+        se = np.sqrt(law * (1 - law) / n)
+        assert (np.abs(freq - law) <= 5 * se + 1e-9).all()
