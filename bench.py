@@ -59,6 +59,9 @@ def parse_args(argv=None):
     ap.add_argument("--topk", type=int, default=0,
                     help="linear workloads: time specdec_verify_linear_topk (the top-k residual "
                          "approximation) with this many candidates instead of the exact step")
+    ap.add_argument("--alpha", action="store_true",
+                    help="linear workloads: also time specdec_row_alpha (the opt-in acceptance-rate "
+                         "pass) on the same inputs and report its bandwidth")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="skip timing the step replayed from CUDA graphs (reported beside the "
                          "eager value, never instead of it)")
@@ -414,6 +417,32 @@ def run_ours(args, dist):
                  "value": round(dist.sum(units, device) * K / (g_ms / 1e3), 1),
                  "unit": "positions/s", "graphs": n_graphs, "l2_warm": n_graphs < n_sets}
 
+    # ---- the opt-in acceptance-rate pass, timed on its own ----
+    alpha = None
+    if args.alpha and linear:
+        # the statistics in the workspace are those of set 0; alpha reads only M and S
+        # of each row from them, so the passes over the other sets move the same bytes
+        x0 = sets[0]
+        binding.verify_linear(*x0, out=out, workspace=ws, stream=stream)
+        for s_ in range(3):
+            x = sets[s_ % n_sets]
+            binding.row_alpha(x[0], x[1], x[3], ws, stream=stream)
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        n_a = max(1, min(K, 200))
+        a0.record(stream)
+        for s_ in range(n_a):
+            x = sets[s_ % n_sets]
+            binding.row_alpha(x[0], x[1], x[3], ws, stream=stream)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        a_us = a0.elapsed_time(a1) / n_a * 1e3
+        a_bytes = 2 * w.B * gamma * w.V * es
+        alpha = {"kernel": "row_alpha_kernel", "avg_launch_us": round(a_us, 2),
+                 "bytes_per_launch": int(a_bytes), "achieved_gbs": round(a_bytes / a_us / 1e3, 1),
+                 "peak_gbs": peak, "frac": round(a_bytes / a_us / 1e3 / peak, 4), "launches": n_a}
+
     # ---- e2e: pinned host buffers through the public verify call ----
     e2e = run_e2e(args, w, linear, device, stream, dist, units)
 
@@ -449,6 +478,7 @@ def run_ours(args, dist):
         "cpu_baseline": cpu,
         "gpu_launches": kernels * K,
         "graph": graph,
+        "alpha_pass": alpha,
         "clocks": clocks,
     }
     if dist.rank == 0:
