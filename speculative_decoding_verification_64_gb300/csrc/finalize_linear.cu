@@ -641,6 +641,47 @@ namespace topk {
 // rank; rows no rank serves (long runs of equal logits) take the full radix
 // select over the row, with the same per-warp segments so that the digit
 // counts give each warp its output offset.
+// One CTA of 512 threads per request (16 warps; at most 64 registers, so two
+// CTAs share an SM and a B=256 batch runs in one wave): the phases are
+// latency-bound, and more warps per request hide more of it.  These names
+// shadow the 256-thread ones of the other draw kernels.
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+
+// Block reductions of this kernel's 16 warps (two scratch buffers used in
+// turn, as for the other kernels).
+struct Red {
+  unsigned long long *buf;  // [2][kWarps]
+  int phase;
+  __device__ __forceinline__ unsigned long long *next() {
+    unsigned long long *r = buf + phase * kWarps;
+    phase ^= 1;
+    return r;
+  }
+};
+
+__device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long long v, Red &rr,
+                                                               unsigned long long &total) {
+  unsigned long long *red = rr.next();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const unsigned long long y = shfl_up_u64(inc, d);
+    if (lane >= d) inc += y;
+  }
+  if (lane == 31) red[warp] = inc;
+  __syncthreads();
+  unsigned long long pre = 0, tot = 0;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) {
+    if (i < warp) pre += red[i];
+    tot += red[i];
+  }
+  total = tot;
+  return pre + inc - v;
+}
+
 constexpr int kU = 8;                   // 16-byte vectors in flight per lane
 constexpr int kUF = 8;                  // the same in the one-pass filter and the bonus draw
 constexpr int kCap = 4096;              // elements the filter may keep
@@ -671,7 +712,7 @@ struct Smem {
   unsigned long long w[SPECDEC_MAX_TOPK];
   unsigned long long red[2 * kWarps];
 };
-static_assert(kThreads == 256, "one digit per thread in the selections");
+static_assert(kThreads >= 256, "one digit per thread in the selections");
 
 // Order-preserving unsigned key of a logit's bits (bf16: 16 bits; float32:
 // 32), -0 taking the key of +0 so that equal values have equal keys.
@@ -802,7 +843,7 @@ __device__ __forceinline__ void count_digit(unsigned *hist, bool match, uint32_t
 // holds digit 255 - t, so an exclusive scan in thread order sums the larger
 // digits.
 __device__ __forceinline__ void fix_digit(unsigned cnt, uint32_t prefix, int shift, Smem &sm, Red &rr) {
-  const int mine = 255 - (int)threadIdx.x;
+  const int mine = 255 - (int)threadIdx.x;  // negative past 255: count 0, never selected
   unsigned long long total;
   const unsigned long long larger = block_exscan_u64(cnt, rr, total);
   const unsigned long long nd = (unsigned long long)sm.need;
@@ -832,7 +873,7 @@ __device__ __forceinline__ uint32_t smem_select(const uint32_t *keys, int n, int
 #pragma unroll 1
   for (int shift = kBits - 8; shift >= 0; shift -= 8) {
     __syncthreads();
-    sm.h[tid] = 0u;
+    if (tid < 256) sm.h[tid] = 0u;
     __syncthreads();
     const uint32_t prefix = sm.prefix;
     const uint32_t hi_mask = (shift + 8 >= 32) ? 0u : (0xFFFFFFFFu << (shift + 8));
@@ -841,7 +882,7 @@ __device__ __forceinline__ uint32_t smem_select(const uint32_t *keys, int n, int
       count_digit(sm.h, key != 0u && (key & hi_mask) == (prefix & hi_mask), (key >> shift) & 0xFFu);
     }
     __syncthreads();
-    fix_digit(sm.h[255 - tid], prefix, shift, sm, rr);
+    fix_digit(tid < 256 ? sm.h[255 - tid] : 0u, prefix, shift, sm, rr);
   }
   need = sm.need;
   return sm.prefix;
@@ -1009,7 +1050,7 @@ __device__ __forceinline__ void radix_pass(const uint8_t *row, bool aligned, int
   __syncthreads();
   unsigned cnt = 0;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) cnt += sm.u.hist[w][255 - tid];
+  for (int w = 0; w < kWarps && tid < 256; ++w) cnt += sm.u.hist[w][255 - tid];
   fix_digit(cnt, prefix, shift, sm, rr);
   const int dgt = sm.dgt;
   unsigned a = 0;
@@ -1272,8 +1313,10 @@ __global__ void __launch_bounds__(kThreads, 2) topk_draw_kernel(const LinearFina
 cudaError_t launch_linear_topk(const LinearFinalizeParams &p, int topk, cudaStream_t stream) {
   if (p.B <= 0) return cudaSuccess;
   if (p.dtype == SPECDEC_F32)
-    return launch_pdl(topk::topk_draw_kernel<SPECDEC_F32>, dim3((unsigned)p.B), dim3(kThreads), 0, stream, p, topk);
-  return launch_pdl(topk::topk_draw_kernel<SPECDEC_BF16>, dim3((unsigned)p.B), dim3(kThreads), 0, stream, p, topk);
+    return launch_pdl(topk::topk_draw_kernel<SPECDEC_F32>, dim3((unsigned)p.B), dim3(topk::kThreads), 0,
+                      stream, p, topk);
+  return launch_pdl(topk::topk_draw_kernel<SPECDEC_BF16>, dim3((unsigned)p.B), dim3(topk::kThreads), 0,
+                    stream, p, topk);
 }
 
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream) {
