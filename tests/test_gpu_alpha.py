@@ -67,3 +67,13 @@ def test_alpha_special_rows(oracle_lib):
     want = oracle_lib.row_alpha(w.logits, w.q, w.dtype, w.temperature)
     check(got, want)
     assert np.isnan(got[1, 0]) and np.isnan(got[3]).all() and got[4, 1] == 0.0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V,gamma", [(1, 1), (2, 32), (7, 3), (4097, 32)])
+def test_alpha_vocabulary_and_gamma_edges(oracle_lib, dtype, V, gamma):
+    w = W.make_linear("normal2_tq08", B=5, gamma=gamma, V=V, dtype=dtype, seed=45 + V)
+    w.temperature[1] = 0.0                # one greedy request
+    got = gpu_alpha(w, verify=(V > 1))
+    want = oracle_lib.row_alpha(w.logits, w.q, w.dtype, w.temperature)
+    check(got, want)
