@@ -72,7 +72,9 @@ __device__ __forceinline__ unsigned long long block_exscan_u64(unsigned long lon
 }
 
 constexpr int kU = 8;                   // 16-byte vectors in flight per lane
-constexpr int kUF = 8;                  // the same in the one-pass filter and the bonus draw
+constexpr int kUF = 4;                  // the same in the one-pass filter (measured faster
+                                        // than 2 or 8 with 512 threads)
+constexpr int kUB = 8;                  // the same in the bonus draw
 constexpr int kCap = 4096;              // elements the filter may keep
 constexpr int kReg = kCap / kWarps;     // per warp
 constexpr int kSample = 4096;           // keys of the threshold sample (at most)
@@ -594,7 +596,7 @@ __device__ __forceinline__ uint4 pad_neg_inf(uint4 x, int nv) {
 }
 
 // Bonus draw, exact, from p over the whole final row: per-vector weight sums
-// (the vector-ordered CDF of the bulk draw), summed per round of kUF * 32
+// (the vector-ordered CDF of the bulk draw), summed per round of kUB * 32
 // vectors of each warp's segment; the round holding U * Z is then walked
 // again by its warp.
 constexpr int kMaxRounds = sizeof(((Smem *)nullptr)->u) / sizeof(unsigned long long) / kWarps;
@@ -611,19 +613,19 @@ __device__ __forceinline__ void bonus_draw(const LinearFinalizeParams &p, long l
   const int nvec = (V + kN - 1) / kN;
   const int segw = (((nvec + kWarps - 1) / kWarps) + 31) & ~31;
   const int s0 = min(nvec, warp * segw), s1 = min(nvec, s0 + segw);
-  const int nround = (s1 - s0 + kUF * 32 - 1) / (kUF * 32);
+  const int nround = (s1 - s0 + kUB * 32 - 1) / (kUB * 32);
   constexpr int kMaxSeg = (((SPECDEC_MAX_V / 4 + kWarps - 1) / kWarps) + 31) & ~31;
-  static_assert((kMaxSeg + kUF * 32 - 1) / (kUF * 32) <= kMaxRounds, "round sums fit in shared memory");
+  static_assert((kMaxSeg + kUB * 32 - 1) / (kUB * 32) <= kMaxRounds, "round sums fit in shared memory");
   unsigned long long *rs = reinterpret_cast<unsigned long long *>(&sm.u) + warp * kMaxRounds;
   const uint4 none = make_uint4(0u, 0u, 0u, 0u);
   unsigned long long wsum = 0;
   for (int r = 0; r < nround; ++r) {
-    const int base = s0 + r * kUF * 32;
-    uint4 x[kUF];
+    const int base = s0 + r * kUB * 32;
+    uint4 x[kUB];
     load_batch<DT>(x, row, aligned, base, s1, V, lane);
     unsigned long long acc = 0;
 #pragma unroll
-    for (int u = 0; u < kUF; ++u) {
+    for (int u = 0; u < kUB; ++u) {
       const int vi = base + u * 32 + lane;
       if (vi < s1)
         acc += to_fixed40(drawc::vec_sum<DT>(pad_neg_inf<DT>(x[u], vec_valid<DT>(vi, s1, V)), none, d, false));
@@ -646,11 +648,11 @@ __device__ __forceinline__ void bonus_draw(const LinearFinalizeParams &p, long l
   int r = 0;
   unsigned long long run = before;
   while (r < nround - 1 && run + rs[r] <= target) run += rs[r++];
-  const int base = s0 + r * kUF * 32;
-  uint4 x[kUF];
+  const int base = s0 + r * kUB * 32;
+  uint4 x[kUB];
   load_batch<DT>(x, row, aligned, base, s1, V, lane);
 #pragma unroll
-  for (int u = 0; u < kUF; ++u) {
+  for (int u = 0; u < kUB; ++u) {
     const int vi = base + u * 32 + lane;
     const uint4 xv = pad_neg_inf<DT>(x[u], vec_valid<DT>(vi, s1, V));
     const unsigned long long f = (vi < s1) ? to_fixed40(drawc::vec_sum<DT>(xv, none, d, false)) : 0ull;
