@@ -633,10 +633,25 @@ def cpu_baseline(w, linear, units, seconds):
     for _ in range(reps):
         _oracle_run(oracle, probe, linear)
     el = time.perf_counter() - t
+    cores = oracle.num_threads()
+    # the same code on one thread, on a shorter sample (about a fifth of the time)
+    oracle.set_threads(1)
+    one = w.subset(np.arange(1))
+    t = time.perf_counter()
+    _oracle_run(oracle, one, linear)
+    d1 = max(time.perf_counter() - t, 1e-6)
+    reps1 = max(1, int(seconds / 5 / d1))
+    t = time.perf_counter()
+    for _ in range(reps1):
+        _oracle_run(oracle, one, linear)
+    el1 = time.perf_counter() - t
+    oracle.set_threads(cores)
     return {"value": round(n_req * per_req / el, 1), "unit": "positions/s",
-            "cores": oracle.num_threads(), "kind": "oracle",
+            "cores": cores, "kind": "oracle",
             "sample": f"{n_req} requests ({reps} x the first {probe.B} of the workload), "
-                      f"{el:.1f} s, float64 C with OpenMP over requests"}
+                      f"{el:.1f} s, float64 C with OpenMP over requests",
+            "single_thread": {"value": round(reps1 * per_req / el1, 1), "unit": "positions/s",
+                              "sample": f"{reps1} x the first request, {el1:.1f} s"}}
 
 
 def run_reference(args, dist):

@@ -65,6 +65,8 @@ def _load():
         lib.specdec_oracle_verify_tree.restype = i
         lib.specdec_oracle_num_threads.argtypes = []
         lib.specdec_oracle_num_threads.restype = i
+        lib.specdec_oracle_set_threads.argtypes = [i]
+        lib.specdec_oracle_set_threads.restype = None
         lib.specdec_oracle_verify_linear_topk.argtypes = [p, p, i, p, p, p, i, i, i, i,
                                                           p, p, p, p, p, p, p, p, p]
         lib.specdec_oracle_verify_linear_topk.restype = i
@@ -159,6 +161,11 @@ def path_logprob(logits: np.ndarray, dtype: str, temperature: np.ndarray, out_to
 def num_threads() -> int:
     """OpenMP threads the oracle's parallel loops use."""
     return int(_load().specdec_oracle_num_threads())
+
+
+def set_threads(n: int) -> None:
+    """Use n OpenMP threads in the oracle's parallel loops from now on."""
+    _load().specdec_oracle_set_threads(int(n))
 
 
 def _dtype_code(dtype: str) -> int:

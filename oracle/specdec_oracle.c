@@ -515,6 +515,16 @@ int specdec_oracle_verify_tree(const void *logits, const void *q, int dtype,
 }
 
 /* Number of OpenMP threads a parallel region of this library uses. */
+/* Threads of the oracle's parallel loops from now on (n >= 1); no effect
+ * without OpenMP. */
+void specdec_oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 int specdec_oracle_num_threads(void) {
   int n = 1;
 #ifdef _OPENMP
