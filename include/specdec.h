@@ -128,6 +128,18 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * How many kernels specdec_verify_linear launches for these arguments: 1 when
+ * a small batch takes the one-launch path (rows 16-byte aligned, logits and q
+ * 16-byte aligned, B * 8 CTAs fitting the GPU at once, and the request's
+ * gamma + 1 target rows and gamma q rows fitting the shared memory of an
+ * 8-CTA cluster: each CTA holds 1/8 of every row), else 2 (the stats pass,
+ * then the draw).  Both paths give the same outputs and leave the same
+ * workspace.  0 for B = 0, -1 for invalid sizes.  Host only.
+ */
+int specdec_verify_linear_launches(int B, int gamma, int V, int dtype, const void *logits,
+                                   const void *q);
+
+/*
  * Phase 1 of either form, callable alone: per-row softmax statistics
  * (section 15.1.2 step 2) of B*rows_per_request rows of V logits, written
  * into the workspace as per-stage partials (max, base-2 exponential sum,

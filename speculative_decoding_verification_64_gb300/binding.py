@@ -40,6 +40,8 @@ _EXPORTS = {
     "specdec_row_entropy": ([ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                              ctypes.c_void_p], ctypes.c_int),
+    "specdec_verify_linear_launches": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "specdec_row_alpha": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                            ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
@@ -377,6 +379,14 @@ def row_entropy(logits: torch.Tensor, temperature: torch.Tensor, workspace: torc
                                             _stream_ptr(stream))
     _check(rc, "specdec_row_entropy")
     return out
+
+
+def verify_linear_launches(logits: torch.Tensor, q: torch.Tensor) -> int:
+    """Kernels ``verify_linear`` launches for these inputs: 1 (a small batch, one
+    launch) or 2 (the stats pass, then the draw)."""
+    B, R, V = logits.shape
+    return int(load_library().specdec_verify_linear_launches(B, R - 1, V, dtype_code(logits),
+                                                             _ptr(logits), _ptr(q)))
 
 
 def row_alpha(logits: torch.Tensor, q: torch.Tensor, temperature: torch.Tensor,

@@ -11,6 +11,9 @@ namespace specdec {
 cudaError_t launch_row_alpha(const void *logits, const void *q, int dtype, const RowPartial *part,
                              const float *temperature, int B, int gamma, int V, int spr,
                              float *alpha, cudaStream_t stream);
+// small_verify.cu: the linear step of a small batch in one launch
+bool small_verify_applies(int B, int gamma, int V, int dtype, const void *logits, const void *q);
+cudaError_t launch_small_verify(const LinearFinalizeParams &p, cudaStream_t stream);
 }  // namespace specdec
 
 using namespace specdec;
@@ -227,11 +230,26 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
                          workspace_bytes);
   if (st != SPECDEC_OK || B == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (small_verify_applies(B, gamma, V, dtype, logits, q)) {
+    // a small batch: both phases in one launch, leaving the same workspace
+    const LinearFinalizeParams p =
+        linear_params(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
+                      n_accepted, out_tokens, final_token, is_bonus, row_status, p_draft, workspace);
+    return cuda_status(launch_small_verify(p, s));
+  }
   st = launch_stats(logits, q, dtype, draft_tokens, temperature, B, gamma + 1, V, workspace, s);
   if (st != SPECDEC_OK) return st;
   return linear_finalize_launch(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma,
                                 V, n_accepted, out_tokens, final_token, is_bonus, row_status,
                                 p_draft, workspace, s);
+}
+
+int specdec_verify_linear_launches(int B, int gamma, int V, int dtype, const void *logits,
+                                   const void *q) {
+  if (B <= 0) return 0;
+  if (check_sizes(B, gamma + 1, V, dtype) != SPECDEC_OK || gamma < 1 || gamma > SPECDEC_MAX_GAMMA)
+    return -1;
+  return small_verify_applies(B, gamma, V, dtype, logits, q) ? 1 : 2;
 }
 
 static int tree_checks(const void *logits, const void *q, int dtype, const int32_t *tokens,

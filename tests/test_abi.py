@@ -168,3 +168,16 @@ def test_row_alpha_argument_checks(lib):
     assert ra(d, d, BF16, d, 2, 8, 1000, d, 1 << 30, N, N) == 1         # no output
     assert ra(d, d, BF16, d, 2, 8, 1000, d, 8, d, N) == 3               # workspace too small
     assert ra(d, d, 7, d, 2, 8, 1000, d, 1 << 30, d, N) == 1            # dtype
+
+
+def test_verify_linear_launches_query(lib):
+    from speculative_decoding_verification_64_gb300.binding import BF16, F32
+    N = None
+    vl = lib.specdec_verify_linear_launches
+    assert vl(0, 4, 1000, BF16, N, N) == 0                     # B = 0
+    assert vl(1, 0, 1000, BF16, N, N) == -1                    # gamma 0
+    assert vl(1, 4, 1000, 7, N, N) == -1                       # dtype
+    # unaligned rows (7 bf16 elements = 14 bytes) take the two kernels
+    assert vl(1, 4, 7, BF16, ctypes.c_void_p(256), ctypes.c_void_p(512)) == 2
+    # a large batch takes the two kernels
+    assert vl(4096, 8, 128256, BF16, ctypes.c_void_p(256), ctypes.c_void_p(512)) == 2
