@@ -24,7 +24,8 @@
 //
 // Every CTA of a cluster runs the same sequence of cluster barriers (the
 // branches between them depend only on the decision, which all CTAs compute
-// alike); the one wait on memory (the bulk copies) is bounded.
+// alike); the one wait on memory (the bulk copies) is bounded.  Remote shared
+// memory is read only between two cluster barriers.
 #include <cfloat>
 
 #include <cooperative_groups.h>
@@ -39,7 +40,7 @@ namespace cg = cooperative_groups;
 using namespace drawc;
 
 constexpr int kC = 8;                      // CTAs per request: one portable cluster
-constexpr int kT = 256;                    // threads per CTA
+constexpr int kT = 512;                    // threads per CTA (a warp per stage at B = 1)
 constexpr int kW = kT / 32;
 constexpr int kVecPerStage = kStageBytes / 16;
 constexpr int kMaxDynSmem = 200 * 1024;    // row slices plus the header
@@ -222,9 +223,9 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1)
       }
     }
   }
-  // no CTA leaves while another may still read its shared memory; copies of a
-  // CTA whose wait gave up are waited for (bounded) before it exits
-  cluster.sync();
+  // No CTA reads another's shared memory after the draw's last cluster barrier
+  // (and none at all on the other paths), so a CTA may leave now.  Copies of a
+  // CTA whose wait gave up are waited for (bounded) before it exits.
   if (h.abort_flag && tid == 0) mbar_wait_bounded(&h.full, 0);
 }
 

@@ -46,6 +46,20 @@ def test_linear_calls_repeat_exactly():
     check_same([snapshot(o) for o in outs])
 
 
+def test_one_launch_calls_repeat_exactly():
+    import torch
+    from speculative_decoding_verification_64_gb300 import binding
+    w = W.make_workload("linear_b1_g4_v32000_f32", B=8)
+    x = binding.linear_inputs_to_device(w)
+    assert binding.verify_linear_launches(x[0], x[1]) == 1
+    ws = binding.alloc_workspace(w.B, w.gamma + 1, w.V, binding.dtype_code(x[0]))
+    outs = [binding.LinearOut.empty(w.B, w.gamma, "cuda") for _ in range(N_CALLS)]
+    for o in outs:
+        binding.verify_linear(*x, out=o, workspace=ws)
+    torch.cuda.synchronize()
+    check_same([snapshot(o) for o in outs])
+
+
 def test_topk_calls_repeat_exactly():
     import torch
     from speculative_decoding_verification_64_gb300 import binding
