@@ -9,9 +9,9 @@ gamma=8 drafts, V=128256, bf16 logits, Zipf-shaped logits at T=0.7).
 Prints ONE JSON line (rank 0):
   value      verified draft positions / s over all ranks (B * gamma per step),
              inputs resident in HBM, CUDA events on the launching stream;
-  e2e        the same metric through the public call with pinned HOST
-             buffers: host->device copy of the step's inputs, the verify call
-             and device->host copy of its outputs inside the timed region;
+  e2e        the same metric through the C-ABI host-buffer call with pinned
+             HOST buffers: host->device copy of the step's inputs, the verify
+             and the device->host copy of its outputs inside the timed region;
   roofline   the row-statistics kernel: algorithmic bytes per launch / its
              CUDA-event time against the measured HBM copy peak;
   cpu_baseline  the float64 oracle on the host cores, on a bounded sample.
@@ -52,7 +52,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps of the end-to-end timing (default: enough for ~4 GB of "
+                         "host-to-device copies, 20 to 2000 steps)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -496,9 +498,6 @@ def run_ours(args, dist):
 
 L2_BYTES = 129_000_000  # GB300 L2
 PHASE_EVERY = 32        # timed steps per step issued as two phases with events
-E2E_COPY_STREAMS = 4    # streams the e2e host-to-device copies are split over
-
-
 def input_rotation(set_bytes: int):
     """How many resident copies of a step's inputs to use in turn so that a
     step's inputs were last touched at least 3 x L2 bytes of other inputs ago."""
@@ -536,84 +535,86 @@ def _config(w, name, linear, l2_note, topk=0):
 
 
 def run_e2e(args, w, linear, device, stream, dist, units):
+    """The C-ABI host-buffer call (specdec_verify_linear_host / _tree_host):
+    every step copies its inputs from page-locked host memory, verifies and
+    copies its outputs back.  Two staging buffers on two streams, used in turn,
+    so that step i+1's copies may overlap step i's kernels; the arguments are
+    marshalled once, outside the timed region."""
+    import ctypes
     import torch
     from speculative_decoding_verification_64_gb300 import binding
 
-    def pinned(a, bf16=False):
-        a = np.ascontiguousarray(a)
-        t = torch.from_numpy(a.view(np.int16) if bf16 else a)
-        t = t.view(torch.bfloat16) if bf16 else t
-        return t.pin_memory()
-
-    bf = w.dtype == "bf16"
-    if linear:
-        host_in = [pinned(w.logits, bf), pinned(w.q, bf), pinned(w.draft_tokens),
-                   pinned(w.temperature), pinned(w.uniforms)]
-    else:
-        host_in = [pinned(w.logits, bf), pinned(w.q, bf), pinned(w.node_tokens),
-                   pinned(w.parent), pinned(w.temperature), pinned(w.uniforms)]
-    # two device copies of the inputs: step i+1's copies run while step i
-    # verifies; each copy is split over E2E_COPY_STREAMS streams (several copy
-    # engines), and a set is overwritten only after the verify that read it
-    dev_sets = [[torch.empty_like(t, device=device) for t in host_in] for _ in range(2)]
-    out = (binding.LinearOut.empty(w.B, w.gamma, device) if linear
-           else binding.TreeOut.empty(w.B, w.N, w.max_depth, device))
-    ws = binding.alloc_workspace(w.B, w.rows, w.V, binding.dtype_code(dev_sets[0][0]), device)
-    out_fields = [f for f in vars(out) if getattr(out, f) is not None]
-    host_out = {f: torch.empty_like(getattr(out, f), device="cpu").pin_memory() for f in out_fields}
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-    copy_streams = [torch.cuda.Stream(device) for _ in range(E2E_COPY_STREAMS)]
-    read_done = [None, None]  # event: the last verify that read set j has run
-
-    def one(i, start=None):
-        j = i % 2
-        dev_in = dev_sets[j]
-        ready = []
-        for c, cs in enumerate(copy_streams):
-            if start is not None:
-                cs.wait_event(start)
-            if read_done[j] is not None:
-                cs.wait_event(read_done[j])
-            with torch.cuda.stream(cs):
-                for d, h in zip(dev_in, host_in):
-                    n = d.numel()
-                    lo, hi = n * c // len(copy_streams), n * (c + 1) // len(copy_streams)
-                    if hi > lo:
-                        d.view(-1)[lo:hi].copy_(h.view(-1)[lo:hi], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(cs)
-            ready.append(ev)
-        for ev in ready:
-            stream.wait_event(ev)
+    lib = binding.load_library()
+    host_in = (binding.linear_inputs_to_host(w) if linear else binding.tree_inputs_to_host(w))
+    dt = binding.dtype_code(host_in[0])
+    P = binding._ptr
+    streams = [torch.cuda.Stream(device) for _ in range(2)]
+    calls = []
+    for j in range(2):
         if linear:
-            binding.verify_linear(*dev_in, out=out, workspace=ws, stream=stream)
+            out = binding._host_out(None, lambda: binding.LinearOut.empty(w.B, w.gamma, "cpu"))
+            nbytes = binding.linear_staging_size(w.B, w.gamma, w.V, dt)
         else:
-            binding.verify_tree(*dev_in, w.max_depth, out=out, workspace=ws, stream=stream)
-        read_done[j] = torch.cuda.Event()
-        read_done[j].record(stream)
-        for f in out_fields:
-            host_out[f].copy_(getattr(out, f), non_blocking=True)
+            out = binding._host_out(None, lambda: binding.TreeOut.empty(w.B, w.N, w.max_depth,
+                                                                        "cpu"))
+            nbytes = binding.tree_staging_size(w.B, w.N, w.V, w.max_depth, dt)
+        st = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        sp = ctypes.c_void_p(streams[j].cuda_stream)
+        if linear:
+            a = (P(host_in[0]), P(host_in[1]), dt, P(host_in[2]), P(host_in[3]), P(host_in[4]),
+                 w.B, w.gamma, w.V, P(out.n_accepted), P(out.out_tokens), P(out.final_token),
+                 P(out.is_bonus), P(out.row_status), P(out.p_draft), P(st), nbytes, sp)
+            fn = lib.specdec_verify_linear_host
+        else:
+            a = (P(host_in[0]), P(host_in[1]), dt, P(host_in[2]), P(host_in[3]), P(host_in[4]),
+                 P(host_in[5]), w.B, w.N, w.V, w.max_depth, P(out.n_accepted),
+                 P(out.path_nodes), P(out.out_tokens), P(out.final_token), P(out.is_bonus),
+                 P(out.row_status), P(out.p_node), P(st), nbytes, sp)
+            fn = lib.specdec_verify_tree_host
+        calls.append((fn, a, st, out))
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(v.numel() * v.element_size() for v in vars(calls[0][3]).values() if v is not None)
 
-    for i in range(2):
+    def one(i):
+        fn, a = calls[i % 2][:2]
+        rc = fn(*a)
+        if rc != 0:
+            raise RuntimeError(f"{fn.__name__}: {binding.status_string(rc)}")
+
+    for i in range(4):
         one(i)
     torch.cuda.synchronize()
-    n = max(1, min(args.e2e_steps, args.steps))
+    n = args.e2e_steps
+    if n is None:  # about 4 GB of host-to-device copies
+        n = min(2000, max(20, -(-4_000_000_000 // h2d)))
+    n = max(1, min(n, args.steps))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize()
     e0.record(stream)
+    for s in streams:
+        s.wait_event(e0)
     for i in range(n):
-        one(i, start=e0 if i < 2 else None)
+        one(i)
+    for s in streams:
+        ev = torch.cuda.Event()
+        ev.record(s)
+        stream.wait_event(ev)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = dist.max(e0.elapsed_time(e1), device)
     val = dist.sum(units, device) * n / (ms / 1e3)
     return {"value": round(val, 1), "unit": "positions/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": round(ms / n, 4),
-            "h2d_gbs": round(h2d * n / (ms / 1e3) / 1e9, 1), "copy_streams": E2E_COPY_STREAMS,
-            "pipelined": "step i+1's copies overlap step i's verify (two device input sets)"}
+            "h2d_gbs": round(h2d * n / (ms / 1e3) / 1e9, 1),
+            "call": fn_name(linear),
+            "pipelined": "two staging buffers on two streams in turn: step i+1's copies may "
+                         "overlap step i's kernels"}
+
+
+def fn_name(linear):
+    return "specdec_verify_linear_host" if linear else "specdec_verify_tree_host"
 
 
 # ----------------------------------------------------------------------------

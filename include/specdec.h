@@ -24,7 +24,8 @@
  *   whose children are all rejected draws from the renormalised residual.
  *
  * Conventions (all functions):
- *   - every array pointer is a DEVICE pointer owned by the caller; row-major;
+ *   - every array pointer is a DEVICE pointer owned by the caller (the
+ *     *_host calls take host arrays and a device staging buffer); row-major;
  *   - logits and q hold float32 (SPECDEC_F32) or bfloat16 bits (SPECDEC_BF16),
  *     both in the same dtype;
  *   - uniforms are float32 values in (0, 1) that the caller draws (e.g. from a
@@ -231,6 +232,49 @@ int specdec_verify_linear_static(const void *logits, const void *q, int dtype,
                                  int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
                                  uint8_t *is_bonus, int32_t *row_status, float *p_draft,
                                  void *stream);
+
+/*
+ * Host-buffer forms of the two verify calls.
+ *
+ * No counterpart in the method description: an addition of this library for
+ * callers whose inputs and results live in host memory (one request at a
+ * time, the latency case).  Here every array argument is a HOST pointer;
+ * only `staging` is device memory.  One call enqueues on `stream`:
+ *   1. one host-to-device copy per input array into `staging`;
+ *   2. the device call (specdec_verify_linear / specdec_verify_tree) on those
+ *      copies, with its workspace inside `staging`;
+ *   3. one device-to-host copy per output array (p_draft / p_node skipped
+ *      when NULL).
+ * It returns once they are enqueued: synchronise `stream` (or an event
+ * recorded after the call) before reading the outputs or reusing the input
+ * buffers.  Page-locked host memory (cudaHostAlloc, cudaHostRegister) keeps
+ * the copies asynchronous; pageable memory works, but the runtime then copies
+ * synchronously with respect to the host, and cannot be captured into a CUDA
+ * graph.  Arguments, layouts, outputs and return codes as in the device
+ * calls, with the staging buffer in place of the workspace:
+ *   staging   device memory, 16-byte aligned, at least
+ *             specdec_linear_staging_size(B, gamma, V, dtype) /
+ *             specdec_tree_staging_size(B, N, V, max_depth, dtype) bytes;
+ *             SPECDEC_ERR_WORKSPACE if smaller, unaligned or NULL.  Calls that
+ *             share a staging buffer must not overlap on the GPU.
+ * The size functions return 0 for invalid sizes and for B = 0.  A CUDA error
+ * while enqueuing (SPECDEC_ERR_CUDA) may leave earlier copies enqueued.
+ */
+size_t specdec_linear_staging_size(int B, int gamma, int V, int dtype);
+size_t specdec_tree_staging_size(int B, int N, int V, int max_depth, int dtype);
+int specdec_verify_linear_host(const void *logits, const void *q, int dtype,
+                               const int32_t *draft_tokens, const float *temperature,
+                               const float *uniforms, int B, int gamma, int V,
+                               int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
+                               uint8_t *is_bonus, int32_t *row_status, float *p_draft,
+                               void *staging, size_t staging_bytes, void *stream);
+int specdec_verify_tree_host(const void *logits, const void *q, int dtype,
+                             const int32_t *node_tokens, const int32_t *parent,
+                             const float *temperature, const float *uniforms, int B, int N,
+                             int V, int max_depth, int32_t *n_accepted, int32_t *path_nodes,
+                             int32_t *out_tokens, int32_t *final_token, uint8_t *is_bonus,
+                             int32_t *row_status, float *p_node, void *staging,
+                             size_t staging_bytes, void *stream);
 
 /* Phase 2 of the tree form (phase 1 is specdec_row_stats with rows_per_request = N). */
 int specdec_tree_finalize(const void *logits, const void *q, int dtype,

@@ -74,6 +74,16 @@ _EXPORTS = {
     "specdec_verify_linear_static": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
                                      [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 +
                                      [ctypes.c_void_p] * 7, ctypes.c_int),
+    "specdec_linear_staging_size": ([ctypes.c_int] * 4, ctypes.c_size_t),
+    "specdec_tree_staging_size": ([ctypes.c_int] * 5, ctypes.c_size_t),
+    "specdec_verify_linear_host": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
+                                   [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 +
+                                   [ctypes.c_void_p] * 7 + [ctypes.c_size_t, ctypes.c_void_p],
+                                   ctypes.c_int),
+    "specdec_verify_tree_host": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
+                                 [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 +
+                                 [ctypes.c_void_p] * 8 + [ctypes.c_size_t, ctypes.c_void_p],
+                                 ctypes.c_int),
     "specdec_tree_finalize": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] +
                               [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 +
                               [ctypes.c_void_p] * 8 + [ctypes.c_size_t, ctypes.c_void_p],
@@ -317,6 +327,119 @@ def tree_finalize(logits, q, node_tokens, parent, temperature, uniforms, max_dep
         _ptr(out.p_node), _ptr(ws), ws.numel(), _stream_ptr(stream))
     _check(rc, "specdec_tree_finalize")
     return out
+
+
+# ---------------------------------------------------------------------------
+# host-buffer calls: inputs and outputs in host memory, a device staging buffer
+# ---------------------------------------------------------------------------
+
+def linear_staging_size(B: int, gamma: int, V: int, dtype: int) -> int:
+    return int(load_library().specdec_linear_staging_size(B, gamma, V, dtype))
+
+
+def tree_staging_size(B: int, N: int, V: int, max_depth: int, dtype: int) -> int:
+    return int(load_library().specdec_tree_staging_size(B, N, V, max_depth, dtype))
+
+
+def _staging(nbytes: int, staging, device) -> torch.Tensor:
+    if staging is None:
+        return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+    if staging.device.type != "cuda" or staging.dtype != torch.uint8:
+        raise ValueError("staging must be a uint8 CUDA tensor")
+    return staging
+
+
+def _host_out(out, make):
+    """A result container in page-locked host memory (made when None)."""
+    if out is None:
+        out = make()
+        for k, v in vars(out).items():
+            if v is not None:
+                setattr(out, k, v.pin_memory())
+    return out
+
+
+def verify_linear_host(logits: torch.Tensor, q: torch.Tensor, draft_tokens: torch.Tensor,
+                       temperature: torch.Tensor, uniforms: torch.Tensor,
+                       out: Optional[LinearOut] = None, staging: Optional[torch.Tensor] = None,
+                       stream=None, sync: bool = True, device="cuda") -> LinearOut:
+    """Linear verify of host tensors (``specdec_verify_linear_host``): inputs and the
+    returned outputs live in host memory (page-locked keeps the copies
+    asynchronous); ``staging`` is device memory of ``linear_staging_size`` bytes.
+    With ``sync=False`` the outputs are valid only after ``stream`` has reached
+    the call."""
+    cpu = torch.device("cpu")
+    B, R, V = logits.shape
+    gamma = R - 1
+    dt = dtype_code(logits)
+    _req(logits, "logits", logits.dtype, (B, R, V), cpu)
+    _req(q, "q", logits.dtype, (B, gamma, V), cpu)
+    _req(draft_tokens, "draft_tokens", torch.int32, (B, gamma), cpu)
+    _req(temperature, "temperature", torch.float32, (B,), cpu)
+    _req(uniforms, "uniforms", torch.float32, (B, R), cpu)
+    out = _host_out(out, lambda: LinearOut.empty(B, gamma, cpu))
+    st = _staging(linear_staging_size(B, gamma, V, dt), staging, device)
+    s = stream if stream is not None else torch.cuda.current_stream(st.device)
+    rc = load_library().specdec_verify_linear_host(
+        _ptr(logits), _ptr(q), dt, _ptr(draft_tokens), _ptr(temperature), _ptr(uniforms),
+        B, gamma, V, _ptr(out.n_accepted), _ptr(out.out_tokens), _ptr(out.final_token),
+        _ptr(out.is_bonus), _ptr(out.row_status), _ptr(out.p_draft), _ptr(st), st.numel(),
+        ctypes.c_void_p(s.cuda_stream))
+    _check(rc, "specdec_verify_linear_host")
+    if sync:
+        s.synchronize()
+    return out
+
+
+def verify_tree_host(logits, q, node_tokens, parent, temperature, uniforms, max_depth: int,
+                     out: Optional[TreeOut] = None, staging: Optional[torch.Tensor] = None,
+                     stream=None, sync: bool = True, device="cuda") -> TreeOut:
+    """Token-tree verify of host tensors (``specdec_verify_tree_host``); as
+    ``verify_linear_host``, with ``tree_staging_size`` bytes of staging."""
+    cpu = torch.device("cpu")
+    B, N, V = logits.shape
+    dt = dtype_code(logits)
+    _req(logits, "logits", logits.dtype, (B, N, V), cpu)
+    _req(q, "q", logits.dtype, (B, N, V), cpu)
+    _req(node_tokens, "node_tokens", torch.int32, (B, N), cpu)
+    _req(parent, "parent", torch.int32, (B, N), cpu)
+    _req(temperature, "temperature", torch.float32, (B,), cpu)
+    _req(uniforms, "uniforms", torch.float32, (B, N), cpu)
+    out = _host_out(out, lambda: TreeOut.empty(B, N, max_depth, cpu))
+    st = _staging(tree_staging_size(B, N, V, max_depth, dt), staging, device)
+    s = stream if stream is not None else torch.cuda.current_stream(st.device)
+    rc = load_library().specdec_verify_tree_host(
+        _ptr(logits), _ptr(q), dt, _ptr(node_tokens), _ptr(parent), _ptr(temperature),
+        _ptr(uniforms), B, N, V, max_depth, _ptr(out.n_accepted), _ptr(out.path_nodes),
+        _ptr(out.out_tokens), _ptr(out.final_token), _ptr(out.is_bonus), _ptr(out.row_status),
+        _ptr(out.p_node), _ptr(st), st.numel(), ctypes.c_void_p(s.cuda_stream))
+    _check(rc, "specdec_verify_tree_host")
+    if sync:
+        s.synchronize()
+    return out
+
+
+def to_host(a, bf16: bool = False, pin: bool = True) -> torch.Tensor:
+    """numpy array -> CPU tensor (page-locked by default); uint16 arrays with
+    ``bf16`` are bfloat16 bits."""
+    import numpy as np
+    a = np.ascontiguousarray(a)
+    t = torch.from_numpy(a.view(np.int16) if bf16 else a)
+    t = t.view(torch.bfloat16) if bf16 else t
+    return t.pin_memory() if pin else t.clone()
+
+
+def linear_inputs_to_host(w, pin: bool = True):
+    bf = w.dtype == "bf16"
+    return (to_host(w.logits, bf, pin), to_host(w.q, bf, pin), to_host(w.draft_tokens, pin=pin),
+            to_host(w.temperature, pin=pin), to_host(w.uniforms, pin=pin))
+
+
+def tree_inputs_to_host(w, pin: bool = True):
+    bf = w.dtype == "bf16"
+    return (to_host(w.logits, bf, pin), to_host(w.q, bf, pin), to_host(w.node_tokens, pin=pin),
+            to_host(w.parent, pin=pin), to_host(w.temperature, pin=pin),
+            to_host(w.uniforms, pin=pin))
 
 
 # ---------------------------------------------------------------------------

@@ -181,3 +181,52 @@ def test_verify_linear_launches_query(lib):
     assert vl(1, 4, 7, BF16, ctypes.c_void_p(256), ctypes.c_void_p(512)) == 2
     # a large batch takes the two kernels
     assert vl(4096, 8, 128256, BF16, ctypes.c_void_p(256), ctypes.c_void_p(512)) == 2
+
+
+def test_staging_sizes(lib):
+    from speculative_decoding_verification_64_gb300.binding import BF16, F32
+    ls, ts, ws = lib.specdec_linear_staging_size, lib.specdec_tree_staging_size, \
+        lib.specdec_workspace_size
+    B, g, V = 1, 4, 32000
+    # the inputs, the outputs (each region 256-byte aligned) and the workspace
+    inputs = B * (g + 1) * V * 4 + B * g * V * 4
+    assert ls(B, g, V, F32) >= inputs + ws(B, g + 1, V, F32)
+    assert ls(B, g, V, F32) <= inputs + ws(B, g + 1, V, F32) + 11 * 256 + 4096
+    assert ls(B, g, V, F32) % 256 == 0
+    assert ls(256, 8, 128256, BF16) > ls(128, 8, 128256, BF16) > 0
+    for bad in ((0, 4, 1000, BF16), (-1, 4, 1000, BF16), (2, 0, 1000, BF16), (2, 33, 1000, BF16),
+                (2, 4, 0, BF16), (2, 4, 1000, 7), (2, 4, (1 << 21) + 1, F32)):
+        assert ls(*bad) == 0, bad
+    n = 64
+    assert ts(32, n, 128256, 8, BF16) >= 2 * 32 * n * 128256 * 2 + ws(32, n, 128256, BF16)
+    for bad in ((0, n, 1000, 8, BF16), (2, 0, 1000, 8, BF16), (2, 2000, 1000, 8, BF16),
+                (2, n, 1000, -1, BF16), (2, n, 1000, 65, BF16), (2, n, 1000, 8, 7)):
+        assert ts(*bad) == 0, bad
+
+
+def test_host_call_argument_checks(lib):
+    from speculative_decoding_verification_64_gb300.binding import BF16
+    N = None
+    d = ctypes.c_void_p(16)
+    vl = lib.specdec_verify_linear_host
+    assert vl(N, N, BF16, N, N, N, 0, 8, 1000, N, N, N, N, N, N, N, 0, N) == 0     # B = 0
+    assert vl(N, N, BF16, N, N, N, 0, 8, (1 << 21) + 1, N, N, N, N, N, N, N, 0, N) == 2
+    assert vl(N, N, BF16, N, N, N, 4, 8, 1000, N, N, N, N, N, N, N, 0, N) == 1     # nulls
+    assert vl(d, d, BF16, d, d, d, 4, 0, 1000, d, d, d, d, d, N, d, 1 << 30, N) == 1
+    assert vl(d, d, BF16, d, d, d, 4, 33, 1000, d, d, d, d, d, N, d, 1 << 30, N) == 2
+    assert vl(d, d, 5, d, d, d, 4, 4, 1000, d, d, d, d, d, N, d, 1 << 30, N) == 1
+    # staging missing, too small or unaligned: nothing is copied
+    need = lib.specdec_linear_staging_size(4, 4, 1000, BF16)
+    assert vl(d, d, BF16, d, d, d, 4, 4, 1000, d, d, d, d, d, N, N, need, N) == 3
+    assert vl(d, d, BF16, d, d, d, 4, 4, 1000, d, d, d, d, d, N, d, need - 1, N) == 3
+    assert vl(d, d, BF16, d, d, d, 4, 4, 1000, d, d, d, d, d, N, ctypes.c_void_p(24), need,
+              N) == 3
+    vt = lib.specdec_verify_tree_host
+    assert vt(N, N, BF16, N, N, N, N, 0, 64, 1000, 5, N, N, N, N, N, N, N, N, 0, N) == 0
+    assert vt(N, N, BF16, N, N, N, N, 2, 64, 1000, 5, N, N, N, N, N, N, N, N, 0, N) == 1
+    assert vt(N, N, BF16, N, N, N, N, 2, 0, 1000, 5, N, N, N, N, N, N, N, N, 0, N) == 1
+    assert vt(N, N, BF16, N, N, N, N, 2, 2000, 1000, 5, N, N, N, N, N, N, N, N, 0, N) == 2
+    assert vt(N, N, BF16, N, N, N, N, 2, 64, 1000, 65, N, N, N, N, N, N, N, N, 0, N) == 2
+    need = lib.specdec_tree_staging_size(2, 64, 1000, 5, BF16)
+    assert vt(d, d, BF16, d, d, d, d, 2, 64, 1000, 5, d, d, d, d, d, d, N, d, need - 1,
+              N) == 3
