@@ -143,7 +143,7 @@ struct DrawSmem {
   unsigned long long warp_tile[kMaxTilesPerCta][kWarps];
   unsigned long long tile_tot[kMaxTilesPerCta];
   unsigned long long cta_total;        // this pass's CTA total
-  unsigned long long shared_total[2];  // read by the other CTAs; double-buffered by pass
+  unsigned long long totals[2][kG];    // every CTA's total, written by that CTA; by pass parity
   unsigned long long prefix, Z, base;
   float Zf;  // Z as a float, in units of the row maximum
   unsigned long long scan_warp[kWarps];
@@ -187,22 +187,31 @@ __device__ __forceinline__ void draw_sums(DrawSmem &ds, const DrawRow &r, int pa
     unsigned long long s = 0;
     for (int i = 0; i < nt; ++i) s += ds.tile_tot[i];
     ds.cta_total = s;
-    ds.shared_total[pass & 1] = s;
   }
 }
 
-// Cluster-wide exclusive prefix of the CTA totals (all CTAs call it).  A
-// slot is rewritten two passes later, after every CTA has passed the cluster
-// barrier of the pass in between, so no reader can see a later value.
+// Cluster-wide exclusive prefix of the CTA totals (all CTAs call it).  Each
+// CTA stores its total into slot [pass & 1][rank] of every CTA's shared memory
+// (remote stores, made visible by the cluster barrier), then reads its own
+// copy: no remote load on the path.  A slot is rewritten two passes later,
+// after every CTA has passed the cluster barrier of the pass in between, i.e.
+// after every reader of the old value has read it.
 __device__ __forceinline__ void draw_exchange(DrawSmem &ds, cg::cluster_group &cluster,
                                               int pass) {
+  if (threadIdx.x == 0) {
+    const unsigned rank = cluster.block_rank();
+    const unsigned long long s = ds.cta_total;
+#pragma unroll
+    for (unsigned r = 0; r < (unsigned)kG; ++r)
+      cluster.map_shared_rank(&ds, r)->totals[pass & 1][rank] = s;
+  }
   cluster.sync();
   if (threadIdx.x == 0) {
     const unsigned rank = cluster.block_rank();
     unsigned long long pre = 0, tot = 0;
+#pragma unroll
     for (unsigned r = 0; r < (unsigned)kG; ++r) {
-      const DrawSmem *other = cluster.map_shared_rank(&ds, r);
-      const unsigned long long x = other->shared_total[pass & 1];
+      const unsigned long long x = ds.totals[pass & 1][r];
       if (r < rank) pre += x;
       tot += x;
     }

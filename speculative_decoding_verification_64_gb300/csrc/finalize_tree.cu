@@ -19,11 +19,12 @@
 // rows (L2-resident after the first), and the next sibling's test needs only
 // its gathered logit and q value.
 //
-// One 8-CTA cluster per request.  Every CTA validates the tree, merges the
-// row statistics and gathers l_parent(t_n), q_parent(t_n) for all nodes; the
-// walk is replicated in every CTA (the decisions depend only on those values
-// and on exact fixed-point cluster sums, so all CTAs agree); reductions over
-// the vocabulary are split across the cluster.
+// One 8-CTA cluster per request.  Every CTA validates the tree and gathers
+// l_parent(t_n), q_parent(t_n) for all nodes; the row statistics are merged
+// one eighth per CTA and copied between the CTAs through distributed shared
+// memory; the walk is replicated in every CTA (the decisions depend only on
+// those values and on exact fixed-point cluster sums, so all CTAs agree);
+// reductions over the vocabulary are split across the cluster.
 #include "finalize_common.cuh"
 
 namespace specdec {
@@ -45,6 +46,8 @@ struct TreeSmem {
   float rowM[kMaxN];
   float rowS[kMaxN];
   int rowA[kMaxN];    // first arg-max (greedy requests)
+  int rowF[kMaxN];    // status bits of the row (partial flags, unusable statistics)
+  int tok[kMaxN];     // t_n
   int path[SPECDEC_MAX_TREE_DEPTH + 1];
   int status, nkids;
 };
@@ -73,7 +76,7 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
   if (tid == 0) sm.status = temperature_valid(T) ? 0 : SPECDEC_ROW_BAD_TEMP;
   __syncthreads();
 
-  // ---- structure, row statistics ---------------------------------------------
+  // ---- structure, the drafted tokens' logits and q values ---------------------
   int st = 0;
   for (int n = tid; n < N; n += kThreads) {
     const int a = __ldg(p.parent + nodebase + n);
@@ -81,17 +84,48 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
     if (n == 0 ? (a != -1) : (a < 0 || a >= n)) st |= SPECDEC_ROW_BAD_TREE;
     sm.anc[n] = (n == 0) ? -1 : a;
     sm.dep[n] = (n == 0) ? 0 : 1;
+    sm.lg[n] = 0.0f;
+    sm.qg[n] = 1.0f;
+    if (n == 0) continue;
+    const int t = __ldg(p.tokens + nodebase + n);
+    sm.tok[n] = t;
+    if (t < 0 || t >= V) {
+      st |= SPECDEC_ROW_BAD_TOKEN;
+      continue;
+    }
+    if (a < 0 || a >= n) continue;
+    const long long prow = nodebase + a;
+    const float qt = load_elem(p.q, DT, prow * V + t);
+    const float lt = load_elem(p.logits, DT, prow * V + t);
+    if (!(qt > 0.0f) || qt == INFINITY) st |= SPECDEC_ROW_BAD_Q;
+    sm.qg[n] = qt;
+    sm.lg[n] = lt;
   }
-  for (int n = warp; n < N; n += kWarps) {
+  // ---- row statistics: row n merged by warp (n / kG) % kWarps of CTA n % kG,
+  // then every CTA copies the other CTAs' rows (one remote round trip instead
+  // of a warp merging N / kWarps rows one after another)
+  for (int n = rank + kG * warp; n < N; n += kG * kWarps) {
     const RowStat r = warp_merge_row(p.part, nodebase + n, p.spr, c, lane);
     if (lane == 0) {
       sm.rowM[n] = r.M;
       sm.rowS[n] = r.S;
       sm.rowA[n] = r.arg;
-      if (r.flags) st |= r.flags;
-      if (!row_usable(r)) st |= SPECDEC_ROW_NONFINITE;
+      sm.rowF[n] = r.flags | (row_usable(r) ? 0 : SPECDEC_ROW_NONFINITE);
     }
   }
+  cluster.sync();  // every owner's rows written
+  for (int n = tid; n < N; n += kThreads) {
+    const int owner = n % kG;
+    if (owner != rank) {
+      const TreeSmem *o = cluster.map_shared_rank(&sm, owner);
+      sm.rowM[n] = o->rowM[n];
+      sm.rowS[n] = o->rowS[n];
+      sm.rowA[n] = o->rowA[n];
+      sm.rowF[n] = o->rowF[n];
+    }
+  }
+  cluster.sync();  // every copy done before any CTA goes on (or exits)
+  for (int n = tid; n < N; n += kThreads) st |= sm.rowF[n];
   if (st) atomicOr(&sm.status, st);
   __syncthreads();
   const bool tree_ok = !(sm.status & SPECDEC_ROW_BAD_TREE);
@@ -121,34 +155,22 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
     }
   }
 
-  // ---- tokens and gathers ----------------------------------------------------
+  // ---- depths and p_parent of every drafted token ----------------------------
   st = 0;
   for (int n = tid; n < N; n += kThreads) {
     if (tree_ok && sm.dep[n] > p.max_depth) st |= SPECDEC_ROW_BAD_TREE;
-    sm.lg[n] = 0.0f;
     sm.pg[n] = 0.0f;
-    sm.qg[n] = 1.0f;
     if (n == 0) continue;
-    const int t = __ldg(p.tokens + nodebase + n);
+    const int t = sm.tok[n];
     const int a = sm.par[n];
-    if (t < 0 || t >= V) {
-      st |= SPECDEC_ROW_BAD_TOKEN;
-      continue;
-    }
-    if (a < 0 || a >= n) continue;
-    const long long prow = nodebase + a;
-    const float qt = load_elem(p.q, DT, prow * V + t);
-    const float lt = load_elem(p.logits, DT, prow * V + t);
-    if (!(qt > 0.0f) || qt == INFINITY) st |= SPECDEC_ROW_BAD_Q;
-    sm.qg[n] = qt;
-    sm.lg[n] = lt;
+    if (t < 0 || t >= V || a < 0 || a >= n) continue;
     if (greedy) {
       sm.pg[n] = (t == sm.rowA[a]) ? 1.0f : 0.0f;
     } else {
       RowStat r;
       r.M = sm.rowM[a];
       r.S = sm.rowS[a];
-      sm.pg[n] = target_prob(lt, r, c);
+      sm.pg[n] = target_prob(sm.lg[n], r, c);
     }
   }
   if (st) atomicOr(&sm.status, st);
@@ -284,7 +306,7 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
   if (rank == 0) {
     for (int j = tid; j < D1; j += kThreads) {
       p.path_nodes[b * D1 + j] = (j <= nacc) ? sm.path[j] : -1;
-      if (j < nacc) p.out_tokens[b * D1 + j] = __ldg(p.tokens + nodebase + sm.path[j + 1]);
+      if (j < nacc) p.out_tokens[b * D1 + j] = sm.tok[sm.path[j + 1]];
       else if (j > nacc) p.out_tokens[b * D1 + j] = -1;
     }
     if (tid == 0) {
@@ -297,7 +319,8 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
       }
     }
   }
-  if (!greedy) cluster.sync();  // the other CTAs may still read this CTA's smem
+  // No shared memory of another CTA is touched after the last cluster barrier
+  // (the walk's exchanges store before their barrier), so CTAs leave freely.
 }
 
 }  // namespace
