@@ -25,7 +25,8 @@
 // Every CTA of a cluster runs the same sequence of cluster barriers (the
 // branches between them depend only on the decision, which all CTAs compute
 // alike); the one wait on memory (the bulk copies) is bounded.  Remote shared
-// memory is read only between two cluster barriers.
+// memory is only written (each slot once per launch) before a cluster barrier,
+// never read.
 #include <cfloat>
 
 #include <cooperative_groups.h>
@@ -49,8 +50,7 @@ struct Head {
   alignas(8) uint64_t full;                // completes when this CTA's slices have landed
   lindec::DecisionSmem dec;
   unsigned long long red[kW];
-  unsigned long long total;                // this CTA's draw weight (read by the others)
-  unsigned long long pre, Z;
+  unsigned long long tot[2][kC];           // every CTA's draw weight, stored by that CTA; by attempt
   int abort_flag;
 };
 constexpr int kHeadBytes = (int)((sizeof(Head) + 127) / 128 * 128);
@@ -166,8 +166,11 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1)
     // the workspace's partials (read-only for the draw kernels, written here)
     if (lane == 0) const_cast<RowPartial *>(p.part)[(b * R + r) * (long long)spr + j] = part;
   }
-  __threadfence();  // the partials and gathers, for the other CTAs of the cluster
-  cluster.sync();
+  // A cluster barrier with release (arrive) and acquire (wait) semantics at
+  // cluster scope orders global memory as well: the partials and gathers
+  // written above are visible to every CTA of the cluster after it, with no
+  // GPU-scope fence.
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
   // ---- the accept test: every CTA alike, rank 0 writes the outputs ----------
   const LinearDecision d = lindec::request_decision<DT, kT>(p, b, rank == 0, h.dec);
   if (!(d.status || d.greedy)) {
@@ -186,22 +189,19 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1)
       for (int v = v0; v < v1; ++v) mine += to_fixed40(vec_sum<DT>(lk[v], use_q ? qk[v] : none, d, use_q));
       unsigned long long tot;
       pre = cta_exscan_u64(mine, h.red, tot);
-      if (tid == 0) h.total = tot;
+      // this CTA's total into slot [attempt][rank] of every CTA (remote stores,
+      // visible after the barrier; a slot is written once per launch)
+      if (tid == 0)
+        for (int r = 0; r < kC; ++r) cluster.map_shared_rank(&h, r)->tot[attempt][rank] = tot;
       cluster.sync();
-      if (tid == 0) {
-        unsigned long long before = 0, all = 0;
-        for (int r = 0; r < kC; ++r) {
-          const Head *other = cluster.map_shared_rank(&h, r);
-          const unsigned long long x = other->total;
-          if (r < rank) before += x;
-          all += x;
-        }
-        h.pre = before;
-        h.Z = all;
+      cta_pre = 0;
+      Z = 0;
+#pragma unroll
+      for (int r = 0; r < kC; ++r) {
+        const unsigned long long x = h.tot[attempt][r];
+        if (r < rank) cta_pre += x;
+        Z += x;
       }
-      cluster.sync();  // every CTA has read the totals before any rewrites them
-      cta_pre = h.pre;
-      Z = h.Z;
       if (!(Z == 0 && use_q)) break;
       use_q = false;   // residual mass 0 (only by rounding): draw from p, as the other draws do
     }
@@ -223,8 +223,9 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1)
       }
     }
   }
-  // No CTA reads another's shared memory after the draw's last cluster barrier
-  // (and none at all on the other paths), so a CTA may leave now.  Copies of a
+  // No CTA touches another's shared memory after the draw's last cluster
+  // barrier (the totals are stored before it; none at all on the other
+  // paths), so a CTA may leave now.  Copies of a
   // CTA whose wait gave up are waited for (bounded) before it exits.
   if (h.abort_flag && tid == 0) mbar_wait_bounded(&h.full, 0);
 }
