@@ -48,6 +48,7 @@ struct TreeSmem {
   int rowA[kMaxN];    // first arg-max (greedy requests)
   int rowF[kMaxN];    // status bits of the row (partial flags, unusable statistics)
   int tok[kMaxN];     // t_n
+  float uu[kMaxN];    // the request's uniforms (slot 0: final draw; slot n: test of node n)
   int path[SPECDEC_MAX_TREE_DEPTH + 1];
   int status, nkids;
 };
@@ -86,6 +87,7 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
     sm.dep[n] = (n == 0) ? 0 : 1;
     sm.lg[n] = 0.0f;
     sm.qg[n] = 1.0f;
+    sm.uu[n] = __ldg(p.uniforms + nodebase + n);  // the walk then needs no global load per test
     if (n == 0) continue;
     const int t = __ldg(p.tokens + nodebase + n);
     sm.tok[n] = t;
@@ -130,19 +132,23 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
   __syncthreads();
   const bool tree_ok = !(sm.status & SPECDEC_ROW_BAD_TREE);
   if (tree_ok) {
-    // depths by pointer jumping (parent[n] < n, so every chain ends at the root)
+    // depths by pointer jumping (parent[n] < n, so every chain ends at the
+    // root); a tree of depth d is done after ceil(log2 d) + 1 rounds, and the
+    // rounds stop as soon as no node has an ancestor left to jump over
     for (int it = 0; it < 11; ++it) {
       int na[kMaxN / kThreads], nd[kMaxN / kThreads];
+      bool more = false;
 #pragma unroll
       for (int k = 0; k < kMaxN / kThreads; ++k) {
         const int n = tid + k * kThreads;
         if (n < N) {
           const int a = sm.anc[n];
+          more |= (a > 0);
           na[k] = (a > 0) ? sm.anc[a] : a;
           nd[k] = (a > 0) ? sm.dep[n] + sm.dep[a] : sm.dep[n];
         }
       }
-      __syncthreads();
+      if (!__syncthreads_or(more)) break;  // uniform: nothing would change
 #pragma unroll
       for (int k = 0; k < kMaxN / kThreads; ++k) {
         const int n = tid + k * kThreads;
@@ -243,7 +249,7 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
     for (int i = 0; i < nk; ++i) {
       const int child = sm.kids[i];
       const float qt = sm.qg[child];
-      const float u = __ldg(p.uniforms + nodebase + child);
+      const float u = sm.uu[child];
       bool acc;
       if (greedy) {
         acc = (sm.pg[child] == 1.0f);
@@ -294,7 +300,7 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
       draw_exchange(sm.ds, cluster, pass);
       ++pass;
     }
-    const float U = __ldg(p.uniforms + nodebase);
+    const float U = sm.uu[0];
     const unsigned long long target = uniform_target(U, sm.ds.Z);
     const int v = draw_search<DT>(sm.ds, r, target);
     if (tid == 0 && v >= 0) {
