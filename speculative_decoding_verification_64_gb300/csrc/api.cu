@@ -11,6 +11,8 @@ namespace specdec {
 cudaError_t launch_row_alpha(const void *logits, const void *q, int dtype, const RowPartial *part,
                              const float *temperature, int B, int gamma, int V, int spr,
                              float *alpha, cudaStream_t stream);
+// finalize_linear.cu: the draw launched right after this call's stats pass
+cudaError_t launch_linear_finalize_after_stats(const LinearFinalizeParams &p, cudaStream_t stream);
 // small_verify.cu: the linear step of a small batch in one launch
 bool small_verify_applies(int B, int gamma, int V, int dtype, const void *logits, const void *q);
 cudaError_t launch_small_verify(const LinearFinalizeParams &p, cudaStream_t stream);
@@ -197,11 +199,13 @@ static int linear_finalize_launch(const void *logits, const void *q, int dtype,
                                   const float *uniforms, int B, int gamma, int V,
                                   int32_t *n_accepted, int32_t *out_tokens,
                                   int32_t *final_token, uint8_t *is_bonus, int32_t *row_status,
-                                  float *p_draft, void *workspace, cudaStream_t stream) {
+                                  float *p_draft, void *workspace, cudaStream_t stream,
+                                  bool after_stats = false) {
   const LinearFinalizeParams p =
       linear_params(logits, q, dtype, tokens, temperature, uniforms, B, gamma, V, n_accepted,
                     out_tokens, final_token, is_bonus, row_status, p_draft, workspace);
-  return cuda_status(launch_linear_finalize(p, stream));
+  return cuda_status(after_stats ? launch_linear_finalize_after_stats(p, stream)
+                                 : launch_linear_finalize(p, stream));
 }
 
 int specdec_linear_finalize(const void *logits, const void *q, int dtype,
@@ -241,7 +245,7 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
   if (st != SPECDEC_OK) return st;
   return linear_finalize_launch(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma,
                                 V, n_accepted, out_tokens, final_token, is_bonus, row_status,
-                                p_draft, workspace, s);
+                                p_draft, workspace, s, /*after_stats=*/true);
 }
 
 int specdec_verify_linear_launches(int B, int gamma, int V, int dtype, const void *logits,

@@ -74,7 +74,10 @@ struct DraftIn {
   float2 g;
 };
 
-__device__ __forceinline__ DraftIn load_draft(const LinearFinalizeParams &p, long long b, int lane) {
+// The call's own inputs (draft token, uniform): a kernel launched dependent on
+// the stats pass may read them before waiting for it.
+__device__ __forceinline__ DraftIn load_draft_inputs(const LinearFinalizeParams &p, long long b,
+                                                     int lane) {
   DraftIn in;
   in.x = -1;
   in.u = 0.0f;
@@ -82,8 +85,19 @@ __device__ __forceinline__ DraftIn load_draft(const LinearFinalizeParams &p, lon
   if (lane < p.gamma) {
     in.x = __ldg(p.tokens + b * p.gamma + lane);
     in.u = __ldg(p.uniforms + b * (p.gamma + 1) + lane);
-    in.g = __ldcg(p.ws.gather + b * (p.gamma + 1) + lane);  // meaningful for a valid x only
   }
+  return in;
+}
+
+// The (logit, q) pair the stats pass gathered: only after waiting for it.
+__device__ __forceinline__ void load_draft_gather(const LinearFinalizeParams &p, long long b,
+                                                  int lane, DraftIn &in) {
+  if (lane < p.gamma) in.g = __ldcg(p.ws.gather + b * (p.gamma + 1) + lane);  // valid x only
+}
+
+__device__ __forceinline__ DraftIn load_draft(const LinearFinalizeParams &p, long long b, int lane) {
+  DraftIn in = load_draft_inputs(p, b, lane);
+  load_draft_gather(p, b, lane, in);
   return in;
 }
 

@@ -370,9 +370,13 @@ struct Smem {
   volatile int abort_flag;
 };
 
-template <int DT>
+// kEarly: launched right after the stats pass of the same call (a plain
+// launch, so everything before it is complete and visible), the call's own
+// inputs may be read before waiting for the stats pass, which does not write
+// them.  Launched after an arbitrary kernel, everything waits.
+template <int DT, bool kEarly>
 __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFinalizeParams p) {
-  pdl_wait();
+  if (!kEarly) pdl_wait();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
   constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
@@ -398,14 +402,17 @@ __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFina
 
   // ---- head: row merges (16-lane segments over (request, row) pairs) ------
   // warp j, which runs request j's accept test, loads its inputs first so that
-  // their round trip overlaps the merges
+  // their round trip overlaps the merges (the call's own inputs before the
+  // wait for the stats pass when kEarly; its gathered values after)
   DraftIn din;
   float Tj = 0.0f;
   if (warp < nreq) {
     const long long b = (long long)p.B - 1 - (rb0 + warp);
     Tj = __ldg(p.temperature + b);
-    din = load_draft(p, b, lane);
+    din = load_draft_inputs(p, b, lane);
   }
+  if (kEarly) pdl_wait();
+  if (warp < nreq) load_draft_gather(p, (long long)p.B - 1 - (rb0 + warp), lane, din);
   const int pairs = nreq * R;
   for (int base = 0; base < pairs; base += kThreads / kSeg) {
     if (base + warp * (32 / kSeg) >= pairs) continue;  // both segments of this warp idle
@@ -548,7 +555,7 @@ bool bulk_draw_applies(const LinearFinalizeParams &p, int grid) {
   return (per_cta + upr - 1) / upr + 1 <= bulk::kMaxReq;
 }
 
-template <int DT>
+template <int DT, bool kEarly>
 cudaError_t launch_bulk(const LinearFinalizeParams &p, unsigned grid, cudaStream_t stream) {
   static bool attr_set[64] = {};
   int dev = 0;
@@ -556,35 +563,21 @@ cudaError_t launch_bulk(const LinearFinalizeParams &p, unsigned grid, cudaStream
   if (err != cudaSuccess) return err;
   const int smem = (int)sizeof(bulk::Smem);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    err = cudaFuncSetAttribute(bulk::draw_bulk_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               smem);
+    err = cudaFuncSetAttribute(bulk::draw_bulk_kernel<DT, kEarly>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
-  return launch_pdl(bulk::draw_bulk_kernel<DT>, dim3(grid), dim3(bulk::kThreads), (size_t)smem, stream, p);
+  return launch_pdl(bulk::draw_bulk_kernel<DT, kEarly>, dim3(grid), dim3(bulk::kThreads),
+                    (size_t)smem, stream, p);
 }
-
-
-// ---------------------------------------------------------------------------
-// The linear draw with the top-k residual: an approximation of step 4 after
-// the chapter's implementation note (precompute the residual probabilities of
-// the top-k candidates instead of the whole vocabulary).  At a rejection the
-// residual max(0, p - q) is restricted to the k tokens of largest p (ties to
-// the lower index) and renormalised; with no mass there, p restricted to the
-// candidates.  The bonus draw is exact.  One CTA per request:
-//   * the accept test as in the chunked draw;
-//   * candidates: radix select of the k-th largest logit key (8 bits a pass:
-//     two passes for bf16, four for float32), then a collection pass in index
-//     order (block scans of the per-thread counts, ties at the threshold to
-//     the lower index);
-//   * weights of the candidates only (q is gathered at k tokens, never read
-//     as a row), each as 40-bit fixed point; inverse CDF in index order.
-// ---------------------------------------------------------------------------
 
 
 }  // namespace
 
-cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream) {
+namespace {
+
+cudaError_t launch_finalize(const LinearFinalizeParams &p, cudaStream_t stream, bool after_stats) {
   if (p.B <= 0) return cudaSuccess;
   {
     const int es = (p.dtype == SPECDEC_F32) ? 4 : 2;
@@ -592,9 +585,14 @@ cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t s
     const long long units = (long long)p.B * ((nst + bulk::kUnitStages - 1) / bulk::kUnitStages);
     const long long sms = device_sm_count();
     const int grid = (int)(units < sms ? units : sms);
-    if (bulk_draw_applies(p, grid))
-      return (p.dtype == SPECDEC_F32) ? launch_bulk<SPECDEC_F32>(p, (unsigned)grid, stream)
-                                      : launch_bulk<SPECDEC_BF16>(p, (unsigned)grid, stream);
+    if (bulk_draw_applies(p, grid)) {
+      const unsigned g = (unsigned)grid;
+      if (after_stats)
+        return (p.dtype == SPECDEC_F32) ? launch_bulk<SPECDEC_F32, true>(p, g, stream)
+                                        : launch_bulk<SPECDEC_BF16, true>(p, g, stream);
+      return (p.dtype == SPECDEC_F32) ? launch_bulk<SPECDEC_F32, false>(p, g, stream)
+                                      : launch_bulk<SPECDEC_BF16, false>(p, g, stream);
+    }
   }
   const long long items = (long long)p.B * p.nchunk;
   const long long slots = (long long)device_sm_count() * kMinBlocks;
@@ -602,6 +600,19 @@ cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t s
   if (p.dtype == SPECDEC_F32)
     return launch_pdl(linear_draw_kernel<SPECDEC_F32>, dim3(grid), dim3(kThreads), 0, stream, p);
   return launch_pdl(linear_draw_kernel<SPECDEC_BF16>, dim3(grid), dim3(kThreads), 0, stream, p);
+}
+
+}  // namespace
+
+cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream) {
+  return launch_finalize(p, stream, false);
+}
+
+// Right after the stats pass of the same call (launched by this library as a
+// plain launch): the draw may read the call's inputs before its dependency wait.
+cudaError_t launch_linear_finalize_after_stats(const LinearFinalizeParams &p,
+                                               cudaStream_t stream) {
+  return launch_finalize(p, stream, true);
 }
 
 }  // namespace specdec
