@@ -1,14 +1,15 @@
 // Linear verify of a small batch in one launch ("Chapter 15: Decoding
-// acceleration", section 15.1.2 steps 2-4): the B = 1 latency case.
+// acceleration", section 15.1.2 steps 2-4): the B = 1 latency case and
+// batches up to a few dozen requests.
 //
 // The two-kernel step (stats pass, then the draw) pays two launches and
-// several dependent memory round trips in each; with a handful of requests
-// the data is small enough to stay on chip instead.  One 8-CTA cluster per
-// request:
+// several dependent memory round trips in each; with few requests the data is
+// small enough to stay on chip instead.  One cluster of C CTAs per request
+// (C = 8, 4 or 2: the largest with B * C CTAs on the GPU at once):
 //
-// * CTA r bulk-copies its share of every row of the request -- stages r*n ..
-//   r*n + n - 1 (8 KB each) of the gamma+1 target rows and of the gamma q
-//   rows -- into shared memory, once;
+// * CTA r bulk-copies its share of every target row of the request -- stages
+//   r*n .. r*n + n - 1 (8 KB each) of the gamma+1 rows -- into shared memory,
+//   once, and the same share of the gamma q rows when they fit as well;
 // * each warp reduces whole stages exactly as the stats pass does (the same
 //   stage routines on the same 8 KB stages), so the partials it writes to the
 //   workspace are the stats pass's, bit for bit; rank 0 also writes the
@@ -16,6 +17,9 @@
 //   so the workspace ends as the two-kernel step leaves it;
 // * after a cluster barrier every CTA merges the partials and runs the accept
 //   test with the draw kernels' own routine (same merge order, same decision);
+// * when the q rows are not resident and draft k was rejected, each CTA copies
+//   its share of q row k into the slot of the bonus row, which is no longer
+//   needed (k < gamma);
 // * the draw reads row k's slices from shared memory: per-vector weights in
 //   40-bit fixed point summed per thread, a scan over the CTA and one over the
 //   cluster (distributed shared memory), then the thread whose range holds
@@ -24,7 +28,7 @@
 //
 // Every CTA of a cluster runs the same sequence of cluster barriers (the
 // branches between them depend only on the decision, which all CTAs compute
-// alike); the one wait on memory (the bulk copies) is bounded.  Remote shared
+// alike); the waits on memory (the bulk copies) are bounded.  Remote shared
 // memory is only written (each slot once per launch) before a cluster barrier,
 // never read.
 #include <cfloat>
@@ -40,7 +44,7 @@ namespace {
 namespace cg = cooperative_groups;
 using namespace drawc;
 
-constexpr int kC = 8;                      // CTAs per request: one portable cluster
+constexpr int kMaxC = 8;                   // CTAs per request at most: a portable cluster
 constexpr int kT = 512;                    // threads per CTA (a warp per stage at B = 1)
 constexpr int kW = kT / 32;
 constexpr int kVecPerStage = kStageBytes / 16;
@@ -50,8 +54,9 @@ struct Head {
   alignas(8) uint64_t full;                // completes when this CTA's slices have landed
   lindec::DecisionSmem dec;
   unsigned long long red[kW];
-  unsigned long long tot[2][kC];           // every CTA's draw weight, stored by that CTA; by attempt
-  int abort_flag;
+  unsigned long long tot[2][kMaxC];        // every CTA's draw weight, stored by that CTA; by attempt
+  int abort_flag;                          // 1 + the parity of the copy wait that gave up, or 0
+  int abort_any;                           // set in every CTA by a CTA whose q-row wait gave up
 };
 constexpr int kHeadBytes = (int)((sizeof(Head) + 127) / 128 * 128);
 
@@ -78,9 +83,11 @@ __device__ __forceinline__ unsigned long long cta_exscan_u64(unsigned long long 
   return pre + inc - v;
 }
 
+// kC: CTAs per request (the launch's cluster size); qres: the q rows are
+// resident too, else q row k is copied in after the decision.
 template <int DT>
-__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1)
-    small_verify_kernel(const LinearFinalizeParams p) {
+__global__ void __launch_bounds__(kT, 1)
+    small_verify_kernel(const LinearFinalizeParams p, const int kC, const bool qres) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Head &h = *reinterpret_cast<Head *>(smem_raw);
   uint8_t *slices = smem_raw + kHeadBytes;
@@ -96,28 +103,30 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1)
   const int j0 = rank * nst;                    // this CTA's first stage
   const int nj = max(0, min(spr - j0, nst));    // stages it holds
   uint8_t *lsl = slices;                        // [R][nst][kStageBytes]
-  uint8_t *qsl = slices + (size_t)R * nst * kStageBytes;  // [gamma][nst][kStageBytes]
+  uint8_t *qsl = slices + (size_t)R * nst * kStageBytes;  // [gamma][nst][kStageBytes] if qres
+  const uint8_t *qg = reinterpret_cast<const uint8_t *>(p.q) + (size_t)b * gamma * rowbytes;
   auto stage_bytes = [&](int j) { return min(kStageBytes, rowbytes - j * kStageBytes); };
 
   if (tid == 0) {
     mbar_init(&h.full, 1);
     h.abort_flag = 0;
+    h.abort_any = 0;  // before the first cluster barrier, so before any remote store
     fence_mbar_init();
   }
   __syncthreads();
   // ---- this CTA's slices of the request's rows, one bulk copy per stage ----
   if (tid == 0) {
+    const int qrows = qres ? gamma : 0;
     uint32_t total = 0;
-    for (int t = 0; t < nj; ++t) total += (uint32_t)stage_bytes(j0 + t) * (uint32_t)(R + gamma);
+    for (int t = 0; t < nj; ++t) total += (uint32_t)stage_bytes(j0 + t) * (uint32_t)(R + qrows);
     mbar_arrive_expect_tx(&h.full, total);
     const uint8_t *lg = reinterpret_cast<const uint8_t *>(p.logits) + (size_t)b * R * rowbytes;
-    const uint8_t *qg = reinterpret_cast<const uint8_t *>(p.q) + (size_t)b * gamma * rowbytes;
     for (int r = 0; r < R; ++r)
       for (int t = 0; t < nj; ++t)
         bulk_copy_g2s(lsl + ((size_t)r * nst + t) * kStageBytes,
                       lg + (size_t)r * rowbytes + (size_t)(j0 + t) * kStageBytes,
                       (uint32_t)stage_bytes(j0 + t), &h.full);
-    for (int r = 0; r < gamma; ++r)
+    for (int r = 0; r < qrows; ++r)
       for (int t = 0; t < nj; ++t)
         bulk_copy_g2s(qsl + ((size_t)r * nst + t) * kStageBytes,
                       qg + (size_t)r * rowbytes + (size_t)(j0 + t) * kStageBytes,
@@ -135,7 +144,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1)
   if (rank == 0 && tid == 0) p.ws.draw_cnt[b] = 0u;
   // ---- stage statistics, as the stats pass computes them --------------------
   const bool ok = mbar_wait_bounded(&h.full, 0);
-  if (!ok) h.abort_flag = 1;
+  if (!ok) h.abort_flag = 1;  // the partials carry SPECDEC_ROW_INTERNAL: no draw follows
   const float T = __ldg(p.temperature + b);
   const float c = temperature_scale(T);
   for (int item = warp; item < R * nj; item += kW) {
@@ -180,6 +189,30 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1)
     const int nvec = (nj > 0) ? (nj - 1) * kVecPerStage + stage_bytes(j0 + nj - 1) / 16 : 0;
     const uint4 *lk = reinterpret_cast<const uint4 *>(lsl + (size_t)k * nst * kStageBytes);
     const uint4 *qk = reinterpret_cast<const uint4 *>(qsl + (size_t)(use_q ? k : 0) * nst * kStageBytes);
+    if (!qres && use_q) {
+      // q row k into the bonus row's slot (k < gamma; every read of that slot
+      // was before the cluster barrier above), second phase of the barrier
+      uint8_t *slot = lsl + (size_t)gamma * nst * kStageBytes;
+      if (tid == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        uint32_t total = 0;
+        for (int t = 0; t < nj; ++t) total += (uint32_t)stage_bytes(j0 + t);
+        mbar_arrive_expect_tx(&h.full, total);
+        for (int t = 0; t < nj; ++t)
+          bulk_copy_g2s(slot + (size_t)t * kStageBytes,
+                        qg + (size_t)k * rowbytes + (size_t)(j0 + t) * kStageBytes,
+                        (uint32_t)stage_bytes(j0 + t), &h.full);
+      }
+      qk = reinterpret_cast<const uint4 *>(slot);
+      if (!mbar_wait_bounded(&h.full, 1)) {
+        // this CTA's share never landed: the request gets SPECDEC_ROW_INTERNAL
+        // (told to every CTA with the first draw barrier); its sums are junk
+        if (tid == 0) {
+          h.abort_flag = 2;
+          for (int r = 0; r < kC; ++r) *cluster.map_shared_rank(&h.abort_any, r) = 1;
+        }
+      }
+    }
     const int per = (nvec + kT - 1) / kT;
     const int v0 = min(nvec, tid * per), v1 = min(nvec, v0 + per);
     const uint4 none = make_uint4(0u, 0u, 0u, 0u);
@@ -194,9 +227,9 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1)
       if (tid == 0)
         for (int r = 0; r < kC; ++r) cluster.map_shared_rank(&h, r)->tot[attempt][rank] = tot;
       cluster.sync();
+      if (h.abort_any) break;  // uniform: every CTA was told before the barrier
       cta_pre = 0;
       Z = 0;
-#pragma unroll
       for (int r = 0; r < kC; ++r) {
         const unsigned long long x = h.tot[attempt][r];
         if (r < rank) cta_pre += x;
@@ -207,7 +240,18 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1)
     }
     const unsigned long long target = uniform_target(__ldg(p.uniforms + b * R + gamma), Z);
     const unsigned long long lo = cta_pre + pre;
-    if (lo <= target && target - lo < mine) {
+    if (h.abort_any) {
+      // the malformed-request outputs, over what the decision wrote (same threads)
+      if (rank == 0) {
+        if (tid < R) p.out_tokens[b * R + tid] = -1;
+        if (tid == 0) {
+          p.n_accepted[b] = 0;
+          p.is_bonus[b] = 0;
+          p.row_status[b] = SPECDEC_ROW_INTERNAL;
+          p.final_token[b] = -1;
+        }
+      }
+    } else if (lo <= target && target - lo < mine) {
       unsigned long long run = lo;
       for (int v = v0; v < v1; ++v) {
         const uint4 lv = lk[v], qv = use_q ? qk[v] : none;
@@ -227,11 +271,37 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1)
   // barrier (the totals are stored before it; none at all on the other
   // paths), so a CTA may leave now.  Copies of a
   // CTA whose wait gave up are waited for (bounded) before it exits.
-  if (h.abort_flag && tid == 0) mbar_wait_bounded(&h.full, 0);
+  if (h.abort_flag && tid == 0) mbar_wait_bounded(&h.full, (uint32_t)(h.abort_flag - 1));
+}
+
+// The cluster size and residency a call takes, or false for the two kernels.
+struct Plan {
+  int C;
+  bool qres;
+};
+
+bool plan_for(int B, int gamma, int V, int dtype, const void *logits, const void *q, Plan &pl) {
+  const int es = (dtype == SPECDEC_F32) ? 4 : 2;
+  const long long rowbytes = (long long)V * es;
+  if (B < 1 || rowbytes % 16 != 0) return false;
+  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(q)) & 15) return false;
+  const long long sms = device_sm_count();
+  int C = kMaxC;  // the largest cluster with every CTA on the GPU at once (one CTA per SM)
+  while (C >= 2 && (long long)B * C > sms) C /= 2;
+  if (C < 2) return false;
+  const int spr = stages_per_row(V, es);
+  const long long slot = (long long)((spr + C - 1) / C) * kStageBytes;  // one row's share
+  pl.C = C;
+  if ((long long)(2 * gamma + 1) * slot <= kMaxDynSmem) {
+    pl.qres = true;
+    return true;
+  }
+  pl.qres = false;
+  return (long long)(gamma + 1) * slot <= kMaxDynSmem;
 }
 
 template <int DT>
-cudaError_t launch_dt(const LinearFinalizeParams &p, cudaStream_t stream) {
+cudaError_t launch_dt(const LinearFinalizeParams &p, const Plan &pl, cudaStream_t stream) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -244,29 +314,36 @@ cudaError_t launch_dt(const LinearFinalizeParams &p, cudaStream_t stream) {
   }
   const int es = (DT == SPECDEC_F32) ? 4 : 2;
   const int spr = stages_per_row(p.V, es);
-  const int nst = (spr + kC - 1) / kC;
-  const size_t smem = (size_t)kHeadBytes + (size_t)(2 * p.gamma + 1) * nst * kStageBytes;
-  small_verify_kernel<DT><<<(unsigned)(p.B * kC), kT, smem, stream>>>(p);
-  return cudaGetLastError();
+  const int nst = (spr + pl.C - 1) / pl.C;
+  const int rows = pl.qres ? 2 * p.gamma + 1 : p.gamma + 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * pl.C));
+  cfg.blockDim = dim3(kT);
+  cfg.dynamicSmemBytes = (size_t)kHeadBytes + (size_t)rows * nst * kStageBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)pl.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, small_verify_kernel<DT>, p, pl.C, pl.qres);
 }
 
 }  // namespace
 
 bool small_verify_applies(int B, int gamma, int V, int dtype, const void *logits, const void *q) {
-  const int es = (dtype == SPECDEC_F32) ? 4 : 2;
-  const long long rowbytes = (long long)V * es;
-  if (B < 1 || rowbytes % 16 != 0) return false;
-  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(q)) & 15) return false;
-  if ((long long)B * kC > device_sm_count()) return false;  // one CTA per SM, one wave
-  const int spr = stages_per_row(V, es);
-  const int nst = (spr + kC - 1) / kC;
-  return (long long)(2 * gamma + 1) * nst * kStageBytes <= kMaxDynSmem;
+  Plan pl;
+  return plan_for(B, gamma, V, dtype, logits, q, pl);
 }
 
 cudaError_t launch_small_verify(const LinearFinalizeParams &p, cudaStream_t stream) {
   if (p.B <= 0) return cudaSuccess;
-  return (p.dtype == SPECDEC_F32) ? launch_dt<SPECDEC_F32>(p, stream)
-                                  : launch_dt<SPECDEC_BF16>(p, stream);
+  Plan pl;
+  if (!plan_for(p.B, p.gamma, p.V, p.dtype, p.logits, p.q, pl)) return cudaErrorInvalidValue;
+  return (p.dtype == SPECDEC_F32) ? launch_dt<SPECDEC_F32>(p, pl, stream)
+                                  : launch_dt<SPECDEC_BF16>(p, pl, stream);
 }
 
 }  // namespace specdec

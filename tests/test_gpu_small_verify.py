@@ -1,7 +1,12 @@
-"""The one-launch path of specdec_verify_linear for small batches (one 8-CTA
-cluster per request, rows held in shared memory) against the two-kernel
+"""The one-launch path of specdec_verify_linear for small batches (one cluster
+of 8, 4 or 2 CTAs per request, rows held in shared memory; the q rows too when
+they fit, else q row k copied in after the decision) against the two-kernel
 path (specdec_row_stats, then specdec_linear_finalize) and the oracle:
-outputs, p_draft and the workspace's stage partials bit for bit."""
+outputs, p_draft and the workspace's stage partials bit for bit.
+
+With 152 SMs the cases below take: B <= 19 clusters of 8, B = 24 clusters of
+4, B = 40 .. 64 clusters of 2; the q rows are resident except in the cases
+marked "q row k after the decision"."""
 import numpy as np
 import pytest
 
@@ -53,6 +58,10 @@ def both_paths(w):
     ("linear_b64_g5_v32000_bf16", 19, None, None),    # the largest batch of one wave
     ("linear_b64_g5_v32000_bf16", 3, 4104, None),     # a last stage of 16 bytes
     ("mixed_b512_g4_v152064_bf16", 12, 30000, None),  # greedy rows, several temperatures
+    ("linear_b64_g5_v32000_bf16", 24, None, None),    # clusters of 4
+    ("linear_b64_g5_v32000_bf16", 64, None, None),    # the B = 64 workload: q row k after the decision
+    ("mixed_b512_g4_v152064_bf16", 40, 30000, None),  # greedy rows; q row k after the decision
+    ("linear_b1_g4_v32000_f32", 50, 16000, None),     # float32; q row k after the decision
 ])
 def test_one_launch_equals_two_and_the_oracle(oracle_lib, name, B, V, gamma):
     w = W.make_workload(name, B=B, V=V)
@@ -60,10 +69,11 @@ def test_one_launch_equals_two_and_the_oracle(oracle_lib, name, B, V, gamma):
     compare_linear(w, g, oracle_lib.verify_linear_workload(w))
 
 
-@pytest.mark.parametrize("gamma,V,dtype", [(1, 8, "f32"), (8, 64, "bf16"), (12, 2048, "f32"),
-                                           (5, 12288, "bf16")])
-def test_one_launch_edges(oracle_lib, gamma, V, dtype):
-    w = W.make_linear("normal2_tq08", B=4, gamma=gamma, V=V, dtype=dtype, seed=60 + gamma)
+@pytest.mark.parametrize("B,gamma,V,dtype", [(4, 1, 8, "f32"), (4, 8, 64, "bf16"),
+                                             (4, 12, 2048, "f32"), (4, 5, 12288, "bf16"),
+                                             (40, 4, 32768, "bf16")])  # q row k after the decision
+def test_one_launch_edges(oracle_lib, B, gamma, V, dtype):
+    w = W.make_linear("normal2_tq08", B=B, gamma=gamma, V=V, dtype=dtype, seed=60 + gamma)
     w.temperature[1] = 0.0                       # greedy
     w.draft_tokens[2, 0] = V                     # a token out of range: malformed
     g = both_paths(w)
