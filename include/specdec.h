@@ -130,12 +130,13 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
 
 /*
  * How many kernels specdec_verify_linear launches for these arguments: 1 when
- * a small batch takes the one-launch path (rows 16-byte aligned, logits and q
- * 16-byte aligned, B * 8 CTAs fitting the GPU at once, and the request's
- * gamma + 1 target rows and gamma q rows fitting the shared memory of an
- * 8-CTA cluster: each CTA holds 1/8 of every row), else 2 (the stats pass,
- * then the draw).  Both paths give the same outputs and leave the same
- * workspace.  0 for B = 0, -1 for invalid sizes.  Host only.
+ * a small batch takes the one-launch path, else 2 (the stats pass, then the
+ * draw).  The one-launch path runs one cluster of C CTAs per request, C the
+ * largest of 8, 4, 2 with B * C no more than the GPU's SMs; it needs rows
+ * 16-byte aligned, logits and q 16-byte aligned, and each CTA's 1/C share of
+ * the request's gamma + 1 target rows (plus the gamma q rows, or else of one
+ * q row) fitting its shared memory.  Both paths give the same outputs and
+ * leave the same workspace.  0 for B = 0, -1 for invalid sizes.  Host only.
  */
 int specdec_verify_linear_launches(int B, int gamma, int V, int dtype, const void *logits,
                                    const void *q);
