@@ -28,6 +28,11 @@
  *     *_host calls take host arrays and a device staging buffer); row-major;
  *   - logits and q hold float32 (SPECDEC_F32) or bfloat16 bits (SPECDEC_BF16),
  *     both in the same dtype;
+ *   - every device array starts on a multiple of its element size: 4 bytes
+ *     for float32 data and for the int32 / float32 arrays, 2 for bfloat16
+ *     data; a call given a misaligned device array returns
+ *     SPECDEC_ERR_INVALID_ARG and launches nothing (rows need not be 16-byte
+ *     aligned: such rows are read through aligned vectors and shifts);
  *   - uniforms are float32 values in (0, 1) that the caller draws (e.g. from a
  *     counter-based generator); the library draws no random numbers;
  *   - the library allocates nothing; scratch lives in a caller-provided
@@ -46,9 +51,10 @@
  *
  * Numerics: target probabilities are computed in float32 with base-2
  * exponentials (exp(z) = 2^(z log2 e)) and compared in float64; the final
- * draw sums its weights in float32 per 16 elements and in 52-bit fixed point
- * above that, so the crossing index of the inverse CDF is exact for the
- * weights the kernel computes.
+ * draw sums its weights in float32 over short runs of consecutive elements
+ * (one 16-byte vector, or 16 or 32 elements, depending on the kernel) and in
+ * 64-bit fixed point with 40 fraction bits above that, so the crossing index
+ * of the inverse CDF is exact for the weights the kernel computes.
  */
 #ifndef SPECDEC_H
 #define SPECDEC_H

@@ -3,6 +3,7 @@
 // nothing; see include/specdec.h for the contract of each call.
 #include <climits>
 #include <cstring>
+#include <initializer_list>
 
 #include "common.cuh"
 
@@ -82,6 +83,22 @@ int check_workspace(const void *ws, size_t ws_bytes, int B, int R, int V, int dt
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA; }
 
+// An array must start on a multiple of its element size: a misaligned
+// element load or store faults the device, so such pointers are refused here.
+bool misaligned(const void *ptr, uintptr_t elem) {
+  return (reinterpret_cast<uintptr_t>(ptr) & (elem - 1)) != 0;
+}
+
+// logits and q in their dtype; every other array holds 4-byte elements
+bool arrays_misaligned(int dtype, const void *logits, const void *q,
+                       std::initializer_list<const void *> words) {
+  const uintptr_t es = (uintptr_t)elem_bytes(dtype);
+  if (misaligned(logits, es) || misaligned(q, es)) return true;
+  for (const void *w : words)
+    if (misaligned(w, 4)) return true;
+  return false;
+}
+
 int launch_stats(const void *logits, const void *q, int dtype, const int32_t *tokens,
                  const float *temperature, int B, int R, int V, void *workspace,
                  cudaStream_t stream, bool entropy = false) {
@@ -141,6 +158,8 @@ int specdec_row_stats(const void *logits, const void *q, int dtype, const int32_
   if (linear == 1) return SPECDEC_ERR_INVALID_ARG;
   if (linear && (rows_per_request < 2 || rows_per_request - 1 > SPECDEC_MAX_GAMMA))
     return SPECDEC_ERR_INVALID_ARG;
+  if (arrays_misaligned(dtype, logits, q, {draft_tokens, temperature}))
+    return SPECDEC_ERR_INVALID_ARG;
   st = check_workspace(workspace, workspace_bytes, B, rows_per_request, V, dtype);
   if (st != SPECDEC_OK) return st;
   return launch_stats(logits, linear ? q : nullptr, dtype, linear ? draft_tokens : nullptr,
@@ -151,8 +170,8 @@ int specdec_row_stats(const void *logits, const void *q, int dtype, const int32_
 static int linear_checks(const void *logits, const void *q, int dtype, const int32_t *tokens,
                          const float *temperature, const float *uniforms, int B, int gamma,
                          int V, int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
-                         uint8_t *is_bonus, int32_t *row_status, void *workspace,
-                         size_t workspace_bytes) {
+                         uint8_t *is_bonus, int32_t *row_status, const float *p_draft,
+                         void *workspace, size_t workspace_bytes) {
   if (gamma < 1) return SPECDEC_ERR_INVALID_ARG;
   if (gamma > SPECDEC_MAX_GAMMA) return SPECDEC_ERR_UNSUPPORTED;
   int st = check_sizes(B, gamma + 1, V, dtype);
@@ -160,6 +179,10 @@ static int linear_checks(const void *logits, const void *q, int dtype, const int
   if (B == 0) return SPECDEC_OK;
   if (!logits || !q || !tokens || !temperature || !uniforms || !n_accepted || !out_tokens ||
       !final_token || !is_bonus || !row_status)
+    return SPECDEC_ERR_INVALID_ARG;
+  if (arrays_misaligned(dtype, logits, q,
+                        {tokens, temperature, uniforms, n_accepted, out_tokens, final_token,
+                         row_status, p_draft}))
     return SPECDEC_ERR_INVALID_ARG;
   return check_workspace(workspace, workspace_bytes, B, gamma + 1, V, dtype);
 }
@@ -216,7 +239,7 @@ int specdec_linear_finalize(const void *logits, const void *q, int dtype,
                             void *workspace, size_t workspace_bytes, void *stream) {
   const int st = linear_checks(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma,
                                V, n_accepted, out_tokens, final_token, is_bonus, row_status,
-                               workspace, workspace_bytes);
+                               p_draft, workspace, workspace_bytes);
   if (st != SPECDEC_OK || B == 0) return st;
   return linear_finalize_launch(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma,
                                 V, n_accepted, out_tokens, final_token, is_bonus, row_status,
@@ -230,8 +253,8 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
                           uint8_t *is_bonus, int32_t *row_status, float *p_draft,
                           void *workspace, size_t workspace_bytes, void *stream) {
   int st = linear_checks(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
-                         n_accepted, out_tokens, final_token, is_bonus, row_status, workspace,
-                         workspace_bytes);
+                         n_accepted, out_tokens, final_token, is_bonus, row_status, p_draft,
+                         workspace, workspace_bytes);
   if (st != SPECDEC_OK || B == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (small_verify_applies(B, gamma, V, dtype, logits, q)) {
@@ -260,8 +283,8 @@ static int tree_checks(const void *logits, const void *q, int dtype, const int32
                        const int32_t *parent, const float *temperature, const float *uniforms,
                        int B, int N, int V, int max_depth, int32_t *n_accepted,
                        int32_t *path_nodes, int32_t *out_tokens, int32_t *final_token,
-                       uint8_t *is_bonus, int32_t *row_status, void *workspace,
-                       size_t workspace_bytes) {
+                       uint8_t *is_bonus, int32_t *row_status, const float *p_node,
+                       void *workspace, size_t workspace_bytes) {
   if (N < 1 || max_depth < 0) return SPECDEC_ERR_INVALID_ARG;
   if (N > SPECDEC_MAX_TREE_NODES || max_depth > SPECDEC_MAX_TREE_DEPTH)
     return SPECDEC_ERR_UNSUPPORTED;
@@ -270,6 +293,10 @@ static int tree_checks(const void *logits, const void *q, int dtype, const int32
   if (B == 0) return SPECDEC_OK;
   if (!logits || !q || !tokens || !parent || !temperature || !uniforms || !n_accepted ||
       !path_nodes || !out_tokens || !final_token || !is_bonus || !row_status)
+    return SPECDEC_ERR_INVALID_ARG;
+  if (arrays_misaligned(dtype, logits, q,
+                        {tokens, parent, temperature, uniforms, n_accepted, path_nodes,
+                         out_tokens, final_token, row_status, p_node}))
     return SPECDEC_ERR_INVALID_ARG;
   return check_workspace(workspace, workspace_bytes, B, N, V, dtype);
 }
@@ -314,7 +341,7 @@ int specdec_tree_finalize(const void *logits, const void *q, int dtype,
                           size_t workspace_bytes, void *stream) {
   const int st = tree_checks(logits, q, dtype, node_tokens, parent, temperature, uniforms, B, N,
                              V, max_depth, n_accepted, path_nodes, out_tokens, final_token,
-                             is_bonus, row_status, workspace, workspace_bytes);
+                             is_bonus, row_status, p_node, workspace, workspace_bytes);
   if (st != SPECDEC_OK || B == 0) return st;
   return tree_finalize_launch(logits, q, dtype, node_tokens, parent, temperature, uniforms, B, N,
                               V, max_depth, n_accepted, path_nodes, out_tokens, final_token,
@@ -330,7 +357,7 @@ int specdec_verify_tree(const void *logits, const void *q, int dtype, const int3
                         size_t workspace_bytes, void *stream) {
   int st = tree_checks(logits, q, dtype, node_tokens, parent, temperature, uniforms, B, N, V,
                        max_depth, n_accepted, path_nodes, out_tokens, final_token, is_bonus,
-                       row_status, workspace, workspace_bytes);
+                       row_status, p_node, workspace, workspace_bytes);
   if (st != SPECDEC_OK || B == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = launch_stats(logits, nullptr, dtype, nullptr, temperature, B, N, V, workspace, s);
@@ -347,6 +374,7 @@ int specdec_philox_uniforms(const uint64_t *key, const uint64_t *counter,
   if (n < 0) return SPECDEC_ERR_INVALID_ARG;
   if (n == 0) return SPECDEC_OK;
   if (!key || !counter || !out) return SPECDEC_ERR_INVALID_ARG;
+  if (misaligned(out, 4)) return SPECDEC_ERR_INVALID_ARG;
   if (n > SPECDEC_MAX_UNIFORMS) return SPECDEC_ERR_UNSUPPORTED;
   if (first_word > ~0ull - (unsigned long long)(n - 1)) return SPECDEC_ERR_INVALID_ARG;
   PhiloxParams p;
@@ -366,6 +394,7 @@ int specdec_row_entropy(const void *workspace, size_t workspace_bytes, int dtype
   if (st != SPECDEC_OK) return st;
   if (B == 0) return SPECDEC_OK;
   if (!temperature || !entropy) return SPECDEC_ERR_INVALID_ARG;
+  if (misaligned(temperature, 4) || misaligned(entropy, 4)) return SPECDEC_ERR_INVALID_ARG;
   st = check_workspace(workspace, workspace_bytes, B, rows_per_request, V, dtype);
   if (st != SPECDEC_OK) return st;
   return cuda_status(launch_row_entropy(reinterpret_cast<const RowPartial *>(workspace),
@@ -382,6 +411,7 @@ int specdec_row_alpha(const void *logits, const void *q, int dtype, const float 
   if (st != SPECDEC_OK) return st;
   if (B == 0) return SPECDEC_OK;
   if (!logits || !q || !temperature || !alpha) return SPECDEC_ERR_INVALID_ARG;
+  if (arrays_misaligned(dtype, logits, q, {temperature, alpha})) return SPECDEC_ERR_INVALID_ARG;
   st = check_workspace(workspace, workspace_bytes, B, gamma + 1, V, dtype);
   if (st != SPECDEC_OK) return st;
   return cuda_status(launch_row_alpha(logits, q, dtype, reinterpret_cast<const RowPartial *>(workspace),
@@ -398,6 +428,9 @@ int specdec_path_logprob(const void *logits, int dtype, const float *temperature
   if (st != SPECDEC_OK) return st;
   if (B == 0) return SPECDEC_OK;
   if (!logits || !temperature || !out_tokens || !n_accepted || !logprob || path_len < 1)
+    return SPECDEC_ERR_INVALID_ARG;
+  if (arrays_misaligned(dtype, logits, nullptr,
+                        {temperature, out_tokens, n_accepted, path_nodes, row_status, logprob}))
     return SPECDEC_ERR_INVALID_ARG;
   st = check_workspace(workspace, workspace_bytes, B, rows_per_request, V, dtype);
   if (st != SPECDEC_OK) return st;
@@ -428,8 +461,8 @@ int specdec_verify_linear_topk(const void *logits, const void *q, int dtype,
   if (topk < 1) return SPECDEC_ERR_INVALID_ARG;
   if (topk > SPECDEC_MAX_TOPK) return SPECDEC_ERR_UNSUPPORTED;
   int st = linear_checks(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
-                         n_accepted, out_tokens, final_token, is_bonus, row_status, workspace,
-                         workspace_bytes);
+                         n_accepted, out_tokens, final_token, is_bonus, row_status, p_draft,
+                         workspace, workspace_bytes);
   if (st != SPECDEC_OK || B == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = launch_stats(logits, q, dtype, draft_tokens, temperature, B, gamma + 1, V, workspace, s);

@@ -83,40 +83,76 @@ __device__ __forceinline__ Draw make_draw(const LinearFinalizeParams &p, long lo
   return w;
 }
 
-// Elements are read 64 bytes (four 16-byte vectors) per array at a time: 32
-// bf16 or 16 float32 values.
+// Two 16-byte vectors of the bytes at p (2-byte aligned, not necessarily
+// 16-byte aligned): the aligned 16-byte vectors that overlap those 32 bytes
+// (three, or two when p is 16-byte aligned), then whole-word and half-word
+// shifts.  Each vector read holds at least one of the 32 bytes, and an
+// aligned 16-byte vector never straddles a page, so no read leaves the pages
+// of the caller's buffer.
+__device__ __forceinline__ void load32_shifted(const uint8_t *p, uint4 &o0, uint4 &o1) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const unsigned mis = (unsigned)(a & 15u);
+  const uint4 *v = reinterpret_cast<const uint4 *>(a - mis);
+  const uint4 x0 = __ldg(v), x1 = __ldg(v + 1);
+  const uint4 x2 = mis ? __ldg(v + 2) : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t w[12] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w, x2.x, x2.y, x2.z, x2.w};
+  const unsigned ws = mis >> 2, hs = (mis & 2u) ? 16u : 0u;
+  uint32_t d[9];
+#pragma unroll
+  for (int j = 0; j < 9; ++j)
+    d[j] = ws == 0 ? w[j] : ws == 1 ? w[j + 1] : ws == 2 ? w[j + 2] : w[j + 3];
+  o0 = make_uint4(__funnelshift_r(d[0], d[1], hs), __funnelshift_r(d[1], d[2], hs),
+                  __funnelshift_r(d[2], d[3], hs), __funnelshift_r(d[3], d[4], hs));
+  o1 = make_uint4(__funnelshift_r(d[4], d[5], hs), __funnelshift_r(d[5], d[6], hs),
+                  __funnelshift_r(d[6], d[7], hs), __funnelshift_r(d[7], d[8], hs));
+}
+
+// Elements are read 32 bytes (two 16-byte vectors) per array at a time: 16
+// bf16 or 8 float32 values.
 template <int DT>
 struct Sub {
   static constexpr int kEs = (DT == SPECDEC_F32) ? 4 : 2;
-  static constexpr int kElems = 64 / kEs;
-  uint4 l[4], q[4];
+  static constexpr int kElems = 32 / kEs;
+  uint4 l[2], q[2];
 
   // the raw bits of element i (a compile-time index after unrolling)
-  __device__ __forceinline__ static uint32_t word(const uint4 (&v)[4], int j) {
+  __device__ __forceinline__ static uint32_t word(const uint4 (&v)[2], int j) {
     const uint4 x = v[j >> 2];
     return (j & 3) == 0 ? x.x : (j & 3) == 1 ? x.y : (j & 3) == 2 ? x.z : x.w;
   }
-  __device__ __forceinline__ static float value(const uint4 (&v)[4], int i) {
+  __device__ __forceinline__ static float value(const uint4 (&v)[2], int i) {
     if (DT == SPECDEC_F32) return __uint_as_float(word(v, i));
     const uint32_t w = word(v, i >> 1);
     return (i & 1) ? bf16_hi(w) : bf16_lo(w);
   }
 
-  // Elements [e, e + kElems): 16-byte loads when aligned and inside the row,
-  // else element loads with l = -inf, q = 0 beyond V (weight 0 there).
+  // Elements [e, e + kElems): 16-byte loads inside the row (shifted into
+  // place when the row is not 16-byte aligned); element loads in the row's
+  // last partial group, with l = -inf, q = 0 beyond V (weight 0 there).
   __device__ __forceinline__ void load(const Draw &w, int e) {
-    if (w.vec_ok && e + kElems <= w.V) {
-      const uint4 *lp = reinterpret_cast<const uint4 *>(w.lrow + (size_t)e * kEs);
-      const uint4 *qp = reinterpret_cast<const uint4 *>(w.qrow + (size_t)e * kEs);
+    if (e + kElems <= w.V) {
+      const uint8_t *lb = w.lrow + (size_t)e * kEs;
+      const uint8_t *qb = w.qrow + (size_t)e * kEs;
+      if (w.vec_ok) {
+        const uint4 *lp = reinterpret_cast<const uint4 *>(lb);
+        const uint4 *qp = reinterpret_cast<const uint4 *>(qb);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) l[k] = __ldg(lp + k);
+        for (int k = 0; k < 2; ++k) l[k] = __ldg(lp + k);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) q[k] = w.use_q ? __ldg(qp + k) : make_uint4(0u, 0u, 0u, 0u);
+        for (int k = 0; k < 2; ++k) q[k] = w.use_q ? __ldg(qp + k) : make_uint4(0u, 0u, 0u, 0u);
+        return;
+      }
+      load32_shifted(lb, l[0], l[1]);
+      if (w.use_q) {
+        load32_shifted(qb, q[0], q[1]);
+      } else {
+        q[0] = q[1] = make_uint4(0u, 0u, 0u, 0u);
+      }
       return;
     }
-    uint32_t lw[16], qw[16];
+    uint32_t lw[8], qw[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) lw[j] = qw[j] = 0u;
+    for (int j = 0; j < 8; ++j) lw[j] = qw[j] = 0u;
 #pragma unroll
     for (int i = 0; i < kElems; ++i) {
       const int v = e + i;
@@ -132,7 +168,7 @@ struct Sub {
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < 2; ++k) {
       l[k] = make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
       q[k] = make_uint4(qw[4 * k], qw[4 * k + 1], qw[4 * k + 2], qw[4 * k + 3]);
     }

@@ -97,6 +97,80 @@ def test_argument_checks_before_any_device_work(lib):
     assert rs(d, N, BF16, N, d, 2, 9, 1000, 2, d, 1 << 30, N) == 1
 
 
+def test_misaligned_arrays_are_refused_before_any_device_work(lib):
+    """Each device array must start on a multiple of its element size (2 bytes
+    for bf16 data, 4 for float32 data and the int32 / float32 arrays); the call
+    returns INVALID_ARG (1) before launching anything.  With every array
+    aligned and no workspace, the workspace check is the one that fails (3)."""
+    from speculative_decoding_verification_64_gb300.binding import BF16, F32
+    P = ctypes.c_void_p
+    N = None
+    a, two, odd = P(0x10000), P(0x10002), P(0x10001)   # never dereferenced
+
+    def linear_args(**kw):
+        names = ["logits", "q", "dtype", "tokens", "temperature", "uniforms", "B", "gamma",
+                 "V", "n_accepted", "out_tokens", "final_token", "is_bonus", "row_status",
+                 "p_draft", "workspace", "ws_bytes", "stream"]
+        vals = dict(logits=a, q=a, dtype=BF16, tokens=a, temperature=a, uniforms=a, B=4,
+                    gamma=4, V=1000, n_accepted=a, out_tokens=a, final_token=a, is_bonus=a,
+                    row_status=a, p_draft=N, workspace=N, ws_bytes=0, stream=N)
+        vals.update(kw)
+        return [vals[n] for n in names]
+
+    vl = lib.specdec_verify_linear
+    assert vl(*linear_args()) == 3
+    assert vl(*linear_args(logits=two, q=two)) == 3          # bf16: 2-byte alignment suffices
+    assert vl(*linear_args(is_bonus=odd)) == 3               # uint8: any address
+    assert vl(*linear_args(logits=odd)) == 1
+    assert vl(*linear_args(q=odd)) == 1
+    assert vl(*linear_args(dtype=F32, logits=two)) == 1
+    assert vl(*linear_args(dtype=F32, q=two)) == 1
+    for name in ("tokens", "temperature", "uniforms", "n_accepted", "out_tokens",
+                 "final_token", "row_status", "p_draft"):
+        assert vl(*linear_args(**{name: two})) == 1, name
+    tk = lib.specdec_verify_linear_topk
+    args = linear_args(logits=odd)
+    assert tk(*(args[:9] + [32] + args[9:])) == 1
+    args = linear_args()
+    assert tk(*(args[:9] + [32] + args[9:])) == 3
+
+    def tree_args(**kw):
+        names = ["logits", "q", "dtype", "tokens", "parent", "temperature", "uniforms", "B", "N",
+                 "V", "max_depth", "n_accepted", "path_nodes", "out_tokens", "final_token",
+                 "is_bonus", "row_status", "p_node", "workspace", "ws_bytes", "stream"]
+        vals = dict(logits=a, q=a, dtype=BF16, tokens=a, parent=a, temperature=a, uniforms=a,
+                    B=2, N=64, V=1000, max_depth=5, n_accepted=a, path_nodes=a, out_tokens=a,
+                    final_token=a, is_bonus=odd, row_status=a, p_node=N, workspace=N,
+                    ws_bytes=0, stream=N)
+        vals.update(kw)
+        return [vals[n] for n in names]
+
+    vt = lib.specdec_verify_tree
+    assert vt(*tree_args()) == 3
+    for name in ("logits", "q"):
+        assert vt(*tree_args(**{name: odd})) == 1, name
+    for name in ("tokens", "parent", "temperature", "uniforms", "n_accepted", "path_nodes",
+                 "out_tokens", "final_token", "row_status", "p_node"):
+        assert vt(*tree_args(**{name: two})) == 1, name
+
+    rs = lib.specdec_row_stats
+    assert rs(a, a, BF16, a, a, 2, 9, 1000, 0, N, 0, N) == 3
+    assert rs(odd, a, BF16, a, a, 2, 9, 1000, 0, N, 0, N) == 1
+    assert rs(a, a, BF16, two, a, 2, 9, 1000, 0, N, 0, N) == 1
+    assert rs(a, N, F32, N, two, 2, 9, 1000, 0, N, 0, N) == 1
+    ra = lib.specdec_row_alpha
+    assert ra(a, a, BF16, a, 2, 8, 1000, N, 0, a, N) == 3
+    assert ra(a, odd, BF16, a, 2, 8, 1000, N, 0, a, N) == 1
+    assert ra(a, a, BF16, a, 2, 8, 1000, N, 0, two, N) == 1
+    lp = lib.specdec_path_logprob
+    assert lp(a, BF16, a, a, a, N, N, 2, 9, 1000, 9, N, 0, a, N) == 3
+    assert lp(odd, BF16, a, a, a, N, N, 2, 9, 1000, 9, N, 0, a, N) == 1
+    assert lp(a, BF16, a, a, a, two, N, 2, 9, 1000, 9, N, 0, a, N) == 1
+    en = lib.specdec_row_entropy
+    assert en(N, 0, BF16, a, 2, 9, 1000, a, N) == 3
+    assert en(N, 0, BF16, a, 2, 9, 1000, two, N) == 1
+
+
 def test_binding_refuses_to_run_without_the_library(tmp_path):
     from speculative_decoding_verification_64_gb300 import binding
     with pytest.raises(binding.SpecdecError):
