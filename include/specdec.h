@@ -230,7 +230,9 @@ int specdec_verify_tree(const void *logits, const void *q, int dtype,
  * graph.  All calls share the one array: calls whose work overlaps on the GPU
  * (different streams without ordering, or different host threads) race and
  * corrupt each other's results; serialise them.  Nothing in the array needs
- * to start at zero.
+ * to start at zero.  The looked-up address lives as long as the device's
+ * context: do not call this entry point after cudaDeviceReset of that device
+ * in the same process.
  */
 #define SPECDEC_STATIC_SCRATCH_BYTES (4u << 20)
 int specdec_verify_linear_static(const void *logits, const void *q, int dtype,
