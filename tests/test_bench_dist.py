@@ -75,3 +75,29 @@ def test_algorithmic_bytes_counts_every_logit_once():
     assert ab["q_rows"] == 2 * 1000 * 2
     assert ab["total"] > ab["logits"] + ab["q_rows"]
     assert np.isclose(ab["total"], ab["logits"] + ab["q_rows"] + ab["small"])
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    """The reference arm (the float64 oracle on the host cores) prints one JSON
+    line with the keys the benchmark contract names, on the same metric."""
+    import json
+    import bench
+    args = bench.parse_args(["--impl", "reference", "--steps", "2", "--warmup", "3",
+                             "--batch", "3", "--vocab", "300"])
+    bench.run_reference(args, bench.Dist())
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["metric"] == bench.METRIC and d["impl"] == "reference"
+    assert d["steps"] == 2 and d["warmup"] >= 3 and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["unit"] == "positions/s"
+    assert "workload" in d["config"]
+    for key in ("value", "unit", "cores", "kind", "sample"):
+        assert key in d["cpu_baseline"], key
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
