@@ -151,6 +151,20 @@ def _stream_ptr(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _cuda(**tensors):
+    """Every given tensor (None skipped) must live on one CUDA device: the
+    library reads and writes device memory only, and has no CPU path."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor, got {t.device}")
+        if dev is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other arrays on {dev}")
+        dev = t.device
+
+
 def _req(t: torch.Tensor, name: str, dtype, shape, device):
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -202,6 +216,9 @@ class TreeOut:
 
 
 def _linear_args(logits, q, draft_tokens, temperature, uniforms, out, workspace):
+    _cuda(logits=logits, q=q, draft_tokens=draft_tokens, temperature=temperature,
+          uniforms=uniforms, workspace=workspace,
+          **({} if out is None else {k: v for k, v in vars(out).items()}))
     B, R, V = logits.shape
     gamma = R - 1
     dev = logits.device
@@ -261,6 +278,8 @@ def row_stats(logits: torch.Tensor, temperature: torch.Tensor, workspace: torch.
     workspace.  For the linear form pass q and draft_tokens too (phase 2 needs the
     drafted tokens' logits and q values, gathered here).  ``entropy`` keeps the sums
     ``row_entropy`` reads."""
+    _cuda(logits=logits, temperature=temperature, workspace=workspace, q=q,
+          draft_tokens=draft_tokens)
     B, R, V = logits.shape
     rc = load_library().specdec_row_stats(
         _ptr(logits), _ptr(q), dtype_code(logits), _ptr(draft_tokens), _ptr(temperature), B, R, V,
@@ -284,6 +303,9 @@ def linear_finalize(logits, q, draft_tokens, temperature, uniforms, out: LinearO
 
 def _tree_args(logits, q, node_tokens, parent, temperature, uniforms, max_depth, out,
                workspace):
+    _cuda(logits=logits, q=q, node_tokens=node_tokens, parent=parent, temperature=temperature,
+          uniforms=uniforms, workspace=workspace,
+          **({} if out is None else {k: v for k, v in vars(out).items()}))
     B, N, V = logits.shape
     dev = logits.device
     dt = dtype_code(logits)
@@ -495,6 +517,7 @@ def row_entropy(logits: torch.Tensor, temperature: torch.Tensor, workspace: torc
                 stream=None) -> torch.Tensor:
     """Entropies [B, R] of the target rows of ``logits`` from the workspace of a
     ``row_stats(..., entropy=True)`` call on those logits (``specdec_row_entropy``)."""
+    _cuda(logits=logits, temperature=temperature, workspace=workspace)
     B, R, V = logits.shape
     out = torch.empty((B, R), dtype=torch.float32, device=logits.device)
     rc = load_library().specdec_row_entropy(_ptr(workspace), workspace.numel(), dtype_code(logits),
@@ -517,6 +540,7 @@ def row_alpha(logits: torch.Tensor, q: torch.Tensor, temperature: torch.Tensor,
     """Acceptance rates [B, gamma], sum_v min(p_i, q_i) of every drafted row, from the
     logits [B, gamma+1, V], q [B, gamma, V] and the workspace of a ``row_stats`` call on
     those logits (``specdec_row_alpha``)."""
+    _cuda(logits=logits, q=q, temperature=temperature, workspace=workspace)
     B, R, V = logits.shape
     gamma = R - 1
     out = torch.empty((B, gamma), dtype=torch.float32, device=logits.device)
@@ -532,6 +556,8 @@ def path_logprob(logits: torch.Tensor, temperature: torch.Tensor, out_tokens: to
                  path_nodes: Optional[torch.Tensor] = None,
                  row_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Log-probabilities [B] of the emitted paths (``specdec_path_logprob``)."""
+    _cuda(logits=logits, temperature=temperature, out_tokens=out_tokens, n_accepted=n_accepted,
+          workspace=workspace, path_nodes=path_nodes, row_status=row_status)
     B, R, V = logits.shape
     out = torch.empty(B, dtype=torch.float32, device=logits.device)
     rc = load_library().specdec_path_logprob(

@@ -304,3 +304,33 @@ def test_host_call_argument_checks(lib):
     need = lib.specdec_tree_staging_size(2, 64, 1000, 5, BF16)
     assert vt(d, d, BF16, d, d, d, d, 2, 64, 1000, 5, d, d, d, d, d, d, N, d, need - 1,
               N) == 3
+
+
+def test_binding_refuses_host_tensors_for_device_calls():
+    """The device calls take CUDA tensors only: host tensors are refused in the
+    binding, before the library is called (the host-buffer calls are the ones
+    for host memory)."""
+    import torch
+    from speculative_decoding_verification_64_gb300 import binding
+    B, g, V = 2, 3, 50
+    logits = torch.zeros(B, g + 1, V)
+    q = torch.full((B, g, V), 1.0 / V)
+    toks = torch.zeros(B, g, dtype=torch.int32)
+    temp = torch.ones(B)
+    uni = torch.full((B, g + 1), 0.5)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.verify_linear(logits, q, toks, temp, uni)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.verify_linear_topk(logits, q, toks, temp, uni, 4)
+    par = torch.tensor([[-1, 0, 0, 1]] * B, dtype=torch.int32)
+    tl = torch.zeros(B, 4, V)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.verify_tree(tl, tl, torch.zeros(B, 4, dtype=torch.int32), par, temp,
+                            torch.full((B, 4), 0.5), 3)
+    ws = torch.empty(1 << 16, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.row_stats(logits, temp, ws)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.row_alpha(logits, q, temp, ws)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.row_entropy(logits, temp, ws)
