@@ -12,8 +12,13 @@ Prints ONE JSON line (rank 0):
   e2e        the same metric through the C-ABI host-buffer call with pinned
              HOST buffers: host->device copy of the step's inputs, the verify
              and the device->host copy of its outputs inside the timed region;
-  roofline   the row-statistics kernel: algorithmic bytes per launch / its
-             CUDA-event time against the measured HBM copy peak;
+  roofline   the dominant kernel: algorithmic bytes per launch / its
+             CUDA-event time against the measured HBM copy peak.  The kernel
+             times come from steps issued as separate phases with events
+             around each, AFTER the timed region (the timed steps are plain
+             verify calls only);
+  workloads  the other named workloads, each measured the same way in this
+             process (step time, positions/s, requests/s, GB/s, fractions);
   cpu_baseline  the float64 oracle on the host cores, on a bounded sample.
 
 --impl reference times the oracle (the only other implementation there is)
@@ -67,6 +72,11 @@ def parse_args(argv=None):
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="skip timing the step replayed from CUDA graphs (reported beside the "
                          "eager value, never instead of it)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other named workloads (measured after the headline one, "
+                         "reported under 'workloads')")
+    ap.add_argument("--workload-steps", type=int, default=400,
+                    help="timed steps of each of the other workloads")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (a smaller case for profiling; not a bench line)")
     ap.add_argument("--vocab", type=int, default=None,
@@ -249,6 +259,157 @@ def algorithmic_bytes(w, n_accepted_rows_rejected: float) -> dict:
     return dict(logits=logits, q_rows=q_rows, small=small, total=logits + q_rows + small)
 
 
+def _verify_fn(binding, w, linear, out, ws, topk):
+    """One public verify call on an input set (the step), on a given stream."""
+    def verify(x, on):
+        if topk:
+            binding.verify_linear_topk(*x, topk, out=out, workspace=ws, stream=on)
+        elif linear:
+            binding.verify_linear(*x, out=out, workspace=ws, stream=on)
+        else:
+            binding.verify_tree(*x, w.max_depth, out=out, workspace=ws, stream=on)
+    return verify
+
+
+def _phase_fns(binding, w, linear, out, ws):
+    """The two phases of the two-launch path, issued separately (per-kernel times)."""
+    def stats(x, on):
+        if linear:
+            binding.row_stats(x[0], x[3], ws, q=x[1], draft_tokens=x[2], stream=on)
+        else:
+            binding.row_stats(x[0], x[4], ws, stream=on)
+
+    def finalize(x, on):
+        if linear:
+            binding.linear_finalize(*x, out, ws, stream=on)
+        else:
+            binding.tree_finalize(*x, w.max_depth, out, ws, stream=on)
+    return stats, finalize
+
+
+class Setup:
+    """A workload's resident input sets, outputs and workspace on the device."""
+
+    def __init__(self, binding, w, device, topk=0):
+        self.w = w
+        self.linear = isinstance(w, W.LinearWorkload)
+        inputs = (binding.linear_inputs_to_device(w, device) if self.linear
+                  else binding.tree_inputs_to_device(w, device))
+        # resident input sets used in turn, enough of them that a step's inputs
+        # were last touched at least 3 x L2 bytes of other inputs ago (two for
+        # the large workloads, many copies of the small ones)
+        set_bytes = sum(t.numel() * t.element_size() for t in inputs)
+        self.n_sets, self.l2_note = input_rotation(set_bytes)
+        self.sets = [inputs] + [tuple(t.clone() for t in inputs) for _ in range(self.n_sets - 1)]
+        self.dt = binding.dtype_code(inputs[0])
+        self.ws = binding.alloc_workspace(w.B, w.rows, w.V, self.dt, device)
+        self.out = (binding.LinearOut.empty(w.B, w.gamma, device) if self.linear
+                    else binding.TreeOut.empty(w.B, w.N, w.max_depth, device))
+        self.topk = topk if self.linear else 0
+        self.units = w.B * w.gamma if self.linear else w.B * (w.N - 1)
+        self.verify = _verify_fn(binding, w, self.linear, self.out, self.ws, self.topk)
+        self.stats, self.finalize = _phase_fns(binding, w, self.linear, self.out, self.ws)
+        # launches of one verify call: 1 (one kernel) or 2 (stats pass, then the draw)
+        if self.topk:
+            self.launches = 2
+        elif self.linear:
+            self.launches = binding.verify_linear_launches(inputs[0], inputs[1])
+        else:
+            self.launches = 2
+
+
+def time_steps(torch, st, K, warmup, stream, dist, sampler=None):
+    """K verify calls back to back between two events (after `warmup` calls);
+    every call is the public entry point, nothing else is issued in between."""
+    for s in range(max(warmup, 3)):
+        st.verify(st.sets[s % st.n_sets], stream)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("begin")
+    t0.record(stream)
+    for s in range(K):
+        st.verify(st.sets[s % st.n_sets], stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("end")
+    dist.barrier()
+    return t0.elapsed_time(t1)
+
+
+def time_phases(torch, st, n, stream):
+    """Per-kernel times, measured apart from the timed steps: `n` steps issued
+    as separate phases with events around each (two-launch path), or the
+    one-kernel call between two events.  Medians in ms."""
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for s in range(n):
+        x = st.sets[s % st.n_sets]
+        e0, e1, e2 = ev[s]
+        e0.record(stream)
+        if st.launches == 1 or st.topk:
+            st.verify(x, stream)
+            e1.record(stream)
+        else:
+            st.stats(x, stream)
+            e1.record(stream)
+            st.finalize(x, stream)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    a = float(np.median([e[0].elapsed_time(e[1]) for e in ev]))
+    b = float(np.median([e[1].elapsed_time(e[2]) for e in ev]))
+    return a, b
+
+
+def kernel_names(st):
+    if st.topk:
+        return "row_stats_kernel + topk_draw_kernel"
+    if st.linear and st.launches == 1:
+        return "small_verify_kernel"
+    return "row_stats_kernel"
+
+
+def workload_line(torch, binding, st, ms_per_step, k1_ms, k2_ms, peak, name):
+    """Per-workload figures: step time, throughput, algorithmic GB/s and the
+    dominant kernel's roofline (from the separately timed phases)."""
+    w = st.w
+    nb = st.out.is_bonus.cpu().numpy()
+    rejected = 0.0 if st.topk else float((nb == 0).sum())
+    ab = algorithmic_bytes(w, rejected)
+    gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
+    es = w.elem_bytes
+    spr = -(-w.V * es // 8192)
+    kname = kernel_names(st)
+    if st.topk or st.launches == 1:
+        k_bytes, traffic = ab["total"], None
+    else:
+        k_bytes = ab["logits"] + w.B * w.rows * spr * 16
+        traffic = ncu_traffic(name, kname)
+    k_gbs = k_bytes / (k1_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(k_gbs, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(k_gbs / peak, 4),
+                "traffic": traffic, "algorithmic_bytes_per_launch": int(k_bytes),
+                "avg_launch_us": round(k1_ms * 1e3, 2)}
+    if k1_ms > ms_per_step * 1.0001:
+        # a kernel cannot take longer than the step it belongs to: the phase
+        # timing is not trustworthy, so no fraction is claimed
+        roofline.update(achieved=None, frac=None,
+                        note=f"kernel median {k1_ms * 1e3:.2f} us > step {ms_per_step * 1e3:.2f} us")
+    if st.topk:
+        phase = {"verify_topk": round(k1_ms * 1e3, 2)}
+    elif st.launches == 1:
+        phase = {"verify_one_launch": round(k1_ms * 1e3, 2)}
+    else:
+        phase = {"row_stats": round(k1_ms * 1e3, 2), "finalize": round(k2_ms * 1e3, 2)}
+    return dict(ab=ab, gbs=gbs, roofline=roofline, phase=phase)
+
+
+PHASE_STEPS = 64  # separately issued phase-split steps for the per-kernel medians
+
+
 def run_ours(args, dist):
     import torch
     from speculative_decoding_verification_64_gb300 import binding
@@ -263,151 +424,42 @@ def run_ours(args, dist):
     binding.load_library()
 
     w = W.make_workload(args.workload, B=args.batch, V=args.vocab, seed_offset=1000 * dist.rank)
-    linear = isinstance(w, W.LinearWorkload)
-    R = w.rows
-    es = w.elem_bytes
-    if linear:
-        inputs = binding.linear_inputs_to_device(w, device)
-        gamma = w.gamma
-        units = w.B * gamma               # verified draft positions per step
-    else:
-        inputs = binding.tree_inputs_to_device(w, device)
-        gamma = w.N - 1
-        units = w.B * (w.N - 1)
-    # resident input sets used in turn, enough of them that a step's inputs were
-    # last touched at least 3 x L2 bytes of other inputs ago (two for the
-    # large workloads, many copies of the small ones)
-    set_bytes = sum(t.numel() * t.element_size() for t in inputs)
-    n_sets, l2_note = input_rotation(set_bytes)
-    sets = [inputs] + [tuple(t.clone() for t in inputs) for _ in range(n_sets - 1)]
-    dt = binding.dtype_code(inputs[0])
-    ws = binding.alloc_workspace(w.B, R, w.V, dt, device)
-    out = (binding.LinearOut.empty(w.B, w.gamma, device) if linear
-           else binding.TreeOut.empty(w.B, w.N, w.max_depth, device))
+    st = Setup(binding, w, device, args.topk)
+    linear = st.linear
+    launches, l2_note = st.launches, st.l2_note
     stream = torch.cuda.current_stream(device)
-    lib = binding.load_library()
-
-    def stats(x):
-        if linear:
-            binding.row_stats(x[0], x[3], ws, q=x[1], draft_tokens=x[2], stream=stream)
-        else:
-            binding.row_stats(x[0], x[4], ws, stream=stream)
-
-    # one step = one public verify call (its two launches).  Every
-    # PHASE_EVERY-th timed step is issued as the call's two phases instead,
-    # with events around each, for the per-kernel times; the events cost the
-    # step a few microseconds, so they are kept off the other steps.
-    kernels = 2
-
-    def finalize(x):
-        if linear:
-            binding.linear_finalize(*x, out, ws, stream=stream)
-        else:
-            binding.tree_finalize(*x, w.max_depth, out, ws, stream=stream)
-
-    topk = args.topk if linear else 0
-    # a small batch of aligned rows takes the one-launch path of the linear call
-    one_launch = linear and not topk and binding.verify_linear_launches(inputs[0], inputs[1]) == 1
-    if one_launch:
-        kernels = 1
-
-    def verify(x, on=stream):
-        if topk:
-            binding.verify_linear_topk(*x, topk, out=out, workspace=ws, stream=on)
-        elif linear:
-            binding.verify_linear(*x, out=out, workspace=ws, stream=on)
-        else:
-            binding.verify_tree(*x, w.max_depth, out=out, workspace=ws, stream=on)
-
-    def step(s):
-        verify(sets[s % n_sets])
-
-    def step_timed(s, ph):
-        x = sets[s % n_sets]
-        if ph is None:
-            verify(x)
-            return
-        e0, e1, e2 = ph
-        e0.record(stream)
-        if topk or one_launch:  # one call, timed as a whole
-            verify(x)
-            e1.record(stream)
-        else:
-            stats(x)
-            e1.record(stream)
-            finalize(x)
-        e2.record(stream)
-
-    for s in range(max(args.warmup, 3)):
-        step(s)
-    torch.cuda.synchronize()
-
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] if s % PHASE_EVERY == 0 else None
-          for s in range(K)]
-    t_begin = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    peak, peak_kind = measured_peaks()
+
     sampler = ClockSampler(dist.local_rank) if dist.rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    dist.barrier()
-    torch.cuda.synchronize()
-    if sampler:
-        sampler.mark("begin")
-    t_begin.record(stream)
-    for s in range(K):
-        step_timed(s, ev[s])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    if sampler:
-        sampler.mark("end")
-    dist.barrier()
+    total_ms = time_steps(torch, st, K, args.warmup, stream, dist, sampler)
     clocks = sampler.stop() if sampler else None
+    # outputs of the last timed step (its rejected requests set the q-row bytes)
+    torch.cuda.synchronize()
+    n_acc_sum = float(st.out.n_accepted.sum().item())
+    k1_ms, k2_ms = time_phases(torch, st, max(PHASE_STEPS, 1), stream)
 
-    total_ms = t_begin.elapsed_time(t_end)
-    k1_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev if e is not None]))
-    k2_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev if e is not None]))
     total_ms = dist.max(total_ms, device)
     ms_per_step = total_ms / K
-    value = dist.sum(units, device) * K / (total_ms / 1e3)
-
-    # rejected requests in the last step: their q row is part of the algorithmic bytes
-    # (the top-k approximation reads none of it)
-    nb = out.is_bonus.cpu().numpy()
-    rejected = 0.0 if topk else float((nb == 0).sum())
-    ab = algorithmic_bytes(w, rejected)
-    gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
-    peak, peak_kind = measured_peaks()
-
-    # roofline of the dominant kernel (row statistics)
-    spr = -(-w.V * es // 8192)
-    if topk:  # both launches of the call, timed together
-        kname, k_bytes = "row_stats_kernel + topk_draw_kernel", ab["total"]
-        traffic = None
-    elif one_launch:  # the whole step is one kernel
-        kname, k_bytes = "small_verify_kernel", ab["total"]
-        traffic = None
-    else:
-        kname, k_bytes = "row_stats_kernel", ab["logits"] + w.B * R * spr * 16
-        traffic = ncu_traffic(_workload_name(args), kname)
-    k_gbs = k_bytes / (k1_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(k_gbs, 1),
-                "peak": peak, "unit": "GB/s", "frac": round(k_gbs / peak, 4),
-                "peak_kind": peak_kind, "traffic": traffic,
-                "algorithmic_bytes_per_launch": int(k_bytes), "avg_launch_us": round(k1_ms * 1e3, 2)}
+    value = dist.sum(st.units, device) * K / (total_ms / 1e3)
+    line = workload_line(torch, binding, st, ms_per_step, k1_ms, k2_ms, peak,
+                         _workload_name(args))
+    roofline = dict(line["roofline"], peak_kind=peak_kind)
 
     # ---- the same steps replayed from CUDA graphs (launch-bound sizes) ----
     graph = None
-    if args.graph and not topk:
+    if args.graph and not st.topk:
         # a serving loop replays one graph on fixed buffers: up to 4 graphs here
         # (fewer than the eager rotation leaves the small inputs warm in L2)
-        n_graphs = min(n_sets, 4)
+        n_graphs = min(st.n_sets, 4)
         graphs = []
         for i in range(n_graphs):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                verify(sets[i], on=None)
+                st.verify(st.sets[i], None)
             graphs.append(g)
         for s_ in range(max(args.warmup, 3)):
             graphs[s_ % n_graphs].replay()
@@ -423,42 +475,39 @@ def run_ours(args, dist):
         torch.cuda.synchronize()
         g_ms = dist.max(g0.elapsed_time(g1), device)
         graph = {"ms_per_step": round(g_ms / K, 5),
-                 "value": round(dist.sum(units, device) * K / (g_ms / 1e3), 1),
-                 "unit": "positions/s", "graphs": n_graphs, "l2_warm": n_graphs < n_sets}
+                 "value": round(dist.sum(st.units, device) * K / (g_ms / 1e3), 1),
+                 "unit": "positions/s", "graphs": n_graphs, "l2_warm": n_graphs < st.n_sets}
+        del graphs
 
     # ---- the opt-in acceptance-rate pass, timed on its own ----
     alpha = None
     if args.alpha and linear:
-        # the statistics in the workspace are those of set 0; alpha reads only M and S
-        # of each row from them, so the passes over the other sets move the same bytes
-        x0 = sets[0]
-        binding.verify_linear(*x0, out=out, workspace=ws, stream=stream)
-        for s_ in range(3):
-            x = sets[s_ % n_sets]
-            binding.row_alpha(x[0], x[1], x[3], ws, stream=stream)
-        torch.cuda.synchronize()
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        n_a = max(1, min(K, 200))
-        a0.record(stream)
-        for s_ in range(n_a):
-            x = sets[s_ % n_sets]
-            binding.row_alpha(x[0], x[1], x[3], ws, stream=stream)
-        a1.record(stream)
-        torch.cuda.synchronize()
-        a_us = a0.elapsed_time(a1) / n_a * 1e3
-        a_bytes = 2 * w.B * gamma * w.V * es
-        alpha = {"kernel": "row_alpha_kernel", "avg_launch_us": round(a_us, 2),
-                 "bytes_per_launch": int(a_bytes), "achieved_gbs": round(a_bytes / a_us / 1e3, 1),
-                 "peak_gbs": peak, "frac": round(a_bytes / a_us / 1e3 / peak, 4), "launches": n_a}
+        alpha = time_alpha(torch, binding, st, K, stream, peak)
 
     # ---- e2e: pinned host buffers through the public verify call ----
-    e2e = run_e2e(args, w, linear, device, stream, dist, units)
+    e2e = run_e2e(args, w, linear, device, stream, dist, st.units)
+
+    # ---- the other workloads, each measured the same way in this process ----
+    others = None
+    if (not args.no_workloads and dist.world == 1 and args.batch is None
+            and args.vocab is None and not args.topk):
+        others = {}
+        del st
+        torch.cuda.empty_cache()
+        for name in sorted(W.WORKLOADS):
+            if name == args.workload:
+                continue
+            others[name] = measure_other(torch, binding, name, device, stream, dist, peak,
+                                         args.workload_steps)
+            torch.cuda.empty_cache()
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, linear, units, args.cpu_seconds)
+        cpu = cpu_baseline(w, linear, w.B * w.gamma if linear else w.B * (w.N - 1),
+                           args.cpu_seconds)
 
+    ab = line["ab"]
+    gbs = line["gbs"]
     res = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -472,23 +521,22 @@ def run_ours(args, dist):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic",
-        "config": _config(w, _workload_name(args), linear, l2_note, topk),
+        "config": _config(w, _workload_name(args), linear, l2_note, args.topk if linear else 0),
         "requests_per_s": round(dist.sum(w.B, device) * K / (total_ms / 1e3), 1),
-        "accepted_tokens_per_s": round(dist.sum(float(out.n_accepted.sum().item() + w.B), device)
-                                       * K / (total_ms / 1e3), 1),
+        "accepted_tokens_per_s": round(dist.sum(n_acc_sum + w.B, device) * K / (total_ms / 1e3), 1),
         "gbs": round(gbs, 1),
         "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
         "frac_of_measured_hbm": round(gbs / peak, 4),
         "algorithmic_bytes_per_step": int(ab["total"]),
-        "phase_us": ({"verify_topk": round(k1_ms * 1e3, 2)} if topk else
-                     {"verify_one_launch": round(k1_ms * 1e3, 2)} if one_launch else
-                     {"row_stats": round(k1_ms * 1e3, 2), "finalize": round(k2_ms * 1e3, 2)}),
+        "phase_us": dict(line["phase"], steps=PHASE_STEPS,
+                         how="median of separately issued steps after the timed region"),
         "roofline": roofline,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": kernels * K,
+        "gpu_launches": launches * K,
         "graph": graph,
         "alpha_pass": alpha,
+        "workloads": others,
         "clocks": clocks,
     }
     if dist.rank == 0:
@@ -496,8 +544,58 @@ def run_ours(args, dist):
     dist.close()
 
 
+def time_alpha(torch, binding, st, K, stream, peak):
+    """The opt-in acceptance-rate pass on the workspace of a verify call on set 0
+    (it reads only M and S of each row from it, so the passes over the other
+    sets move the same bytes)."""
+    w = st.w
+    x0 = st.sets[0]
+    binding.verify_linear(*x0, out=st.out, workspace=st.ws, stream=stream)
+    for s_ in range(3):
+        x = st.sets[s_ % st.n_sets]
+        binding.row_alpha(x[0], x[1], x[3], st.ws, stream=stream)
+    torch.cuda.synchronize()
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    n_a = max(1, min(K, 200))
+    a0.record(stream)
+    for s_ in range(n_a):
+        x = st.sets[s_ % st.n_sets]
+        binding.row_alpha(x[0], x[1], x[3], st.ws, stream=stream)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    a_us = a0.elapsed_time(a1) / n_a * 1e3
+    a_bytes = 2 * w.B * w.gamma * w.V * w.elem_bytes
+    return {"kernel": "row_alpha_kernel", "avg_launch_us": round(a_us, 2),
+            "bytes_per_launch": int(a_bytes), "achieved_gbs": round(a_bytes / a_us / 1e3, 1),
+            "peak_gbs": peak, "frac": round(a_bytes / a_us / 1e3 / peak, 4), "launches": n_a}
+
+
+def measure_other(torch, binding, name, device, stream, dist, peak, steps):
+    """One of the other named workloads, measured in the same process as the
+    headline: resident input sets used in turn (cold L2), `steps` timed verify
+    calls, then the separately issued phase steps for the kernel times."""
+    w = W.make_workload(name)
+    st = Setup(binding, w, device)
+    ms = time_steps(torch, st, steps, 10, stream, dist) / steps
+    k1_ms, k2_ms = time_phases(torch, st, PHASE_STEPS, stream)
+    line = workload_line(torch, binding, st, ms, k1_ms, k2_ms, peak, name)
+    res = {"B": w.B, "V": w.V, "dtype": w.dtype,
+           "gamma" if st.linear else "N": w.gamma if st.linear else w.N,
+           "steps": steps, "us_per_step": round(ms * 1e3, 2),
+           "positions_per_s": round(st.units / (ms / 1e3), 1),
+           "requests_per_s": round(w.B / (ms / 1e3), 1),
+           "gbs": round(line["gbs"], 1),
+           "frac_of_8tbs": round(line["gbs"] / NOMINAL_HBM_GBS, 4),
+           "frac_of_measured_hbm": round(line["gbs"] / peak, 4),
+           "algorithmic_bytes_per_step": int(line["ab"]["total"]),
+           "launches_per_step": st.launches,
+           "phase_us": line["phase"], "roofline": line["roofline"], "l2": st.l2_note}
+    del st
+    return res
+
+
 L2_BYTES = 129_000_000  # GB300 L2
-PHASE_EVERY = 32        # timed steps per step issued as two phases with events
 def input_rotation(set_bytes: int):
     """How many resident copies of a step's inputs to use in turn so that a
     step's inputs were last touched at least 3 x L2 bytes of other inputs ago."""

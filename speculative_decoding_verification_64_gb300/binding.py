@@ -152,8 +152,10 @@ def _stream_ptr(stream) -> ctypes.c_void_p:
 
 
 def _cuda(**tensors):
-    """Every given tensor (None skipped) must live on one CUDA device: the
-    library reads and writes device memory only, and has no CPU path."""
+    """Every given tensor (None skipped) must live on one CUDA device, the
+    current one: the library reads and writes device memory only (it has no
+    CPU path), launches on the current device, and the binding passes that
+    device's current stream."""
     dev = None
     for name, t in tensors.items():
         if t is None:
@@ -163,6 +165,11 @@ def _cuda(**tensors):
         if dev is not None and t.device != dev:
             raise ValueError(f"{name} is on {t.device}, the other arrays on {dev}")
         dev = t.device
+    if dev is not None:
+        cur = torch.cuda.current_device()
+        if (dev.index if dev.index is not None else cur) != cur:
+            raise ValueError(f"the arrays are on {dev}, but the current device is cuda:{cur}: "
+                             f"call under torch.cuda.device({dev.index})")
 
 
 def _req(t: torch.Tensor, name: str, dtype, shape, device):
@@ -368,6 +375,7 @@ def _staging(nbytes: int, staging, device) -> torch.Tensor:
         return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
     if staging.device.type != "cuda" or staging.dtype != torch.uint8:
         raise ValueError("staging must be a uint8 CUDA tensor")
+    _cuda(staging=staging)
     return staging
 
 

@@ -167,14 +167,24 @@ int specdec_row_stats(const void *logits, const void *q, int dtype, const int32_
                       static_cast<cudaStream_t>(stream), (flags & SPECDEC_STATS_ENTROPY) != 0);
 }
 
+}  // extern "C"
+
+// Size checks of every linear entry point (also the no-workspace one), in the
+// order that decides which code a bad call gets.
+int specdec::linear_size_status(int B, int gamma, int V, int dtype) {
+  if (gamma < 1) return SPECDEC_ERR_INVALID_ARG;
+  if (gamma > SPECDEC_MAX_GAMMA) return SPECDEC_ERR_UNSUPPORTED;
+  return check_sizes(B, gamma + 1, V, dtype);
+}
+
+extern "C" {
+
 static int linear_checks(const void *logits, const void *q, int dtype, const int32_t *tokens,
                          const float *temperature, const float *uniforms, int B, int gamma,
                          int V, int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
                          uint8_t *is_bonus, int32_t *row_status, const float *p_draft,
                          void *workspace, size_t workspace_bytes) {
-  if (gamma < 1) return SPECDEC_ERR_INVALID_ARG;
-  if (gamma > SPECDEC_MAX_GAMMA) return SPECDEC_ERR_UNSUPPORTED;
-  int st = check_sizes(B, gamma + 1, V, dtype);
+  const int st = linear_size_status(B, gamma, V, dtype);
   if (st != SPECDEC_OK) return st;
   if (B == 0) return SPECDEC_OK;
   if (!logits || !q || !tokens || !temperature || !uniforms || !n_accepted || !out_tokens ||

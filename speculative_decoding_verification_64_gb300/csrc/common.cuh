@@ -3,8 +3,10 @@
 // mbarriers, thread-block clusters with distributed shared memory.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "specdec.h"
 
@@ -155,8 +157,43 @@ struct PathLogprobParams {
   int dtype, B, R, V, spr, path_len;
 };
 
+// Per-device set-up done once per process: a device is marked only after the
+// set-up succeeded on it; first calls from several host threads serialise on
+// the mutex, later calls read one atomic flag.  Devices past the table redo
+// the set-up on every call.
+constexpr int kMaxCachedDevices = 64;
+struct DeviceOnce {
+  std::mutex mu;
+  std::atomic<bool> done[kMaxCachedDevices]{};
+};
+
+template <typename F>
+inline cudaError_t device_once(DeviceOnce &o, F &&setup) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxCachedDevices) return setup(dev);
+  if (o.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(o.mu);
+  if (o.done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  err = setup(dev);
+  if (err == cudaSuccess) o.done[dev].store(true, std::memory_order_release);
+  return err;
+}
+
+// The dynamic shared-memory opt-in of `kernel`, once per device.
+template <typename K>
+inline cudaError_t smem_opt_in_once(DeviceOnce &o, K kernel, int bytes) {
+  return device_once(o, [&](int) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  });
+}
+
 // Multiprocessor count of the current device (looked up once per device).
 int device_sm_count();
+// Status of the sizes of a linear verify call (gamma, B, V, dtype), as every
+// linear entry point reports them.
+int linear_size_status(int B, int gamma, int V, int dtype);
 cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream);
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream);
 cudaError_t launch_linear_topk(const LinearFinalizeParams &p, int topk, cudaStream_t stream);

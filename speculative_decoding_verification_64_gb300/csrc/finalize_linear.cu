@@ -593,17 +593,10 @@ bool bulk_draw_applies(const LinearFinalizeParams &p, int grid) {
 
 template <int DT, bool kEarly>
 cudaError_t launch_bulk(const LinearFinalizeParams &p, unsigned grid, cudaStream_t stream) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
+  static DeviceOnce once;
   const int smem = (int)sizeof(bulk::Smem);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    err = cudaFuncSetAttribute(bulk::draw_bulk_kernel<DT, kEarly>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
-  }
+  const cudaError_t err = smem_opt_in_once(once, bulk::draw_bulk_kernel<DT, kEarly>, smem);
+  if (err != cudaSuccess) return err;
   return launch_pdl(bulk::draw_bulk_kernel<DT, kEarly>, dim3(grid), dim3(bulk::kThreads),
                     (size_t)smem, stream, p);
 }

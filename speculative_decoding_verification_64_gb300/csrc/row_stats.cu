@@ -242,17 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
 
 template <int DT, bool kA>
 cudaError_t launch_dt(const RowStatsParams &p, cudaStream_t stream) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
+  static DeviceOnce once;
   const int smem = (int)sizeof(StatsSmem);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    err = cudaFuncSetAttribute(row_stats_kernel<DT, kA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               smem);
-    if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
-  }
+  const cudaError_t err = smem_opt_in_once(once, row_stats_kernel<DT, kA>, smem);
+  if (err != cudaSuccess) return err;
   const long long units = p.stages / p.spr * ((p.spr + kUnit - 1) / kUnit);
   long long grid = device_sm_count();
   if (grid > units) grid = units;
@@ -272,19 +265,19 @@ cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream) {
 }
 
 namespace {
-int g_sm_count[64];
+std::atomic<int> g_sm_count[kMaxCachedDevices]{};
 }  // namespace
 
 int device_sm_count() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (g_sm_count[dev] == 0) {
-    int n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  int n = (dev < kMaxCachedDevices) ? g_sm_count[dev].load(std::memory_order_relaxed) : 0;
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 148;
-    g_sm_count[dev] = n;
+    if (dev < kMaxCachedDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
   }
-  return g_sm_count[dev];
+  return n;
 }
 
 }  // namespace specdec

@@ -302,16 +302,9 @@ bool plan_for(int B, int gamma, int V, int dtype, const void *logits, const void
 
 template <int DT>
 cudaError_t launch_dt(const LinearFinalizeParams &p, const Plan &pl, cudaStream_t stream) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  static DeviceOnce once;
+  cudaError_t err = smem_opt_in_once(once, small_verify_kernel<DT>, kHeadBytes + kMaxDynSmem);
   if (err != cudaSuccess) return err;
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    err = cudaFuncSetAttribute(small_verify_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kHeadBytes + kMaxDynSmem);
-    if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
-  }
   const int es = (DT == SPECDEC_F32) ? 4 : 2;
   const int spr = stages_per_row(p.V, es);
   const int nst = (spr + pl.C - 1) / pl.C;

@@ -15,21 +15,23 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_scratch[SPECDEC_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices];
+specdec::DeviceOnce g_scratch_once;
+void *g_scratch_ptr[specdec::kMaxCachedDevices];  // written under g_scratch_once
 
-// Device address of the array on the current device, looked up once.
+// Device address of the array on the current device, looked up once (first
+// calls from several host threads serialise inside device_once).
 cudaError_t static_scratch(void **ptr) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (dev < 0 || dev >= specdec::kMaxCachedDevices) return cudaErrorInvalidDevice;
+  err = specdec::device_once(g_scratch_once, [](int d) {
     void *p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (err != cudaSuccess) return err;
-    g_scratch_ptr[dev] = p;
-  }
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e == cudaSuccess) g_scratch_ptr[d] = p;
+    return e;
+  });
+  if (err != cudaSuccess) return err;
   *ptr = g_scratch_ptr[dev];
   return cudaSuccess;
 }
@@ -43,10 +45,11 @@ extern "C" int specdec_verify_linear_static(const void *logits, const void *q, i
                                             int32_t *out_tokens, int32_t *final_token,
                                             uint8_t *is_bonus, int32_t *row_status,
                                             float *p_draft, void *stream) {
-  if (B == 0) return SPECDEC_OK;
+  // the size checks of specdec_verify_linear first, so that both entry points
+  // return the same code for the same sizes (B = 0 included)
+  const int st = specdec::linear_size_status(B, gamma, V, dtype);
+  if (st != SPECDEC_OK || B == 0) return st;
   const size_t need = specdec_workspace_size(B, gamma + 1, V, dtype);
-  if (need == 0) return (gamma > SPECDEC_MAX_GAMMA || V > SPECDEC_MAX_V)
-                            ? SPECDEC_ERR_UNSUPPORTED : SPECDEC_ERR_INVALID_ARG;
   if (need > (size_t)SPECDEC_STATIC_SCRATCH_BYTES) return SPECDEC_ERR_STATIC_LIMIT;
   void *scratch = nullptr;
   if (static_scratch(&scratch) != cudaSuccess) return SPECDEC_ERR_CUDA;

@@ -40,7 +40,9 @@ Per-request streams make a smaller batch a prefix of a larger one.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
 from typing import Dict, Optional
 
 import numpy as np
@@ -106,6 +108,21 @@ def philox_uniforms(seed: int, shape, offset_words: int = 0) -> np.ndarray:
     k = (raw >> np.uint64(41)).astype(np.float64)
     u = ((k + 0.5) * (2.0 ** -23)).astype(np.float32)
     return u.reshape(shape)
+
+
+def _per_request(B: int, fill) -> None:
+    """Run ``fill(b)`` for every request b on a pool of threads.  Each request
+    draws from its own generators and writes only its own slices, so the
+    result does not depend on the thread count or the order; numpy releases
+    the interpreter lock inside the bulk draws and array arithmetic."""
+    workers = max(1, min(B, os.cpu_count() or 1, 16))
+    if workers == 1:
+        for b in range(B):
+            fill(b)
+        return
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        for f in [ex.submit(fill, b) for b in range(B)]:
+            f.result()
 
 
 def _data_rng(seed: int, b: int) -> np.random.Generator:
@@ -259,7 +276,7 @@ def make_linear(law: str, B: int, gamma: int, V: int, dtype: str, seed: int,
         greedy = np.zeros(B, dtype=bool)
         greedy[sel.permutation(B)[:n_greedy]] = True
         temps[greedy] = 0.0
-    for b in range(B):
+    def fill(b):
         rng = _data_rng(seed, b)
         if law == "mixed_normal3":
             T = float(np.float32(temps[b]))
@@ -273,6 +290,8 @@ def make_linear(law: str, B: int, gamma: int, V: int, dtype: str, seed: int,
         stored_q = decode(q[b], dtype)
         toks[b] = _draw_from_rows(stored_q, _token_rng(seed, b))
         temp[b] = T
+
+    _per_request(B, fill)
     uni = philox_uniforms(seed, (B, R))
     return LinearWorkload(name or f"{law}_b{B}_g{gamma}_v{V}_{dtype}", dtype, B, gamma, V,
                           logits, q, toks, temp, uni)
@@ -325,7 +344,7 @@ def make_tree(B: int, N: int, V: int, dtype: str, seed: int, max_depth: int = 5,
     q = np.empty((B, N, V), dtype=np.float32 if dtype == F32 else np.uint16)
     toks = np.zeros((B, N), dtype=np.int32)
     parent = np.empty((B, N), dtype=np.int32)
-    for b in range(B):
+    def fill(b):
         rng = _data_rng(seed, b)
         trng = _token_rng(seed, b)
         parent[b] = random_tree_shape(N, max_depth, branching, trng)
@@ -337,6 +356,8 @@ def make_tree(B: int, N: int, V: int, dtype: str, seed: int, max_depth: int = 5,
         # node n's token is drawn from its parent's draft distribution
         draws = _draw_from_rows(stored_q[parent[b][1:]], trng)
         toks[b, 1:] = draws
+
+    _per_request(B, fill)
     temp = np.full((B,), temperature, dtype=np.float32)
     uni = philox_uniforms(seed, (B, N))
     return TreeWorkload(name or f"tree_b{B}_n{N}_v{V}_{dtype}", dtype, B, N, V, max_depth,

@@ -334,3 +334,46 @@ def test_binding_refuses_host_tensors_for_device_calls():
         binding.row_alpha(logits, q, temp, ws)
     with pytest.raises(ValueError, match="CUDA tensor"):
         binding.row_entropy(logits, temp, ws)
+
+
+def test_static_entry_point_checks_sizes_like_the_workspace_one(lib):
+    """specdec_verify_linear_static runs the size checks of specdec_verify_linear
+    first, so both entry points return the same code for the same sizes, B = 0
+    included (no device work: every case returns before any CUDA call)."""
+    from speculative_decoding_verification_64_gb300.binding import BF16
+    N = None
+    vl, vs = lib.specdec_verify_linear, lib.specdec_verify_linear_static
+    cases = [
+        (0, 8, 1000, BF16),          # B = 0: a no-op
+        (0, 0, 1000, BF16),          # B = 0, gamma = 0: still a bad gamma
+        (0, 33, 1000, BF16),         # gamma beyond the ABI's limit
+        (0, 4, 1000, 7),             # unknown dtype
+        (0, 4, (1 << 21) + 1, BF16),  # vocabulary beyond the limit
+        (-1, 4, 1000, BF16),
+        ((1 << 31) - 1, 8, 1000, BF16),  # B * (gamma + 1) past INT_MAX
+    ]
+    for B, g, V, dt in cases:
+        want = vl(N, N, dt, N, N, N, B, g, V, N, N, N, N, N, N, N, 0, N)
+        got = vs(N, N, dt, N, N, N, B, g, V, N, N, N, N, N, N, N)
+        assert got == want, (B, g, V, dt, got, want)
+    assert vs(N, N, BF16, N, N, N, 0, 0, 1000, N, N, N, N, N, N, N) == 1
+    assert vs(N, N, BF16, N, N, N, (1 << 31) - 1, 8, 1000, N, N, N, N, N, N, N) == 2
+
+
+def test_binding_refuses_tensors_off_the_current_device(monkeypatch):
+    """The library launches on the current device and the binding passes that
+    device's current stream: tensors on another device are refused before the
+    library is called.  Checked with stand-in tensors (no GPU here)."""
+    import torch
+    from speculative_decoding_verification_64_gb300 import binding
+
+    class Fake:
+        def __init__(self, index):
+            self.device = torch.device("cuda", index)
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    binding._cuda(a=Fake(0), b=Fake(0), c=None)
+    with pytest.raises(ValueError, match="current device"):
+        binding._cuda(a=Fake(1), b=Fake(1))
+    with pytest.raises(ValueError, match="the other arrays"):
+        binding._cuda(a=Fake(0), b=Fake(1))
