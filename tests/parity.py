@@ -7,17 +7,41 @@ Tolerances (written here, used by every parity test):
   a boundary draw: an accept test the oracle ran with |u - min(1, p/q)| < 1e-6,
   or a final draw whose U*Z lies within 1e-6*Z of a CDF boundary around the
   oracle's token.  A mismatch outside that band fails the test.  Mismatches
-  inside the band ("excused") are counted and at most 1e-4 * draws of them
-  (rounded down: none in a case of fewer than 10^4 draws) may occur in one
-  case.  (With V ~ 1e5 every CDF cell is only ~1e-5 wide, so a quarter of
-  all final draws lie inside the band; the allowance therefore limits the
-  draws that actually differ, not the in-band ones.)
+  inside the band ("excused") are counted.  The bound on them is a rate --
+  at most 1e-4 of all draws -- which one case of a few hundred draws cannot
+  estimate: a case fails when its count would be improbable (probability
+  < 1e-3) if mismatches occurred at exactly that rate (``allowed_excused``:
+  none in a case of a few draws, 1 in a case of tens to a few hundred, 2 in
+  one of about a thousand), and
+  ``test_gpu_boundary_rate.py`` checks the rate itself over tens of
+  thousands of draws.  (With V ~ 1e5 a final draw can land in a cell only
+  ~1e-8 of Z wide, and the float32 weights of the GPU path resolve CDF edges
+  to about that precision; so in-band mismatches are rare but possible.)
 * request status bitmasks: exact.
 """
+import math
+
 import numpy as np
 
 BOUNDARY = 1e-6
 P_TOL = {"f32": 2e-5, "bf16": 2e-3}
+MISMATCH_RATE = 1e-4   # excused mismatches allowed per draw
+
+
+def allowed_excused(draws: int, rate: float = MISMATCH_RATE, alpha: float = 1e-3) -> int:
+    """Largest count m of excused mismatches a case of `draws` draws may show:
+    the smallest m with P(X > m) < alpha for X ~ Binomial(draws, rate)."""
+    if draws <= 0:
+        return 0
+    tail, m = 1.0, 0
+    while True:
+        # P(X = m), by the log-gamma form of the binomial coefficient
+        lp = (math.lgamma(draws + 1) - math.lgamma(m + 1) - math.lgamma(draws - m + 1)
+              + m * math.log(rate) + (draws - m) * math.log1p(-rate))
+        tail -= math.exp(lp)
+        if tail < alpha or m >= draws:
+            return m
+        m += 1
 
 
 def linear_draws(o, gamma):
@@ -62,7 +86,7 @@ def compare_linear(w, g, o, max_boundary_frac=1e-4):
                           ratio=o["ratio"][b], u=u[b], margin=o["final_margin"][b],
                           gpu_out=g["out_tokens"][b], ora_out=o["out_tokens"][b])
     rep["draws"] = linear_draws(o, gamma)
-    assert rep["excused"] <= int(max_boundary_frac * rep["draws"]), rep
+    assert rep["excused"] <= allowed_excused(rep["draws"], max_boundary_frac), rep
     return rep
 
 
@@ -95,7 +119,7 @@ def compare_tree(w, g, o, max_boundary_frac=1e-4):
                                         "final_token", "is_bonus")},
                           tm=o["test_margin"][b], fm=o["final_margin"][b])
     rep["draws"] = int(o["n_accepted"].sum() + 2 * B)
-    assert rep["excused"] <= int(max_boundary_frac * rep["draws"]), rep
+    assert rep["excused"] <= allowed_excused(rep["draws"], max_boundary_frac), rep
     return rep
 
 
