@@ -141,7 +141,7 @@ def measured_peaks():
 
 
 KERNEL_SOURCES = {
-    "row_stats_kernel": ("row_stats.cu", "stats_stage.cuh", "common.cuh"),
+    "row_stats_kernel": ("row_stats.cu", "stats_role.cuh", "stats_stage.cuh", "common.cuh"),
 }
 
 
@@ -311,18 +311,57 @@ class Setup:
         self.stats, self.finalize = _phase_fns(binding, w, self.linear, self.out, self.ws)
         # launches of one verify call: 1 (one kernel) or 2 (stats pass, then the draw)
         if self.topk:
-            self.launches = 2
+            self.launches, self.path = 2, binding.PATH_TWO_LAUNCHES
         elif self.linear:
             self.launches = binding.verify_linear_launches(inputs[0], inputs[1])
+            self.path = binding.verify_linear_path(inputs[0], inputs[1])
         else:
-            self.launches = 2
+            self.launches, self.path = 2, binding.PATH_TWO_LAUNCHES
+        self.binding = binding
+
+    def marshal(self, stream):
+        """The C-ABI verify call of every input set with its arguments marshalled
+        once (as a C caller holds them), so that the timed steps measure the
+        library, not the Python binding's per-call checks."""
+        import ctypes
+        b, w, o, ws = self.binding, self.w, self.out, self.ws
+        lib = b.load_library()
+        P = b._ptr
+        sp = ctypes.c_void_p(stream.cuda_stream)
+        calls = []
+        for x in self.sets:
+            if self.topk:
+                fn = lib.specdec_verify_linear_topk
+                a = (P(x[0]), P(x[1]), self.dt, P(x[2]), P(x[3]), P(x[4]), w.B, w.gamma, w.V,
+                     self.topk, P(o.n_accepted), P(o.out_tokens), P(o.final_token),
+                     P(o.is_bonus), P(o.row_status), P(o.p_draft), P(ws), ws.numel(), sp)
+            elif self.linear:
+                fn = lib.specdec_verify_linear
+                a = (P(x[0]), P(x[1]), self.dt, P(x[2]), P(x[3]), P(x[4]), w.B, w.gamma, w.V,
+                     P(o.n_accepted), P(o.out_tokens), P(o.final_token), P(o.is_bonus),
+                     P(o.row_status), P(o.p_draft), P(ws), ws.numel(), sp)
+            else:
+                fn = lib.specdec_verify_tree
+                a = (P(x[0]), P(x[1]), self.dt, P(x[2]), P(x[3]), P(x[4]), P(x[5]), w.B, w.N,
+                     w.V, w.max_depth, P(o.n_accepted), P(o.path_nodes), P(o.out_tokens),
+                     P(o.final_token), P(o.is_bonus), P(o.row_status), P(o.p_node), P(ws),
+                     ws.numel(), sp)
+            calls.append((fn, a))
+        self.calls = calls
+
+    def call(self, s):
+        fn, a = self.calls[s % self.n_sets]
+        rc = fn(*a)
+        if rc != 0:
+            raise RuntimeError(f"{fn.__name__}: {self.binding.status_string(rc)}")
 
 
 def time_steps(torch, st, K, warmup, stream, dist, sampler=None):
     """K verify calls back to back between two events (after `warmup` calls);
-    every call is the public entry point, nothing else is issued in between."""
+    every call is the public C entry point, nothing else is issued in between."""
+    st.marshal(stream)
     for s in range(max(warmup, 3)):
-        st.verify(st.sets[s % st.n_sets], stream)
+        st.call(s)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -332,7 +371,7 @@ def time_steps(torch, st, K, warmup, stream, dist, sampler=None):
         sampler.mark("begin")
     t0.record(stream)
     for s in range(K):
-        st.verify(st.sets[s % st.n_sets], stream)
+        st.call(s)
     t1.record(stream)
     torch.cuda.synchronize()
     if sampler:
@@ -367,9 +406,7 @@ def time_phases(torch, st, n, stream):
 def kernel_names(st):
     if st.topk:
         return "row_stats_kernel + topk_draw_kernel"
-    if st.linear and st.launches == 1:
-        return "small_verify_kernel"
-    return "row_stats_kernel"
+    return st.binding.PATH_KERNELS[st.path]
 
 
 def workload_line(torch, binding, st, ms_per_step, k1_ms, k2_ms, peak, name):
@@ -383,6 +420,10 @@ def workload_line(torch, binding, st, ms_per_step, k1_ms, k2_ms, peak, name):
     es = w.elem_bytes
     spr = -(-w.V * es // 8192)
     kname = kernel_names(st)
+    if st.launches == 1 and not st.topk:
+        # the step is that one kernel: its time is the step's (events around
+        # single launches would add the launch gap of an idle GPU)
+        k1_ms = ms_per_step
     if st.topk or st.launches == 1:
         k_bytes, traffic = ab["total"], None
     else:

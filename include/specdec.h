@@ -135,14 +135,33 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * How many kernels specdec_verify_linear launches for these arguments: 1 when
- * a small batch takes the one-launch path, else 2 (the stats pass, then the
- * draw).  The one-launch path runs one cluster of C CTAs per request, C the
- * largest of 8, 4, 2 with B * C no more than the GPU's SMs; it needs rows
- * 16-byte aligned, logits and q 16-byte aligned, and each CTA's 1/C share of
- * the request's gamma + 1 target rows (plus the gamma q rows, or else of one
- * q row) fitting its shared memory.  Both paths give the same outputs and
- * leave the same workspace.  0 for B = 0, -1 for invalid sizes.  Host only.
+ * Which path specdec_verify_linear takes for these arguments (host only):
+ *   SPECDEC_PATH_SMALL_ONE_LAUNCH  a small batch: one cluster of C CTAs per
+ *       request (C the largest of 8, 4, 2 with B * C no more than the GPU's
+ *       SMs) holding its rows in shared memory; needs rows, logits and q
+ *       16-byte aligned and each CTA's 1/C share of the request's gamma + 1
+ *       target rows (plus the gamma q rows, or else of one q row) fitting its
+ *       shared memory;
+ *   SPECDEC_PATH_LARGE_ONE_LAUNCH  a large batch: one CTA per SM, most of
+ *       them streaming the target rows, the others drawing each request's
+ *       token as soon as its wave of requests has been reduced; needs rows,
+ *       logits and q 16-byte aligned, a final row of 64 KB to 512 KB, and a
+ *       batch of at least twice the drawing CTAs;
+ *   SPECDEC_PATH_TWO_LAUNCHES      the stats pass, then the draw.
+ * Every path gives the same outputs and leaves the same workspace.
+ * SPECDEC_PATH_NONE for B = 0, -1 for invalid sizes.
+ */
+#define SPECDEC_PATH_NONE 0
+#define SPECDEC_PATH_SMALL_ONE_LAUNCH 1
+#define SPECDEC_PATH_LARGE_ONE_LAUNCH 2
+#define SPECDEC_PATH_TWO_LAUNCHES 3
+int specdec_verify_linear_path(int B, int gamma, int V, int dtype, const void *logits,
+                               const void *q);
+
+/*
+ * How many kernels specdec_verify_linear launches for these arguments: 1 on
+ * either one-launch path, 2 on the two-launch path (see
+ * specdec_verify_linear_path).  0 for B = 0, -1 for invalid sizes.  Host only.
  */
 int specdec_verify_linear_launches(int B, int gamma, int V, int dtype, const void *logits,
                                    const void *q);

@@ -42,6 +42,8 @@ _EXPORTS = {
                              ctypes.c_void_p], ctypes.c_int),
     "specdec_verify_linear_launches": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "specdec_verify_linear_path": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "specdec_row_alpha": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                            ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
@@ -541,6 +543,20 @@ def verify_linear_launches(logits: torch.Tensor, q: torch.Tensor) -> int:
     B, R, V = logits.shape
     return int(load_library().specdec_verify_linear_launches(B, R - 1, V, dtype_code(logits),
                                                              _ptr(logits), _ptr(q)))
+
+
+PATH_NONE, PATH_SMALL_ONE_LAUNCH, PATH_LARGE_ONE_LAUNCH, PATH_TWO_LAUNCHES = 0, 1, 2, 3
+PATH_KERNELS = {PATH_SMALL_ONE_LAUNCH: "small_verify_kernel",
+                PATH_LARGE_ONE_LAUNCH: "verify_fused_kernel",
+                PATH_TWO_LAUNCHES: "row_stats_kernel"}
+
+
+def verify_linear_path(logits: torch.Tensor, q: torch.Tensor) -> int:
+    """The path ``verify_linear`` takes for these inputs (``PATH_*``): a small
+    batch in one launch, a large batch in one launch, or two launches."""
+    B, R, V = logits.shape
+    return int(load_library().specdec_verify_linear_path(B, R - 1, V, dtype_code(logits),
+                                                         _ptr(logits), _ptr(q)))
 
 
 def row_alpha(logits: torch.Tensor, q: torch.Tensor, temperature: torch.Tensor,

@@ -34,11 +34,12 @@ bool dtype_ok(int dtype) { return dtype == SPECDEC_F32 || dtype == SPECDEC_BF16;
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t gather, chunk, draw_cnt, total;
+  size_t gather, chunk, draw_cnt, sync, total;
 };
 
 // Stage partials first (the tree form uses only these), then the linear
-// form's gathered values, draw chunk totals and tickets.
+// form's gathered values, draw chunk totals, tickets and the one-launch
+// verify's cross-CTA record (a fixed size: the same for every call shape).
 WsLayout workspace_layout(long long B, int R, int V, int dtype) {
   const long long rows = B * (long long)R;
   WsLayout w;
@@ -47,7 +48,8 @@ WsLayout workspace_layout(long long B, int R, int V, int dtype) {
   w.chunk = w.gather + align256((size_t)rows * sizeof(float2));
   w.draw_cnt = w.chunk + align256((size_t)B * draw_total_slots(V, elem_bytes(dtype)) *
                                   sizeof(unsigned long long));
-  w.total = w.draw_cnt + align256((size_t)B * sizeof(unsigned int));
+  w.sync = w.draw_cnt + align256((size_t)B * sizeof(unsigned int));
+  w.total = w.sync + align256(sizeof(FusedSync));
   return w;
 }
 
@@ -58,6 +60,7 @@ LinearWs linear_ws(void *workspace, long long B, int R, int V, int dtype) {
   ws.gather = reinterpret_cast<float2 *>(base + w.gather);
   ws.chunk_tot = reinterpret_cast<unsigned long long *>(base + w.chunk);
   ws.draw_cnt = reinterpret_cast<unsigned int *>(base + w.draw_cnt);
+  ws.sync = reinterpret_cast<FusedSync *>(base + w.sync);
   return ws;
 }
 
@@ -99,9 +102,9 @@ bool arrays_misaligned(int dtype, const void *logits, const void *q,
   return false;
 }
 
-int launch_stats(const void *logits, const void *q, int dtype, const int32_t *tokens,
-                 const float *temperature, int B, int R, int V, void *workspace,
-                 cudaStream_t stream, bool entropy = false) {
+RowStatsParams stats_params(const void *logits, const void *q, int dtype, const int32_t *tokens,
+                           const float *temperature, int B, int R, int V, void *workspace,
+                           bool entropy) {
   const long long rows = (long long)B * R;
   const int spr = stages_per_row(V, elem_bytes(dtype));
   RowStatsParams p;
@@ -118,7 +121,14 @@ int launch_stats(const void *logits, const void *q, int dtype, const int32_t *to
   p.tokens = tokens;
   p.q = q;
   p.ws = linear_ws(workspace, B, R, V, dtype);
-  return cuda_status(launch_row_stats(p, stream));
+  return p;
+}
+
+int launch_stats(const void *logits, const void *q, int dtype, const int32_t *tokens,
+                 const float *temperature, int B, int R, int V, void *workspace,
+                 cudaStream_t stream, bool entropy = false) {
+  return cuda_status(launch_row_stats(
+      stats_params(logits, q, dtype, tokens, temperature, B, R, V, workspace, entropy), stream));
 }
 
 }  // namespace
@@ -274,6 +284,19 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
                       n_accepted, out_tokens, final_token, is_bonus, row_status, p_draft, workspace);
     return cuda_status(launch_small_verify(p, s));
   }
+  {
+    const LinearFinalizeParams p =
+        linear_params(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
+                      n_accepted, out_tokens, final_token, is_bonus, row_status, p_draft, workspace);
+    if (fused_verify_applies(p)) {
+      // a large batch: the draws overlap the stats pass in one launch, leaving
+      // the same workspace
+      return cuda_status(launch_fused_verify(
+          stats_params(logits, q, dtype, draft_tokens, temperature, B, gamma + 1, V, workspace,
+                       false),
+          p, s));
+    }
+  }
   st = launch_stats(logits, q, dtype, draft_tokens, temperature, B, gamma + 1, V, workspace, s);
   if (st != SPECDEC_OK) return st;
   return linear_finalize_launch(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma,
@@ -281,12 +304,28 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
                                 p_draft, workspace, s, /*after_stats=*/true);
 }
 
+int specdec_verify_linear_path(int B, int gamma, int V, int dtype, const void *logits,
+                               const void *q) {
+  if (B <= 0) return SPECDEC_PATH_NONE;
+  if (linear_size_status(B, gamma, V, dtype) != SPECDEC_OK) return -1;
+  if (small_verify_applies(B, gamma, V, dtype, logits, q)) return SPECDEC_PATH_SMALL_ONE_LAUNCH;
+  LinearFinalizeParams p = {};
+  p.logits = logits;
+  p.q = q;
+  p.dtype = dtype;
+  p.B = B;
+  p.gamma = gamma;
+  p.V = V;
+  p.spr = stages_per_row(V, elem_bytes(dtype));
+  if (fused_verify_applies(p)) return SPECDEC_PATH_LARGE_ONE_LAUNCH;
+  return SPECDEC_PATH_TWO_LAUNCHES;
+}
+
 int specdec_verify_linear_launches(int B, int gamma, int V, int dtype, const void *logits,
                                    const void *q) {
-  if (B <= 0) return 0;
-  if (check_sizes(B, gamma + 1, V, dtype) != SPECDEC_OK || gamma < 1 || gamma > SPECDEC_MAX_GAMMA)
-    return -1;
-  return small_verify_applies(B, gamma, V, dtype, logits, q) ? 1 : 2;
+  const int path = specdec_verify_linear_path(B, gamma, V, dtype, logits, q);
+  if (path <= 0) return path;
+  return path == SPECDEC_PATH_TWO_LAUNCHES ? 2 : 1;
 }
 
 static int tree_checks(const void *logits, const void *q, int dtype, const int32_t *tokens,

@@ -285,14 +285,33 @@ __device__ __forceinline__ void write_outputs_warp(const LinearFinalizeParams &p
   }
 }
 
+// Where a request's fixed-point stage totals live: in the workspace (written
+// by other CTAs of the running kernel: L2 loads), or in this CTA's shared
+// memory with a copy in the workspace.
+struct GlobalTotals {
+  unsigned long long *g;
+  static constexpr bool kRegCache = true;  // keep up to 64 totals in registers
+  __device__ __forceinline__ unsigned long long get(int s) const { return __ldcg(g + s); }
+  __device__ __forceinline__ void set(int s, unsigned long long v) const { g[s] = v; }
+};
+struct SharedTotals {
+  unsigned long long *sm, *g;
+  static constexpr bool kRegCache = false;
+  __device__ __forceinline__ unsigned long long get(int s) const { return sm[s]; }
+  __device__ __forceinline__ void set(int s, unsigned long long v) const {
+    sm[s] = v;
+    g[s] = v;
+  }
+};
+
 // The search of one request by one warp (see the header of this section).
-template <int DT>
+template <int DT, typename Tot>
 __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const Req &rq,
-                                            LinearDecision d, bool aborted, int lane) {
+                                            LinearDecision d, bool aborted, int lane,
+                                            const Tot &tot) {
   constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
   const int gamma = p.gamma, R = gamma + 1;
   const long long b = rq.b;
-  unsigned long long *tot = p.ws.chunk_tot + b * p.ntot;
   if (aborted) {
     // a bounded wait ran out in some CTA of this request: report, draw nothing
     for (int i = lane; i < R; i += 32) p.out_tokens[b * R + i] = -1;
@@ -307,14 +326,14 @@ __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const
   bool use_q = d.k < gamma;
   const float U = __ldg(p.uniforms + b * R + gamma);
   // rows of at most 64 stages keep their stage totals in registers (two per lane)
-  const bool cached = rq.nst <= 64;
+  const bool cached = Tot::kRegCache && rq.nst <= 64;
   unsigned long long c0 = 0, c1 = 0, Z = 0;
   if (cached) {
-    c0 = (lane < rq.nst) ? __ldcg(tot + lane) : 0ull;
-    c1 = (lane + 32 < rq.nst) ? __ldcg(tot + lane + 32) : 0ull;
+    c0 = (lane < rq.nst) ? tot.get(lane) : 0ull;
+    c1 = (lane + 32 < rq.nst) ? tot.get(lane + 32) : 0ull;
     Z = c0 + c1;
   } else {
-    for (int s = lane; s < rq.nst; s += 32) Z += __ldcg(tot + s);
+    for (int s = lane; s < rq.nst; s += 32) Z += tot.get(s);
   }
   Z = warp_sum_u64(Z);
   if (Z == 0 && use_q) {
@@ -328,13 +347,13 @@ __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const
 #pragma unroll
       for (int k = 0; k < kVec; ++k) acc += to_fixed40(vec_sum<DT>(lv[k], qv[k], d, false));
       acc = warp_sum_u64(acc);
-      if (lane == 0) tot[s] = acc;
+      if (lane == 0) tot.set(s, acc);
       Z += acc;
     }
     __syncwarp();
     if (cached) {
-      c0 = (lane < rq.nst) ? __ldcg(tot + lane) : 0ull;
-      c1 = (lane + 32 < rq.nst) ? __ldcg(tot + lane + 32) : 0ull;
+      c0 = (lane < rq.nst) ? tot.get(lane) : 0ull;
+      c1 = (lane + 32 < rq.nst) ? tot.get(lane + 32) : 0ull;
     }
   }
   const unsigned long long target = uniform_target(U, Z);
@@ -343,7 +362,7 @@ __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const
   int st = -1;
   for (int s0 = 0; s0 < rq.nst && st < 0; s0 += 32) {
     const unsigned long long v = cached ? (s0 == 0 ? c0 : c1)
-                                        : ((s0 + lane < rq.nst) ? __ldcg(tot + s0 + lane) : 0ull);
+                                        : ((s0 + lane < rq.nst) ? tot.get(s0 + lane) : 0ull);
     const unsigned long long incl = warp_incl_scan_u64(v, lane);
     const unsigned m = __ballot_sync(0xffffffffu, target < base + incl);
     if (m) {

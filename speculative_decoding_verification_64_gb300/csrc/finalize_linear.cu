@@ -519,9 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFina
       const bool use_q = d.k < gamma;
       // the slot's previous use released first (see the stats pass: a parity
       // wait tells only two phases apart, and copies land in any order)
-      const bool ok = !sm.abort_flag &&
-                      (use == 0 || mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1)) &&
-                      mbar_wait_bounded(&sm.full[slot], use & 1);
+      const bool ok = __all_sync(0xffffffffu,  // one outcome for the whole warp
+                                 !sm.abort_flag &&
+                                     (use == 0 || mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1)) &&
+                                     mbar_wait_bounded(&sm.full[slot], use & 1));
       if (!ok) sm.abort_flag = 1;
       uint4 lv[kVec], qv[kVec];
       const int sbytes = (ok && real) ? min(kStage, rowbytes - s * kStage) : 0;
@@ -566,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFina
     const LinearDecision d = sm.dec[warp];
     const Req rq = make_req<DT>(p, rb0 + warp, d.k);
     if (lane == 0) p.ws.draw_cnt[rq.b] = 0;  // phase 2 may run again on the same phase-1 result
-    search_warp<DT>(p, rq, d, sm.search[warp] == 2, lane);
+    search_warp<DT>(p, rq, d, sm.search[warp] == 2, lane, GlobalTotals{p.ws.chunk_tot + rq.b * p.ntot});
   }
 }
 

@@ -143,7 +143,9 @@ __global__ void __launch_bounds__(kT, 1)
   }
   if (rank == 0 && tid == 0) p.ws.draw_cnt[b] = 0u;
   // ---- stage statistics, as the stats pass computes them --------------------
-  const bool ok = mbar_wait_bounded(&h.full, 0);
+  // one outcome for the whole CTA (the threads could see the wait give up
+  // differently, and the stage reductions below are warp-synchronous)
+  const bool ok = __syncthreads_and(mbar_wait_bounded(&h.full, 0)) != 0;
   if (!ok) h.abort_flag = 1;  // the partials carry SPECDEC_ROW_INTERNAL: no draw follows
   const float T = __ldg(p.temperature + b);
   const float c = temperature_scale(T);
