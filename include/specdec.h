@@ -135,6 +135,25 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The normaliser of each request's final draw in the last verify call on
+ * `workspace` ("Chapter 15: Decoding acceleration", section 15.1.2 step 4:
+ * after a rejection the correction is drawn from max(0, p - q) / Z), a
+ * diagnostic for checking the draw against a reference:
+ *   mass[b] = Z = sum_v max(0, p_k(v) - q_k(v)) after a rejection at row k
+ *             (the linear form), or the sum of the bonus row's p (1 up to
+ *             rounding); in the tree form the mass of max(0, p - c q) at the
+ *             final node after its rejected siblings (the product of the
+ *             renormalisations), 1 up to rounding without one; in the top-k
+ *             mode the residual's mass on the k candidates; NaN for greedy
+ *             and malformed requests (nothing is drawn).
+ * The value comes from the draw's own fixed-point total over the row's merged
+ * sum, so it carries the draw's arithmetic.  B, rows_per_request, V, dtype as
+ * in that call; mass: device float32 [B].  Asynchronous on `stream`.
+ */
+int specdec_final_mass(const void *workspace, size_t workspace_bytes, int B,
+                       int rows_per_request, int V, int dtype, float *mass, void *stream);
+
+/*
  * Which path specdec_verify_linear takes for these arguments (host only):
  *   SPECDEC_PATH_SMALL_ONE_LAUNCH  a small batch: one cluster of C CTAs per
  *       request (C the largest of 8, 4, 2 with B * C no more than the GPU's
@@ -142,18 +161,12 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
  *       16-byte aligned and each CTA's 1/C share of the request's gamma + 1
  *       target rows (plus the gamma q rows, or else of one q row) fitting its
  *       shared memory;
- *   SPECDEC_PATH_LARGE_ONE_LAUNCH  a large batch: one CTA per SM, most of
- *       them streaming the target rows, the others drawing each request's
- *       token as soon as its wave of requests has been reduced; needs rows,
- *       logits and q 16-byte aligned, a final row of 64 KB to 512 KB, and a
- *       batch of at least twice the drawing CTAs;
  *   SPECDEC_PATH_TWO_LAUNCHES      the stats pass, then the draw.
  * Every path gives the same outputs and leaves the same workspace.
  * SPECDEC_PATH_NONE for B = 0, -1 for invalid sizes.
  */
 #define SPECDEC_PATH_NONE 0
 #define SPECDEC_PATH_SMALL_ONE_LAUNCH 1
-#define SPECDEC_PATH_LARGE_ONE_LAUNCH 2
 #define SPECDEC_PATH_TWO_LAUNCHES 3
 int specdec_verify_linear_path(int B, int gamma, int V, int dtype, const void *logits,
                                const void *q);

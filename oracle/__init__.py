@@ -58,17 +58,17 @@ def _load():
         p = ctypes.c_void_p
         i = ctypes.c_int
         lib.specdec_oracle_verify_linear.argtypes = [p, p, i, p, p, p, i, i, i,
-                                                     p, p, p, p, p, p, p, p, p]
+                                                     p, p, p, p, p, p, p, p, p, p]
         lib.specdec_oracle_verify_linear.restype = i
         lib.specdec_oracle_verify_tree.argtypes = [p, p, i, p, p, p, p, i, i, i, i,
-                                                   p, p, p, p, p, p, p, p, p]
+                                                   p, p, p, p, p, p, p, p, p, p]
         lib.specdec_oracle_verify_tree.restype = i
         lib.specdec_oracle_num_threads.argtypes = []
         lib.specdec_oracle_num_threads.restype = i
         lib.specdec_oracle_set_threads.argtypes = [i]
         lib.specdec_oracle_set_threads.restype = None
         lib.specdec_oracle_verify_linear_topk.argtypes = [p, p, i, p, p, p, i, i, i, i,
-                                                          p, p, p, p, p, p, p, p, p]
+                                                          p, p, p, p, p, p, p, p, p, p]
         lib.specdec_oracle_verify_linear_topk.restype = i
         lib.specdec_oracle_row_entropy.argtypes = [p, i, p, i, i, i, p]
         lib.specdec_oracle_row_entropy.restype = None
@@ -187,7 +187,8 @@ def verify_linear(logits, q, dtype, draft_tokens, temperature, uniforms,
 
     Returns numpy arrays: n_accepted, out_tokens, final_token, is_bonus,
     row_status and, with ``diagnostics``, p_draft, ratio, final_margin,
-    row_diag ([B, gamma, 2]: sum min(p,q), sum max(0, p-q)).
+    row_diag ([B, gamma, 2]: sum min(p,q), sum max(0, p-q)) and final_mass
+    (the total Z of the final draw's weights).
     """
     lib = _load()
     logits = _storage(logits, dtype)
@@ -205,13 +206,14 @@ def verify_linear(logits, q, dtype, draft_tokens, temperature, uniforms,
         row_status=np.empty(B, np.int32))
     if diagnostics:
         out.update(p_draft=np.empty((B, gamma)), ratio=np.empty((B, gamma)),
-                   final_margin=np.empty(B), row_diag=np.empty((B, gamma, 2)))
+                   final_margin=np.empty(B), row_diag=np.empty((B, gamma, 2)),
+                   final_mass=np.empty(B))
     rc = lib.specdec_oracle_verify_linear(
         _ptr(logits), _ptr(q), _dtype_code(dtype), _ptr(toks), _ptr(temp), _ptr(uni),
         B, gamma, V, _ptr(out["n_accepted"]), _ptr(out["out_tokens"]),
         _ptr(out["final_token"]), _ptr(out["is_bonus"]), _ptr(out["row_status"]),
         _ptr(out.get("p_draft")), _ptr(out.get("ratio")), _ptr(out.get("final_margin")),
-        _ptr(out.get("row_diag")))
+        _ptr(out.get("row_diag")), _ptr(out.get("final_mass")))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return out
@@ -219,9 +221,9 @@ def verify_linear(logits, q, dtype, draft_tokens, temperature, uniforms,
 
 def verify_linear_topk(logits, q, dtype, draft_tokens, temperature, uniforms, topk: int) -> dict:
     """The linear step with the top-k residual (see specdec_oracle.c): the same
-    outputs as ``verify_linear`` plus p_draft, ratio, final_margin and tv [B] (total
+    outputs as ``verify_linear`` plus p_draft, ratio, final_margin, tv [B] (total
     variation between the exact residual law and the top-k one; NaN where no
-    residual draw happened)."""
+    residual draw happened) and final_mass (the total of the drawn weights)."""
     lib = _load()
     logits = _storage(logits, dtype)
     q = _storage(q, dtype)
@@ -234,12 +236,14 @@ def verify_linear_topk(logits, q, dtype, draft_tokens, temperature, uniforms, to
         n_accepted=np.empty(B, np.int32), out_tokens=np.empty((B, R), np.int32),
         final_token=np.empty(B, np.int32), is_bonus=np.empty(B, np.uint8),
         row_status=np.empty(B, np.int32), p_draft=np.empty((B, gamma)),
-        ratio=np.empty((B, gamma)), final_margin=np.empty(B), tv=np.empty(B))
+        ratio=np.empty((B, gamma)), final_margin=np.empty(B), tv=np.empty(B),
+        final_mass=np.empty(B))
     rc = lib.specdec_oracle_verify_linear_topk(
         _ptr(logits), _ptr(q), _dtype_code(dtype), _ptr(toks), _ptr(temp), _ptr(uni),
         B, gamma, V, int(topk), _ptr(out["n_accepted"]), _ptr(out["out_tokens"]),
         _ptr(out["final_token"]), _ptr(out["is_bonus"]), _ptr(out["row_status"]),
-        _ptr(out["p_draft"]), _ptr(out["ratio"]), _ptr(out["final_margin"]), _ptr(out["tv"]))
+        _ptr(out["p_draft"]), _ptr(out["ratio"]), _ptr(out["final_margin"]), _ptr(out["tv"]),
+        _ptr(out["final_mass"]))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return out
@@ -271,13 +275,13 @@ def verify_tree(logits, q, dtype, node_tokens, parent, temperature, uniforms,
         is_bonus=np.empty(B, np.uint8), row_status=np.empty(B, np.int32))
     if diagnostics:
         out.update(p_node=np.empty((B, N)), test_margin=np.empty(B),
-                   final_margin=np.empty(B))
+                   final_margin=np.empty(B), final_mass=np.empty(B))
     rc = lib.specdec_oracle_verify_tree(
         _ptr(logits), _ptr(q), _dtype_code(dtype), _ptr(toks), _ptr(par), _ptr(temp),
         _ptr(uni), B, N, V, max_depth, _ptr(out["n_accepted"]), _ptr(out["path_nodes"]),
         _ptr(out["out_tokens"]), _ptr(out["final_token"]), _ptr(out["is_bonus"]),
         _ptr(out["row_status"]), _ptr(out.get("p_node")), _ptr(out.get("test_margin")),
-        _ptr(out.get("final_margin")))
+        _ptr(out.get("final_margin")), _ptr(out.get("final_mass")))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return out

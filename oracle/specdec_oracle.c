@@ -124,10 +124,12 @@ static void target_probs(const void *logits, int dtype, size_t off, int V, doubl
 }
 
 /* Inverse-CDF draw: smallest v with C_v > U * Z.  Reports the distance of
- * U * Z to the two CDF boundaries around the chosen v, relative to Z. */
-static int cdf_draw(const double *w, int V, double U, double *margin) {
+ * U * Z to the two CDF boundaries around the chosen v, relative to Z, and Z
+ * itself (the weights' total). */
+static int cdf_draw(const double *w, int V, double U, double *margin, double *total) {
   double Z = 0.0;
   for (int v = 0; v < V; ++v) Z += w[v];
+  *total = Z;
   double t = U * Z;
   double C = 0.0, prev = 0.0;
   for (int v = 0; v < V; ++v) {
@@ -165,7 +167,10 @@ static int cdf_draw(const double *w, int V, double U, double *margin) {
  *   p_draft [B, gamma]    target probability of each drafted token;
  *   ratio   [B, gamma]    min(1, p/q) of each drafted token;
  *   final_margin [B]      distance of U*Z to the nearest CDF boundary / Z;
- *   row_diag [B, gamma, 2] per drafted row: sum_x min(p,q), sum_x max(0,p-q).
+ *   row_diag [B, gamma, 2] per drafted row: sum_x min(p,q), sum_x max(0,p-q);
+ *   final_mass [B]        Z, the total of the final draw's weights: the mass of
+ *                         max(0, p_k - q_k) after a rejection at k, of p_gamma
+ *                         for the bonus draw (NaN for a malformed request).
  * Returns 0, or -1 on a bad argument. */
 /* Candidate set of the top-k residual (the chapter's implementation note:
  * precompute the residual probabilities of the top-k candidates instead of
@@ -198,7 +203,7 @@ static int verify_linear_impl(const void *logits, const void *q, int dtype,
                               int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
                               uint8_t *is_bonus, int32_t *row_status, double *p_draft,
                               double *ratio, double *final_margin, double *row_diag,
-                              double *tv);
+                              double *tv, double *final_mass);
 
 int specdec_oracle_verify_linear(const void *logits, const void *q, int dtype,
                                  const int32_t *draft_tokens, const float *temperature,
@@ -206,10 +211,10 @@ int specdec_oracle_verify_linear(const void *logits, const void *q, int dtype,
                                  int32_t *n_accepted, int32_t *out_tokens,
                                  int32_t *final_token, uint8_t *is_bonus,
                                  int32_t *row_status, double *p_draft, double *ratio,
-                                 double *final_margin, double *row_diag) {
+                                 double *final_margin, double *row_diag, double *final_mass) {
   return verify_linear_impl(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
                             0, n_accepted, out_tokens, final_token, is_bonus, row_status,
-                            p_draft, ratio, final_margin, row_diag, NULL);
+                            p_draft, ratio, final_margin, row_diag, NULL, final_mass);
 }
 
 /* The linear step with the top-k residual (an approximation: the law of the
@@ -226,11 +231,11 @@ int specdec_oracle_verify_linear_topk(const void *logits, const void *q, int dty
                                       int32_t *n_accepted, int32_t *out_tokens,
                                       int32_t *final_token, uint8_t *is_bonus,
                                       int32_t *row_status, double *p_draft, double *ratio,
-                                      double *final_margin, double *tv) {
+                                      double *final_margin, double *tv, double *final_mass) {
   if (topk < 1) return -1;
   return verify_linear_impl(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
                             topk, n_accepted, out_tokens, final_token, is_bonus, row_status,
-                            p_draft, ratio, final_margin, NULL, tv);
+                            p_draft, ratio, final_margin, NULL, tv, final_mass);
 }
 
 static int verify_linear_impl(const void *logits, const void *q, int dtype,
@@ -239,7 +244,7 @@ static int verify_linear_impl(const void *logits, const void *q, int dtype,
                               int32_t *n_accepted, int32_t *out_tokens, int32_t *final_token,
                               uint8_t *is_bonus, int32_t *row_status, double *p_draft,
                               double *ratio, double *final_margin, double *row_diag,
-                              double *tv) {
+                              double *tv, double *final_mass) {
   if (B < 0 || gamma < 1 || V < 1 || (dtype != OR_DT_F32 && dtype != OR_DT_BF16)) return -1;
   const int R = gamma + 1;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -272,6 +277,7 @@ static int verify_linear_impl(const void *logits, const void *q, int dtype,
       if (ratio) for (int i = 0; i < gamma; ++i) ratio[(size_t)b * gamma + i] = NAN;
       if (final_margin) final_margin[b] = NAN;
       if (tv) tv[b] = NAN;
+      if (final_mass) final_mass[b] = NAN;
       continue;
     }
 
@@ -343,8 +349,8 @@ static int verify_linear_impl(const void *logits, const void *q, int dtype,
     } else {
       for (int v = 0; v < V; ++v) w[v] = Pk[v];
     }
-    double margin = 0.0;
-    int fin = cdf_draw(w, V, (double)u[gamma], &margin);
+    double margin = 0.0, mass = 0.0;
+    int fin = cdf_draw(w, V, (double)u[gamma], &margin, &mass);
 
     n_accepted[b] = k;
     for (int j = 0; j < R; ++j) {
@@ -356,6 +362,7 @@ static int verify_linear_impl(const void *logits, const void *q, int dtype,
     final_token[b] = fin;
     is_bonus[b] = (uint8_t)(k == gamma);
     if (final_margin) final_margin[b] = margin;
+    if (final_mass) final_mass[b] = mass;
     free(P);
     free(w);
   }
@@ -379,7 +386,10 @@ static int verify_linear_impl(const void *logits, const void *q, int dtype,
  * Diagnostics (NULL to skip): p_node [B, N] = target probability of node n's
  *   token under its parent's row (before any renormalisation; NaN for n = 0);
  *   test_margin [B] = min |u - r| over the sibling tests that ran (+inf if
- *   none); final_margin [B] as in the linear form. */
+ *   none); final_margin [B] as in the linear form; final_mass [B] = the mass
+ *   of the final node's residual relative to its target row: the product of
+ *   the normalisers of its rejected siblings' renormalisations (1 when none)
+ *   times the total of the drawn weights (NaN for a malformed request). */
 int specdec_oracle_verify_tree(const void *logits, const void *q, int dtype,
                                const int32_t *node_tokens, const int32_t *parent,
                                const float *temperature, const float *uniforms, int B,
@@ -387,7 +397,7 @@ int specdec_oracle_verify_tree(const void *logits, const void *q, int dtype,
                                int32_t *path_nodes, int32_t *out_tokens,
                                int32_t *final_token, uint8_t *is_bonus,
                                int32_t *row_status, double *p_node, double *test_margin,
-                               double *final_margin) {
+                               double *final_margin, double *final_mass) {
   if (B < 0 || N < 1 || V < 1 || max_depth < 0 ||
       (dtype != OR_DT_F32 && dtype != OR_DT_BF16))
     return -1;
@@ -437,6 +447,7 @@ int specdec_oracle_verify_tree(const void *logits, const void *q, int dtype,
       if (p_node) for (int n = 0; n < N; ++n) p_node[(size_t)b * N + n] = NAN;
       if (test_margin) test_margin[b] = NAN;
       if (final_margin) final_margin[b] = NAN;
+      if (final_mass) final_mass[b] = NAN;
       continue;
     }
 
@@ -456,6 +467,7 @@ int specdec_oracle_verify_tree(const void *logits, const void *q, int dtype,
     int *path = (int *)malloc(sizeof(int) * (size_t)D1);
     path[0] = 0;
     double tmin = INFINITY;
+    double node_mass = 1.0; /* product of the renormalisations at the current node */
     target_probs(logits, dtype, base, V, (double)Tf, P);
     for (;;) {
       int has_child = 0, accepted = -1;
@@ -479,21 +491,24 @@ int specdec_oracle_verify_tree(const void *logits, const void *q, int dtype,
           w[v] = x > 0.0 ? x : 0.0;
           Z += w[v];
         }
-        if (Z > 0.0)
+        if (Z > 0.0) {
           for (int v = 0; v < V; ++v) P[v] = w[v] / Z;
+          node_mass *= Z;
+        }
       }
       if (accepted >= 0) {
         cur = accepted;
         ++nacc;
         path[nacc] = cur;
         target_probs(logits, dtype, base + (size_t)cur * V, V, (double)Tf, P);
+        node_mass = 1.0;
         continue;
       }
       bonus = !has_child;
       break;
     }
-    double margin = 0.0;
-    int fin = cdf_draw(P, V, (double)u[0], &margin);
+    double margin = 0.0, total = 0.0;
+    int fin = cdf_draw(P, V, (double)u[0], &margin, &total);
 
     n_accepted[b] = nacc;
     for (int j = 0; j < D1; ++j) {
@@ -507,6 +522,7 @@ int specdec_oracle_verify_tree(const void *logits, const void *q, int dtype,
     is_bonus[b] = (uint8_t)bonus;
     if (test_margin) test_margin[b] = tmin;
     if (final_margin) final_margin[b] = margin;
+    if (final_mass) final_mass[b] = node_mass * total;
     free(P);
     free(w);
     free(path);

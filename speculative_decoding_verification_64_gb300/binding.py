@@ -44,6 +44,9 @@ _EXPORTS = {
                                         ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "specdec_verify_linear_path": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "specdec_final_mass": ([ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                            ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p],
+                           ctypes.c_int),
     "specdec_row_alpha": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                            ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
@@ -545,15 +548,26 @@ def verify_linear_launches(logits: torch.Tensor, q: torch.Tensor) -> int:
                                                              _ptr(logits), _ptr(q)))
 
 
-PATH_NONE, PATH_SMALL_ONE_LAUNCH, PATH_LARGE_ONE_LAUNCH, PATH_TWO_LAUNCHES = 0, 1, 2, 3
-PATH_KERNELS = {PATH_SMALL_ONE_LAUNCH: "small_verify_kernel",
-                PATH_LARGE_ONE_LAUNCH: "verify_fused_kernel",
-                PATH_TWO_LAUNCHES: "row_stats_kernel"}
+def final_mass(workspace: torch.Tensor, B: int, rows_per_request: int, V: int, dtype: int,
+               stream=None) -> torch.Tensor:
+    """Normaliser [B] of each request's final draw in the last verify call on
+    ``workspace`` (``specdec_final_mass``; NaN where nothing was drawn)."""
+    _cuda(workspace=workspace)
+    out = torch.empty(B, dtype=torch.float32, device=workspace.device)
+    rc = load_library().specdec_final_mass(_ptr(workspace), workspace.numel(), B,
+                                           rows_per_request, V, dtype,
+                                           _ptr(out) if B > 0 else None, _stream_ptr(stream))
+    _check(rc, "specdec_final_mass")
+    return out
+
+
+PATH_NONE, PATH_SMALL_ONE_LAUNCH, PATH_TWO_LAUNCHES = 0, 1, 3
+PATH_KERNELS = {PATH_SMALL_ONE_LAUNCH: "small_verify_kernel", PATH_TWO_LAUNCHES: "row_stats_kernel"}
 
 
 def verify_linear_path(logits: torch.Tensor, q: torch.Tensor) -> int:
     """The path ``verify_linear`` takes for these inputs (``PATH_*``): a small
-    batch in one launch, a large batch in one launch, or two launches."""
+    batch in one launch, or two launches."""
     B, R, V = logits.shape
     return int(load_library().specdec_verify_linear_path(B, R - 1, V, dtype_code(logits),
                                                          _ptr(logits), _ptr(q)))

@@ -2,6 +2,7 @@
 // Every entry point is asynchronous on the caller's stream and allocates
 // nothing; see include/specdec.h for the contract of each call.
 #include <climits>
+#include <cstdlib>
 #include <cstring>
 #include <initializer_list>
 
@@ -34,12 +35,12 @@ bool dtype_ok(int dtype) { return dtype == SPECDEC_F32 || dtype == SPECDEC_BF16;
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t gather, chunk, draw_cnt, sync, total;
+  size_t gather, chunk, draw_cnt, mass, total;
 };
 
-// Stage partials first (the tree form uses only these), then the linear
-// form's gathered values, draw chunk totals, tickets and the one-launch
-// verify's cross-CTA record (a fixed size: the same for every call shape).
+// Stage partials first, then the linear form's gathered values, draw chunk
+// totals and tickets, then the normaliser of every request's final draw
+// (both forms).
 WsLayout workspace_layout(long long B, int R, int V, int dtype) {
   const long long rows = B * (long long)R;
   WsLayout w;
@@ -48,8 +49,8 @@ WsLayout workspace_layout(long long B, int R, int V, int dtype) {
   w.chunk = w.gather + align256((size_t)rows * sizeof(float2));
   w.draw_cnt = w.chunk + align256((size_t)B * draw_total_slots(V, elem_bytes(dtype)) *
                                   sizeof(unsigned long long));
-  w.sync = w.draw_cnt + align256((size_t)B * sizeof(unsigned int));
-  w.total = w.sync + align256(sizeof(FusedSync));
+  w.mass = w.draw_cnt + align256((size_t)B * sizeof(unsigned int));
+  w.total = w.mass + align256((size_t)B * sizeof(float));
   return w;
 }
 
@@ -60,7 +61,7 @@ LinearWs linear_ws(void *workspace, long long B, int R, int V, int dtype) {
   ws.gather = reinterpret_cast<float2 *>(base + w.gather);
   ws.chunk_tot = reinterpret_cast<unsigned long long *>(base + w.chunk);
   ws.draw_cnt = reinterpret_cast<unsigned int *>(base + w.draw_cnt);
-  ws.sync = reinterpret_cast<FusedSync *>(base + w.sync);
+  ws.mass = reinterpret_cast<float *>(base + w.mass);
   return ws;
 }
 
@@ -284,19 +285,6 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
                       n_accepted, out_tokens, final_token, is_bonus, row_status, p_draft, workspace);
     return cuda_status(launch_small_verify(p, s));
   }
-  {
-    const LinearFinalizeParams p =
-        linear_params(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
-                      n_accepted, out_tokens, final_token, is_bonus, row_status, p_draft, workspace);
-    if (fused_verify_applies(p)) {
-      // a large batch: the draws overlap the stats pass in one launch, leaving
-      // the same workspace
-      return cuda_status(launch_fused_verify(
-          stats_params(logits, q, dtype, draft_tokens, temperature, B, gamma + 1, V, workspace,
-                       false),
-          p, s));
-    }
-  }
   st = launch_stats(logits, q, dtype, draft_tokens, temperature, B, gamma + 1, V, workspace, s);
   if (st != SPECDEC_OK) return st;
   return linear_finalize_launch(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma,
@@ -309,15 +297,6 @@ int specdec_verify_linear_path(int B, int gamma, int V, int dtype, const void *l
   if (B <= 0) return SPECDEC_PATH_NONE;
   if (linear_size_status(B, gamma, V, dtype) != SPECDEC_OK) return -1;
   if (small_verify_applies(B, gamma, V, dtype, logits, q)) return SPECDEC_PATH_SMALL_ONE_LAUNCH;
-  LinearFinalizeParams p = {};
-  p.logits = logits;
-  p.q = q;
-  p.dtype = dtype;
-  p.B = B;
-  p.gamma = gamma;
-  p.V = V;
-  p.spr = stages_per_row(V, elem_bytes(dtype));
-  if (fused_verify_applies(p)) return SPECDEC_PATH_LARGE_ONE_LAUNCH;
   return SPECDEC_PATH_TWO_LAUNCHES;
 }
 
@@ -372,6 +351,7 @@ static int tree_finalize_launch(const void *logits, const void *q, int dtype,
   p.is_bonus = is_bonus;
   p.row_status = row_status;
   p.p_node = p_node;
+  p.mass = linear_ws(workspace, B, N, V, dtype).mass;
   p.dtype = dtype;
   p.B = B;
   p.N = N;
@@ -416,6 +396,19 @@ int specdec_verify_tree(const void *logits, const void *q, int dtype, const int3
                               is_bonus, row_status, p_node, workspace, s);
 }
 
+
+int specdec_final_mass(const void *workspace, size_t workspace_bytes, int B,
+                       int rows_per_request, int V, int dtype, float *mass, void *stream) {
+  int st = check_sizes(B, rows_per_request, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  if (B == 0) return SPECDEC_OK;
+  if (!mass || misaligned(mass, 4)) return SPECDEC_ERR_INVALID_ARG;
+  st = check_workspace(workspace, workspace_bytes, B, rows_per_request, V, dtype);
+  if (st != SPECDEC_OK) return st;
+  const LinearWs ws = linear_ws(const_cast<void *>(workspace), B, rows_per_request, V, dtype);
+  return cuda_status(cudaMemcpyAsync(mass, ws.mass, (size_t)B * sizeof(float),
+                                     cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)));
+}
 
 int specdec_philox_uniforms(const uint64_t *key, const uint64_t *counter,
                             unsigned long long first_word, long long n, float *out,

@@ -73,32 +73,23 @@ struct LinearDecision {
   int32_t pad;
 };
 
-// Cross-CTA record of the one-launch linear verify for large batches
-// (verify_fused.cu), at the end of every linear workspace: the CTAs that
-// stream the logits publish each finished wave of requests in `flags`, tagged
-// with the launch's epoch, and the drawing CTAs wait for them.  The epoch is
-// `epoch` + 1, read by every CTA when it starts; the last CTA to exit (counted
-// in `exits`, tagged the same way) stores it back.  So no word needs to start
-// at any particular value: a stale or arbitrary flag differs from the current
-// epoch.
-#define SPECDEC_FUSED_MAX_WAVES 64
-#define SPECDEC_FUSED_MAX_STATS_CTAS 256
-struct FusedSync {
-  unsigned int epoch;
-  unsigned int pad;
-  unsigned long long exits;  // (epoch << 32) | CTAs of that launch that have exited
-  unsigned int pad2[60];
-  unsigned int flags[SPECDEC_FUSED_MAX_WAVES * SPECDEC_FUSED_MAX_STATS_CTAS];  // [wave][stats CTA]
-};
-
 // Linear-form workspace records shared by the two phases (device pointers
 // into the caller's workspace).
 struct LinearWs {
   float2 *gather;                // [B*R] (l_i(x~_i), q_i(x~_i)) of row i < gamma
   unsigned long long *chunk_tot; // [B, draw_total_slots] fixed-point chunk / stage sums of the draw
   unsigned int *draw_cnt;        // [B] chunks done (ticket of the draw); the stats pass zeroes it
-  FusedSync *sync;               // the one-launch verify's cross-CTA record
+  float *mass;                   // [B] normaliser of each request's final draw (below)
 };
+
+// The normaliser of a request's final draw, in target-probability units, as
+// specdec_final_mass reports it: the draw's fixed-point weight total (units
+// of the row maximum: weights 2^((l - M) c) or their residual) over the
+// row's merged sum S.  NaN when nothing was drawn.
+__device__ __forceinline__ float draw_mass(unsigned long long Z, float S) {
+  return __ull2float_rn(Z) * 0x1p-40f / S;
+}
+constexpr float kNoMass = __builtin_nanf("");
 
 struct RowStatsParams {
   const void *logits;
@@ -150,6 +141,7 @@ struct TreeFinalizeParams {
   uint8_t *is_bonus;
   int32_t *row_status;
   float *p_node;
+  float *mass;  // [B] normaliser of the final draw (workspace), as in LinearWs
   int dtype, B, N, V, spr, max_depth;
 };
 
@@ -216,11 +208,7 @@ int linear_size_status(int B, int gamma, int V, int dtype);
 cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream);
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream);
 cudaError_t launch_linear_topk(const LinearFinalizeParams &p, int topk, cudaStream_t stream);
-// The one-launch verify of a large batch (verify_fused.cu): whether it takes
-// these sizes and pointers, and the launch.
-bool fused_verify_applies(const LinearFinalizeParams &p);
-cudaError_t launch_fused_verify(const RowStatsParams &st, const LinearFinalizeParams &p,
-                                cudaStream_t stream);
+
 cudaError_t launch_tree_finalize(const TreeFinalizeParams &p, cudaStream_t stream);
 cudaError_t launch_philox_uniforms(const PhiloxParams &p, cudaStream_t stream);
 cudaError_t launch_row_entropy(const RowPartial *part, const float *temperature, int B, int R,

@@ -282,6 +282,7 @@ __device__ __forceinline__ void write_outputs_warp(const LinearFinalizeParams &p
     p.row_status[b] = d.status;
     if (d.status) p.final_token[b] = -1;
     else if (d.greedy) p.final_token[b] = d.arg;
+    if (d.status || d.greedy) p.ws.mass[b] = kNoMass;  // nothing drawn
   }
 }
 
@@ -320,6 +321,7 @@ __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const
       p.n_accepted[b] = 0;
       p.is_bonus[b] = 0;
       p.final_token[b] = -1;
+      p.ws.mass[b] = kNoMass;
     }
     return;
   }
@@ -357,6 +359,7 @@ __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const
     }
   }
   const unsigned long long target = uniform_target(U, Z);
+  if (lane == 0) p.ws.mass[b] = draw_mass(Z, d.S);
   // the stage holding the crossing
   unsigned long long base = 0;
   int st = -1;

@@ -300,6 +300,7 @@ __device__ __forceinline__ void request_search(const LinearFinalizeParams &p, lo
   if (tid == 0) {
     sm.chunk = -1;
     p.ws.draw_cnt[b] = 0;  // phase 2 may run again on the same phase-1 result
+    p.ws.mass[b] = draw_mass(Z, w.K);
   }
   __syncthreads();
   if (tid < nch && pre <= target && target - pre < mine) {

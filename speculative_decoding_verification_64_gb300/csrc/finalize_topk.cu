@@ -563,6 +563,7 @@ __device__ __forceinline__ void draw_candidates(const LinearFinalizeParams &p, l
     pre = block_exscan_u64(zk, rr, Z);
   }
   const unsigned long long target = uniform_target(__ldg(p.uniforms + b * R + gamma), Z);
+  if (tid == 0) p.ws.mass[b] = draw_mass(Z, d.S);  // the restricted residual's mass
   unsigned long long run = pre;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
@@ -643,6 +644,7 @@ __device__ __forceinline__ void bonus_draw(const LinearFinalizeParams &p, long l
     Z += sm.tot[w];
   }
   const unsigned long long target = uniform_target(__ldg(p.uniforms + b * R + gamma), Z);
+  if (threadIdx.x == 0) p.ws.mass[b] = draw_mass(Z, d.S);
   if (!(target >= before && target < before + sm.tot[warp])) return;
   // this warp's segment holds the target: its round, then the vector in u order
   int r = 0;

@@ -196,6 +196,7 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
         p.final_token[b] = -1;
         p.is_bonus[b] = 0;
         p.row_status[b] = status;
+        p.mass[b] = kNoMass;
       }
     }
     return;  // uniform across the cluster
@@ -302,6 +303,7 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
     }
     const float U = sm.uu[0];
     const unsigned long long target = uniform_target(U, sm.ds.Z);
+    if (rank == 0 && tid == 0) p.mass[b] = draw_mass(sm.ds.Z, sm.rowS[cur]);
     const int v = draw_search<DT>(sm.ds, r, target);
     if (tid == 0 && v >= 0) {
       p.final_token[b] = v;
@@ -322,6 +324,7 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
       if (greedy) {
         p.final_token[b] = fin_tok;
         p.out_tokens[b * D1 + nacc] = fin_tok;
+        p.mass[b] = kNoMass;
       }
     }
   }

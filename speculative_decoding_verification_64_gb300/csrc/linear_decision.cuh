@@ -61,6 +61,7 @@ __device__ __forceinline__ LinearDecision request_decision(const LinearFinalizeP
       p.row_status[b] = d.status;
       if (d.status) p.final_token[b] = -1;
       else if (d.greedy) p.final_token[b] = d.arg;
+      if (d.status || d.greedy) p.ws.mass[b] = kNoMass;  // nothing drawn
     }
   }
   return d;

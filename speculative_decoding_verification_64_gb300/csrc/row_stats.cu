@@ -43,8 +43,7 @@ __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsPa
   pdl_launch_dependents();  // phase 2 waits for this grid's completion itself
   extern __shared__ __align__(128) uint8_t smem_raw[];
   StatsSmem &sm = *reinterpret_cast<StatsSmem *>(smem_raw);
-  NoStageHook hook;
-  stats_role<DT, kA>(p, sm, (long long)blockIdx.x, (long long)gridDim.x, hook);
+  stats_role<DT, kA>(p, sm, (long long)blockIdx.x, (long long)gridDim.x);
 }
 
 template <int DT, bool kA>

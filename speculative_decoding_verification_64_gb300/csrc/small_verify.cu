@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(kT, 1)
     }
     const unsigned long long target = uniform_target(__ldg(p.uniforms + b * R + gamma), Z);
     const unsigned long long lo = cta_pre + pre;
+    if (rank == 0 && tid == 0) p.ws.mass[b] = h.abort_any ? kNoMass : draw_mass(Z, d.S);
     if (h.abort_any) {
       // the malformed-request outputs, over what the decision wrote (same threads)
       if (rank == 0) {

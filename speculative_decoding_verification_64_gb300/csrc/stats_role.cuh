@@ -1,10 +1,8 @@
 // The stats pass's loop as a device function of one CTA: the producer thread
 // streaming 16 KB units into the shared-memory ring and the consumer warps
 // reducing 8 KB stages into row partials ("Chapter 15: Decoding
-// acceleration", section 15.1.2 step 2).  The stats kernel runs it on every
-// CTA of its grid; the one-launch linear verify runs it on the CTAs that
-// stream the logits, with a hook that publishes the completion of each wave
-// of requests.
+// acceleration", section 15.1.2 step 2).  The stats kernel (row_stats.cu)
+// runs it on every CTA of its grid.
 #pragma once
 
 #include "stats_stage.cuh"
@@ -20,22 +18,14 @@ struct StatsSmem {
   volatile int abort_flag;
 };
 
-// A hook that does nothing (the plain stats pass).
-struct NoStageHook {
-  __device__ __forceinline__ void operator()(int, int) const {}
-};
-
 // The stats pass of one CTA over units first, first + stride, ... of the
 // row-major unit sequence (see row_stats.cu for the structure).  Every thread
 // of the CTA (kThreads) calls it; it returns once the CTA's stages are
-// reduced and, after a wait that gave up, its copies have landed.  After each
-// of its stages -- padding stages past a row's end included -- a consumer
-// warp calls hook(row, lane) once the stage's partial (and gather) is
-// stored: lane 0 made those stores.
+// reduced and, after a wait that gave up, its copies have landed.
 // kA: also the entropy sums of non-greedy rows (SPECDEC_STATS_ENTROPY).
-template <int DT, bool kA, typename Hook>
+template <int DT, bool kA>
 __device__ __forceinline__ void stats_role(const RowStatsParams &p, StatsSmem &sm,
-                                           long long first, long long stride, Hook &hook) {
+                                           long long first, long long stride) {
   constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
   constexpr int kPerVec = 16 / es;
   const int tid = threadIdx.x;
@@ -185,10 +175,7 @@ __device__ __forceinline__ void stats_role(const RowStatsParams &p, StatsSmem &s
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[slot]);  // this stage is in registers now
-    if (!real) {
-      hook(row, lane);
-      continue;
-    }
+    if (!real) continue;
 
     RowPartial r;
     r.flags = ok ? 0 : SPECDEC_ROW_INTERNAL;
@@ -217,7 +204,6 @@ __device__ __forceinline__ void stats_role(const RowStatsParams &p, StatsSmem &s
       }
     }
     if (lane == 0) p.part[(long long)row * p.spr + u.j0 + t] = r;
-    hook(row, lane);
   }
   // After any wait of the CTA gave up, the consumers stop waiting for copies:
   // keep the CTA until every copy the producer issued has landed.

@@ -17,7 +17,12 @@ Tolerances (written here, used by every parity test):
   thousands of draws.  (With V ~ 1e5 a final draw can land in a cell only
   ~1e-8 of Z wide, and the float32 weights of the GPU path resolve CDF edges
   to about that precision; so in-band mismatches are rare but possible.)
-* request status bitmasks: exact.
+* request status bitmasks: exact;
+* the normaliser Z of each final draw (``specdec_final_mass``: the mass of
+  max(0, p - q) at a rejection, of p for a bonus draw, of the final node's
+  renormalised residual in the tree form), in target-probability units: the
+  probability tolerance above, wherever the GPU and the oracle drew at the
+  same row (greedy requests draw nothing and are skipped).
 """
 import math
 
@@ -50,10 +55,24 @@ def linear_draws(o, gamma):
     return int(tests.sum() + k.size)
 
 
+def _mass_err(w, g, o, rows):
+    """Largest |Z_gpu - Z_oracle| over the given requests (non-greedy, drawn at
+    the same row by both sides); 0 when the GPU outputs carry no Z."""
+    if g.get("final_mass") is None or o.get("final_mass") is None:
+        return 0.0
+    rows = [b for b in rows if w.temperature[b] != 0]
+    if not rows:
+        return 0.0
+    gm = g["final_mass"][rows].astype(np.float64)
+    om = o["final_mass"][rows]
+    assert np.isfinite(gm).all(), ("no Z recorded for a drawn request", gm)
+    return float(np.abs(gm - om).max())
+
+
 def compare_linear(w, g, o, max_boundary_frac=1e-4):
     """g: GPU outputs as numpy dict; o: oracle outputs (with diagnostics)."""
     B, gamma = w.B, w.gamma
-    rep = dict(B=B, draws=0, in_band=0, excused=0, max_p_err=0.0)
+    rep = dict(B=B, draws=0, in_band=0, excused=0, max_p_err=0.0, max_mass_err=0.0)
     assert np.array_equal(g["row_status"], o["row_status"]), \
         (np.nonzero(g["row_status"] != o["row_status"]), g["row_status"], o["row_status"])
     ok = o["row_status"] == 0
@@ -68,6 +87,7 @@ def compare_linear(w, g, o, max_boundary_frac=1e-4):
         rep["max_p_err"] = float(err.max())
         assert rep["max_p_err"] <= P_TOL[w.dtype], rep
     u = w.uniforms.astype(np.float64)
+    same_rows = []
     for b in np.nonzero(ok)[0]:
         k = int(o["n_accepted"][b])
         ran = range(min(k + 1, gamma))
@@ -77,6 +97,8 @@ def compare_linear(w, g, o, max_boundary_frac=1e-4):
         same = (g["n_accepted"][b] == k and g["final_token"][b] == o["final_token"][b]
                 and g["is_bonus"][b] == o["is_bonus"][b]
                 and np.array_equal(g["out_tokens"][b], o["out_tokens"][b]))
+        if same:
+            same_rows.append(int(b))
         if near:
             rep["in_band"] += 1
             rep["excused"] += int(not same)
@@ -87,12 +109,14 @@ def compare_linear(w, g, o, max_boundary_frac=1e-4):
                           gpu_out=g["out_tokens"][b], ora_out=o["out_tokens"][b])
     rep["draws"] = linear_draws(o, gamma)
     assert rep["excused"] <= allowed_excused(rep["draws"], max_boundary_frac), rep
+    rep["max_mass_err"] = _mass_err(w, g, o, same_rows)
+    assert rep["max_mass_err"] <= P_TOL[w.dtype], rep
     return rep
 
 
 def compare_tree(w, g, o, max_boundary_frac=1e-4):
     B = w.B
-    rep = dict(B=B, draws=0, in_band=0, excused=0, max_p_err=0.0)
+    rep = dict(B=B, draws=0, in_band=0, excused=0, max_p_err=0.0, max_mass_err=0.0)
     assert np.array_equal(g["row_status"], o["row_status"]), (g["row_status"], o["row_status"])
     ok = o["row_status"] == 0
     bad = ~ok
@@ -105,11 +129,14 @@ def compare_tree(w, g, o, max_boundary_frac=1e-4):
         err = np.abs(g["p_node"][ok][:, 1:].astype(np.float64) - o["p_node"][ok][:, 1:])
         rep["max_p_err"] = float(err.max()) if err.size else 0.0
         assert rep["max_p_err"] <= P_TOL[w.dtype], rep
+    same_rows = []
     for b in np.nonzero(ok)[0]:
         greedy = w.temperature[b] == 0
         near = (not greedy) and (o["test_margin"][b] < BOUNDARY or o["final_margin"][b] < BOUNDARY)
         same = all(np.array_equal(g[key][b], o[key][b]) for key in
                    ("n_accepted", "path_nodes", "out_tokens", "final_token", "is_bonus"))
+        if same:
+            same_rows.append(int(b))
         if near:
             rep["in_band"] += 1
             rep["excused"] += int(not same)
@@ -120,6 +147,8 @@ def compare_tree(w, g, o, max_boundary_frac=1e-4):
                           tm=o["test_margin"][b], fm=o["final_margin"][b])
     rep["draws"] = int(o["n_accepted"].sum() + 2 * B)
     assert rep["excused"] <= allowed_excused(rep["draws"], max_boundary_frac), rep
+    rep["max_mass_err"] = _mass_err(w, g, o, same_rows)
+    assert rep["max_mass_err"] <= P_TOL[w.dtype], rep
     return rep
 
 
@@ -133,9 +162,14 @@ def gpu_linear(w, device="cuda", offset_elems=0):
     if offset_elems:
         logits = _offset_copy(logits, offset_elems)
         q = _offset_copy(q, offset_elems)
-    out = binding.verify_linear(logits, q, toks, temp, uni)
+    dt = binding.dtype_code(logits)
+    ws = binding.alloc_workspace(w.B, w.gamma + 1, w.V, dt, logits.device)
+    out = binding.verify_linear(logits, q, toks, temp, uni, workspace=ws)
+    mass = binding.final_mass(ws, w.B, w.gamma + 1, w.V, dt)
     torch.cuda.synchronize()
-    return {k: (None if v is None else v.cpu().numpy()) for k, v in vars(out).items()}
+    g = {k: (None if v is None else v.cpu().numpy()) for k, v in vars(out).items()}
+    g["final_mass"] = mass.cpu().numpy()
+    return g
 
 
 def gpu_tree(w, device="cuda", offset_elems=0):
@@ -145,9 +179,14 @@ def gpu_tree(w, device="cuda", offset_elems=0):
     if offset_elems:
         logits = _offset_copy(logits, offset_elems)
         q = _offset_copy(q, offset_elems)
-    out = binding.verify_tree(logits, q, toks, par, temp, uni, w.max_depth)
+    dt = binding.dtype_code(logits)
+    ws = binding.alloc_workspace(w.B, w.N, w.V, dt, logits.device)
+    out = binding.verify_tree(logits, q, toks, par, temp, uni, w.max_depth, workspace=ws)
+    mass = binding.final_mass(ws, w.B, w.N, w.V, dt)
     torch.cuda.synchronize()
-    return {k: (None if v is None else v.cpu().numpy()) for k, v in vars(out).items()}
+    g = {k: (None if v is None else v.cpu().numpy()) for k, v in vars(out).items()}
+    g["final_mass"] = mass.cpu().numpy()
+    return g
 
 
 def _offset_copy(t, off):

@@ -253,11 +253,8 @@ def test_verify_linear_launches_query(lib):
     assert vl(1, 4, 1000, 7, N, N) == -1                       # dtype
     # unaligned rows (7 bf16 elements = 14 bytes) take the two kernels
     assert vl(1, 4, 7, BF16, ctypes.c_void_p(256), ctypes.c_void_p(512)) == 2
-    # a large batch of aligned rows takes the large one-launch path
-    assert vl(4096, 8, 128256, BF16, ctypes.c_void_p(256), ctypes.c_void_p(512)) == 1
-    # ... and short rows (a 16 KB final row) or unaligned q the two kernels
-    assert vl(4096, 8, 8192, BF16, ctypes.c_void_p(256), ctypes.c_void_p(512)) == 2
-    assert vl(4096, 8, 128256, BF16, ctypes.c_void_p(256), ctypes.c_void_p(514)) == 2
+    # a large batch takes the two kernels
+    assert vl(4096, 8, 128256, BF16, ctypes.c_void_p(256), ctypes.c_void_p(512)) == 2
 
 
 def test_verify_linear_path_query(lib):
@@ -268,10 +265,8 @@ def test_verify_linear_path_query(lib):
     assert vp(0, 4, 1000, BF16, N, N) == binding.PATH_NONE
     assert vp(1, 0, 1000, BF16, N, N) == -1
     assert vp(1, 4, 32000, BF16, a, b) == binding.PATH_SMALL_ONE_LAUNCH
-    assert vp(256, 8, 128256, BF16, a, b) == binding.PATH_LARGE_ONE_LAUNCH
-    assert vp(512, 4, 152064, BF16, a, b) == binding.PATH_LARGE_ONE_LAUNCH
+    assert vp(256, 8, 128256, BF16, a, b) == binding.PATH_TWO_LAUNCHES
     assert vp(256, 8, 128255, BF16, a, b) == binding.PATH_TWO_LAUNCHES   # rows not 16-byte multiples
-    assert vp(4096, 8, 1 << 20, BF16, a, b) == binding.PATH_TWO_LAUNCHES  # final row over 512 KB
 
 
 def test_staging_sizes(lib):

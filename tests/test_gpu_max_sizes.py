@@ -112,10 +112,21 @@ def test_linear_past_four_gib(oracle_lib, law, V, B0, reps):
     from speculative_decoding_verification_64_gb300 import binding
     base = W.make_linear(law, B=B0, gamma=8, V=V, dtype="bf16", seed=23)
     x, uni = _tiled_linear(base, reps, seed=24)
-    assert binding.verify_linear_launches(x[0], x[1]) == 2   # stats pass + draw
+    assert binding.verify_linear_path(x[0], x[1]) == binding.PATH_TWO_LAUNCHES
     out = binding.verify_linear(*x)
     torch.cuda.synchronize()
     g = _numpy(out)
+    # the same batch as the call's two phases issued separately: the same
+    # outputs bit for bit
+    ws = binding.alloc_workspace(x[0].shape[0], base.gamma + 1, V, binding.BF16)
+    two = binding.LinearOut.empty(x[0].shape[0], base.gamma, "cuda")
+    binding.row_stats(x[0], x[3], ws, q=x[1], draft_tokens=x[2])
+    binding.linear_finalize(*x, two, ws)
+    torch.cuda.synchronize()
+    g2 = _numpy(two)
+    for key in g:
+        assert np.array_equal(g[key], g2[key], equal_nan=True), key
+    del ws, two
     B = B0 * reps
     _check_layout(g, base.gamma, V, np.tile(base.draft_tokens, (reps, 1)))
     # copies of one generated request: bit-identical target probabilities

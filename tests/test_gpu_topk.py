@@ -22,9 +22,15 @@ def built():
 def gpu_topk(w, topk):
     import torch
     from speculative_decoding_verification_64_gb300 import binding
-    out = binding.verify_linear_topk(*binding.linear_inputs_to_device(w), topk)
+    x = binding.linear_inputs_to_device(w)
+    dt = binding.dtype_code(x[0])
+    ws = binding.alloc_workspace(w.B, w.gamma + 1, w.V, dt)
+    out = binding.verify_linear_topk(*x, topk, workspace=ws)
+    mass = binding.final_mass(ws, w.B, w.gamma + 1, w.V, dt)
     torch.cuda.synchronize()
-    return {k: getattr(out, k).cpu().numpy() for k in KEYS}
+    g = {k: getattr(out, k).cpu().numpy() for k in KEYS}
+    g["final_mass"] = mass.cpu().numpy()
+    return g
 
 
 @pytest.mark.parametrize("name,B,V,topk", [

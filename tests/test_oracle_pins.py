@@ -944,3 +944,96 @@ def test_cascade_of_two_verify_levels_emits_the_target_law(oracle_lib):
         freq = np.bincount(tok, minlength=V) / n
         se = np.sqrt(law * (1 - law) / n)
         assert (np.abs(freq - law) <= 5 * se + 1e-9).all()
+
+
+# ----------------------------------------------------------------------------
+# the final draw's normaliser Z (section 15.1.2 step 4: the correction is
+# drawn from max(0, p - q) / Z)
+# ----------------------------------------------------------------------------
+
+def test_final_mass_of_exercise2(oracle_lib):
+    """Exercise 2's distributions: after any rejection Z = sum (p - q)+ = 0.1
+    (the derivation in the golden file); after an acceptance the bonus draw
+    from p has Z = 1."""
+    g = json.load(open(os.path.join(GOLDEN, "exercise2_pq.json")))
+    p = np.array(g["p"])
+    q = np.array(g["q"], dtype=np.float32)
+    logits = np.stack([np.log(p), np.log(p)]).astype(np.float32)
+    cases = [(tok, u0) for tok in range(3) for u0 in (1e-3, 0.999)]
+    B = len(cases)
+    out = oracle_lib.verify_linear(
+        tile(logits, B), tile(q[None, :], B), "f32",
+        np.array([[c[0]] for c in cases], np.int32), np.ones(B, np.float32),
+        np.array([[c[1], 0.5] for c in cases], np.float32))
+    for i in range(B):
+        if out["n_accepted"][i] == 0:
+            assert abs(out["final_mass"][i] - g["derived"]["sum_residual"]) < 1e-6
+        else:
+            assert abs(out["final_mass"][i] - 1.0) < 1e-12
+    assert (out["n_accepted"] == 0).any() and (out["n_accepted"] == 1).any()
+
+
+def test_final_mass_is_the_conservation_complement(oracle_lib):
+    """At a rejection at row k, Z = sum (p_k - q_k)+ = 1 - sum min(p_k, q_k)
+    (Lemma 1's conservation), with p_k from scipy's softmax; a bonus draw
+    has Z = sum p_gamma = 1.  Malformed requests report NaN."""
+    rng = np.random.default_rng(31)
+    B, gamma, V, T = 64, 4, 300, 0.8
+    logits = rng.normal(0, 2, size=(B, gamma + 1, V)).astype(np.float32)
+    q = special.softmax(rng.normal(0, 2, size=(B, gamma, V)), axis=-1).astype(np.float32)
+    toks = np.array([[rng.choice(V, p=q[b, i] / q[b, i].sum()) for i in range(gamma)]
+                     for b in range(B)], np.int32)
+    temp = np.full(B, T, np.float32)
+    temp[5] = -1.0                                      # malformed: bad temperature
+    uni = rng.uniform(0.05, 0.95, size=(B, gamma + 1)).astype(np.float32)
+    out = oracle_lib.verify_linear(logits, q, "f32", toks, temp, uni)
+    p = special.softmax(logits.astype(np.float64) / float(np.float32(T)), axis=-1)  # T as stored
+    for b in range(B):
+        if out["row_status"][b]:
+            assert np.isnan(out["final_mass"][b])
+            continue
+        k = int(out["n_accepted"][b])
+        if k == gamma:
+            want = p[b, gamma].sum()
+        else:
+            # sum (p - q)+ = sum p - sum min(p, q), whatever q (as stored) sums to
+            want = 1.0 - np.minimum(p[b, k], q[b, k].astype(np.float64)).sum()
+        assert abs(out["final_mass"][b] - want) < 1e-12, (b, k)
+    assert 0 < out["n_accepted"].mean() < gamma
+
+
+def test_final_mass_of_a_tree_after_rejected_siblings(oracle_lib):
+    """A root with K children whose tests all fail: the final draw is from the
+    root's residual after K renormalisations, whose mass relative to p is
+    N_K = sum (p - c_K q)+ with c_0 = 0, N_0 = 1, c_{j+1} = c_j + N_j (the
+    residual identity, here in numpy); with no rejection (a leaf) Z = 1."""
+    rng = np.random.default_rng(8)
+    B, K, V = 40, 3, 50
+    N = K + 1
+    logits = rng.normal(0, 1.5, size=(B, N, V)).astype(np.float32)
+    q = special.softmax(rng.normal(0, 1.5, size=(B, N, V)), axis=-1)
+    q = (q / q.sum(-1, keepdims=True)).astype(np.float32)
+    parent = np.array([[-1] + [0] * K] * B, np.int32)
+    toks = np.zeros((B, N), np.int32)
+    for b in range(B):
+        toks[b, 1:] = rng.choice(V, size=K, p=q[b, 0] / q[b, 0].sum())
+    uni = np.full((B, N), 0.9999999, np.float32)      # every sibling test fails ...
+    uni[::4, 1] = 1e-7                                  # ... except the first on every 4th tree
+    uni[:, 0] = rng.uniform(0.01, 0.99, size=B)
+    temp = np.ones(B, np.float32)
+    out = oracle_lib.verify_tree(logits, q, "f32", toks, parent, temp, uni, max_depth=1)
+    p = special.softmax(logits[:, 0].astype(np.float64), axis=-1)
+    for b in range(B):
+        assert out["row_status"][b] == 0
+        if out["n_accepted"][b] == 1:                   # accepted child: a leaf, bonus draw
+            assert abs(out["final_mass"][b] - 1.0) < 1e-12
+            continue
+        qq = q[b, 0].astype(np.float64)
+        c, Nj = 0.0, 1.0
+        for _ in range(K):                              # one renormalisation per rejected child
+            r = np.maximum(p[b] - (c + Nj) * qq, 0).sum()
+            if r <= 0:
+                break
+            c, Nj = c + Nj, r
+        assert abs(out["final_mass"][b] - Nj) < 1e-12, (b, out["final_mass"][b], Nj)
+    assert (out["n_accepted"] == 0).sum() > 20 and (out["n_accepted"] == 1).sum() > 5
