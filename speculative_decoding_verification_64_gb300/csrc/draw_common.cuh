@@ -377,36 +377,57 @@ __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const
     }
   }
   if (st < 0) return;  // no weight at all: unreachable for a usable row
-  // the vector, in index order (vector lane + 32 k), then the element
+  // the vector, in index order, then the element: lane L takes the stage's
+  // vectors 8L .. 8L + 7, so one warp scan of the lane totals orders them all
   uint4 lv[kVec], qv[kVec];
   const int off = st * kStage;
-  load_stage<DT>(lv, qv, rq.lrow + off, rq.qrow + off, min(kStage, rq.rowbytes - off), use_q, lane,
-                 true);
-  int kx = -1, lx = -1;               // the crossing vector: lane lx's vector kx
-  unsigned long long vbase = 0;       // fixed-point sum before it (valid in lane lx)
+  {
+    const int sb = min(kStage, rq.rowbytes - off);
+    const uint32_t ninf = kNegInfBits(DT);
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int o = (lane * kVec + k) * 16;
+      const bool in = o < sb;
+      lv[k] = in ? __ldg(reinterpret_cast<const uint4 *>(rq.lrow + off + o))
+                 : make_uint4(ninf, ninf, ninf, ninf);
+      qv[k] = (in && use_q) ? __ldg(reinterpret_cast<const uint4 *>(rq.qrow + off + o))
+                            : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  unsigned long long xs[kVec], lt = 0;
 #pragma unroll
   for (int k = 0; k < kVec; ++k) {
-    const unsigned long long x = to_fixed40(vec_sum<DT>(lv[k], qv[k], d, use_q));
-    const unsigned long long incl = warp_incl_scan_u64(x, lane);
-    const unsigned m = __ballot_sync(0xffffffffu, target < base + incl);
-    if (kx < 0 && m) {
-      kx = k;
-      lx = __ffs(m) - 1;
-      vbase = base + incl - x;
-    }
-    base += __shfl_sync(0xffffffffu, incl, 31);
+    xs[k] = to_fixed40(vec_sum<DT>(lv[k], qv[k], d, use_q));
+    lt += xs[k];
   }
-  if (kx < 0 || lane != lx) return;
+  const unsigned long long incl = warp_incl_scan_u64(lt, lane);
+  const unsigned m = __ballot_sync(0xffffffffu, target < base + incl);
+  if (!m) return;
+  const int lx = __ffs(m) - 1;
+  if (lane != lx) return;
+  unsigned long long vbase = base + incl - lt;
+  int kx = kVec - 1;
+#pragma unroll
+  for (int k = kVec - 1; k >= 0; --k) {
+    // the first vector of this lane whose running sum passes the target
+    unsigned long long pre = vbase;
+#pragma unroll
+    for (int j = 0; j < k; ++j) pre += xs[j];
+    if (target < pre + xs[k]) kx = k;
+  }
   uint4 ls = lv[0], qs = qv[0];
 #pragma unroll
-  for (int k = 1; k < kVec; ++k) {
+  for (int k = 0; k < kVec; ++k) {
     if (k == kx) {
       ls = lv[k];
       qs = qv[k];
     }
   }
+#pragma unroll
+  for (int j = 0; j < kVec; ++j)
+    if (j < kx) vbase += xs[j];
   const int e = vec_find<DT>(ls, qs, d, use_q, vbase, target);
-  const int v = off / es + (lane + 32 * kx) * vec_elems<DT>() + e;
+  const int v = off / es + (lane * kVec + kx) * vec_elems<DT>() + e;
   p.final_token[b] = v;
   p.out_tokens[b * R + d.k] = v;
 }
