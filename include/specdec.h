@@ -161,17 +161,12 @@ int specdec_final_mass(const void *workspace, size_t workspace_bytes, int B,
  *       16-byte aligned and each CTA's 1/C share of the request's gamma + 1
  *       target rows (plus the gamma q rows, or else of one q row) fitting its
  *       shared memory;
- *   SPECDEC_PATH_LARGE_ONE_LAUNCH  a large batch (B from half the SMs to 16
- *       per SM): one cooperative launch of one CTA per SM, the stats pass,
- *       a grid barrier, then the decisions and the draw dealt round robin
- *       over the CTAs; needs rows, logits and q 16-byte aligned;
  *   SPECDEC_PATH_TWO_LAUNCHES      the stats pass, then the draw.
  * Every path gives the same outputs and leaves the same workspace.
  * SPECDEC_PATH_NONE for B = 0, -1 for invalid sizes.
  */
 #define SPECDEC_PATH_NONE 0
 #define SPECDEC_PATH_SMALL_ONE_LAUNCH 1
-#define SPECDEC_PATH_LARGE_ONE_LAUNCH 2
 #define SPECDEC_PATH_TWO_LAUNCHES 3
 int specdec_verify_linear_path(int B, int gamma, int V, int dtype, const void *logits,
                                const void *q);

@@ -561,16 +561,13 @@ def final_mass(workspace: torch.Tensor, B: int, rows_per_request: int, V: int, d
     return out
 
 
-PATH_NONE, PATH_SMALL_ONE_LAUNCH, PATH_LARGE_ONE_LAUNCH, PATH_TWO_LAUNCHES = 0, 1, 2, 3
-PATH_KERNELS = {PATH_SMALL_ONE_LAUNCH: "small_verify_kernel",
-                PATH_LARGE_ONE_LAUNCH: "verify_coop_kernel",
-                PATH_TWO_LAUNCHES: "row_stats_kernel"}
+PATH_NONE, PATH_SMALL_ONE_LAUNCH, PATH_TWO_LAUNCHES = 0, 1, 3
+PATH_KERNELS = {PATH_SMALL_ONE_LAUNCH: "small_verify_kernel", PATH_TWO_LAUNCHES: "row_stats_kernel"}
 
 
 def verify_linear_path(logits: torch.Tensor, q: torch.Tensor) -> int:
     """The path ``verify_linear`` takes for these inputs (``PATH_*``): a small
-    batch in one launch, a large batch in one cooperative launch, or two
-    launches."""
+    batch in one launch, or two launches."""
     B, R, V = logits.shape
     return int(load_library().specdec_verify_linear_path(B, R - 1, V, dtype_code(logits),
                                                          _ptr(logits), _ptr(q)))

@@ -35,13 +35,12 @@ bool dtype_ok(int dtype) { return dtype == SPECDEC_F32 || dtype == SPECDEC_BF16;
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t gather, chunk, draw_cnt, dec, dec_ready, mass, total;
+  size_t gather, chunk, draw_cnt, mass, total;
 };
 
 // Stage partials first, then the linear form's gathered values, draw chunk
-// totals, tickets and the decision records of the one-launch step (with their
-// ready flags), then the normaliser of every request's final draw (both
-// forms).
+// totals and tickets, then the normaliser of every request's final draw
+// (both forms).
 WsLayout workspace_layout(long long B, int R, int V, int dtype) {
   const long long rows = B * (long long)R;
   WsLayout w;
@@ -50,9 +49,7 @@ WsLayout workspace_layout(long long B, int R, int V, int dtype) {
   w.chunk = w.gather + align256((size_t)rows * sizeof(float2));
   w.draw_cnt = w.chunk + align256((size_t)B * draw_total_slots(V, elem_bytes(dtype)) *
                                   sizeof(unsigned long long));
-  w.dec = w.draw_cnt + align256((size_t)B * sizeof(unsigned int));
-  w.dec_ready = w.dec + align256((size_t)B * sizeof(LinearDecision));
-  w.mass = w.dec_ready + align256((size_t)B * sizeof(unsigned int));
+  w.mass = w.draw_cnt + align256((size_t)B * sizeof(unsigned int));
   w.total = w.mass + align256((size_t)B * sizeof(float));
   return w;
 }
@@ -64,8 +61,6 @@ LinearWs linear_ws(void *workspace, long long B, int R, int V, int dtype) {
   ws.gather = reinterpret_cast<float2 *>(base + w.gather);
   ws.chunk_tot = reinterpret_cast<unsigned long long *>(base + w.chunk);
   ws.draw_cnt = reinterpret_cast<unsigned int *>(base + w.draw_cnt);
-  ws.dec = reinterpret_cast<LinearDecision *>(base + w.dec);
-  ws.dec_ready = reinterpret_cast<unsigned int *>(base + w.dec_ready);
   ws.mass = reinterpret_cast<float *>(base + w.mass);
   return ws;
 }
@@ -290,22 +285,6 @@ int specdec_verify_linear(const void *logits, const void *q, int dtype,
                       n_accepted, out_tokens, final_token, is_bonus, row_status, p_draft, workspace);
     return cuda_status(launch_small_verify(p, s));
   }
-  {
-    const LinearFinalizeParams p =
-        linear_params(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma, V,
-                      n_accepted, out_tokens, final_token, is_bonus, row_status, p_draft, workspace);
-    if (coop_verify_applies(p)) {
-      // a large batch: both phases in one cooperative launch, leaving the same
-      // workspace.  Should the GPU refuse to hold every CTA at once (others'
-      // work on its SMs), the two launches below do the step instead.
-      const cudaError_t e = launch_coop_verify(
-          stats_params(logits, q, dtype, draft_tokens, temperature, B, gamma + 1, V, workspace,
-                       false),
-          p, s);
-      if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_status(e);
-      (void)cudaGetLastError();  // clear the refused launch
-    }
-  }
   st = launch_stats(logits, q, dtype, draft_tokens, temperature, B, gamma + 1, V, workspace, s);
   if (st != SPECDEC_OK) return st;
   return linear_finalize_launch(logits, q, dtype, draft_tokens, temperature, uniforms, B, gamma,
@@ -318,14 +297,6 @@ int specdec_verify_linear_path(int B, int gamma, int V, int dtype, const void *l
   if (B <= 0) return SPECDEC_PATH_NONE;
   if (linear_size_status(B, gamma, V, dtype) != SPECDEC_OK) return -1;
   if (small_verify_applies(B, gamma, V, dtype, logits, q)) return SPECDEC_PATH_SMALL_ONE_LAUNCH;
-  LinearFinalizeParams p = {};
-  p.logits = logits;
-  p.q = q;
-  p.dtype = dtype;
-  p.B = B;
-  p.gamma = gamma;
-  p.V = V;
-  if (coop_verify_applies(p)) return SPECDEC_PATH_LARGE_ONE_LAUNCH;
   return SPECDEC_PATH_TWO_LAUNCHES;
 }
 

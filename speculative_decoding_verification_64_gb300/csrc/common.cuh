@@ -79,8 +79,6 @@ struct LinearWs {
   float2 *gather;                // [B*R] (l_i(x~_i), q_i(x~_i)) of row i < gamma
   unsigned long long *chunk_tot; // [B, draw_total_slots] fixed-point chunk / stage sums of the draw
   unsigned int *draw_cnt;        // [B] chunks done (ticket of the draw); the stats pass zeroes it
-  LinearDecision *dec;           // [B] decision records of the one-launch step
-  unsigned int *dec_ready;       // [B] their ready flags
   float *mass;                   // [B] normaliser of each request's final draw (below)
 };
 
@@ -210,11 +208,7 @@ int linear_size_status(int B, int gamma, int V, int dtype);
 cudaError_t launch_row_stats(const RowStatsParams &p, cudaStream_t stream);
 cudaError_t launch_linear_finalize(const LinearFinalizeParams &p, cudaStream_t stream);
 cudaError_t launch_linear_topk(const LinearFinalizeParams &p, int topk, cudaStream_t stream);
-// The one-launch step of a large batch (verify_coop.cu): whether it takes
-// these sizes and pointers, and the launch.
-bool coop_verify_applies(const LinearFinalizeParams &p);
-cudaError_t launch_coop_verify(const RowStatsParams &st, const LinearFinalizeParams &p,
-                               cudaStream_t stream);
+
 
 cudaError_t launch_tree_finalize(const TreeFinalizeParams &p, cudaStream_t stream);
 cudaError_t launch_philox_uniforms(const PhiloxParams &p, cudaStream_t stream);
@@ -387,10 +381,6 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
                : "memory");
-}
-
-__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
-  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ void fence_mbar_init() {

@@ -33,14 +33,13 @@ def check_same(outs):
             assert np.array_equal(a, b, equal_nan=True), (i, k)
 
 
-@pytest.mark.parametrize("V", [128256, 128255])   # the cooperative launch; the two kernels
+@pytest.mark.parametrize("V", [128256, 128255])   # the bulk-copy draw; the chunked draw
 def test_linear_calls_repeat_exactly(V):
     import torch
     from speculative_decoding_verification_64_gb300 import binding
     w = W.make_workload("linear_b256_g8_v128256_bf16", V=V)
     x = binding.linear_inputs_to_device(w)
-    want = binding.PATH_LARGE_ONE_LAUNCH if V % 8 == 0 else binding.PATH_TWO_LAUNCHES
-    assert binding.verify_linear_path(x[0], x[1]) == want
+    assert binding.verify_linear_path(x[0], x[1]) == binding.PATH_TWO_LAUNCHES
     ws = binding.alloc_workspace(w.B, w.gamma + 1, w.V, binding.dtype_code(x[0]))
     outs = [binding.LinearOut.empty(w.B, w.gamma, "cuda") for _ in range(N_CALLS)]
     for o in outs:
