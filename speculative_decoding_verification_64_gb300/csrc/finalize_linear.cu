@@ -329,6 +329,7 @@ __device__ __forceinline__ void request_search(const LinearFinalizeParams &p, lo
 // count runs the search.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) linear_draw_kernel(const LinearFinalizeParams p) {
+  pdl_launch_dependents();  // a next call's stats pass waits for this grid's completion itself
   pdl_wait();
   __shared__ DrawSmem sm;
   const int tid = threadIdx.x;
@@ -413,6 +414,7 @@ struct Smem {
 // them.  Launched after an arbitrary kernel, everything waits.
 template <int DT, bool kEarly>
 __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFinalizeParams p) {
+  pdl_launch_dependents();  // a next call's stats pass waits for this grid's completion itself
   if (!kEarly) pdl_wait();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);

@@ -40,7 +40,12 @@ using namespace stage;
 // kA: also the entropy sums of non-greedy rows (SPECDEC_STATS_ENTROPY).
 template <int DT, bool kA>
 __global__ void __launch_bounds__(kThreads, 1) row_stats_kernel(const RowStatsParams p) {
-  pdl_launch_dependents();  // phase 2 waits for this grid's completion itself
+  // Launched programmatically dependent on the kernel before it on the stream:
+  // wait for that kernel's completion before anything else, so only the
+  // launch itself overlaps it; then let phase 2 launch (it waits for this
+  // grid's completion itself).
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   StatsSmem &sm = *reinterpret_cast<StatsSmem *>(smem_raw);
   stats_role<DT, kA>(p, sm, (long long)blockIdx.x, (long long)gridDim.x);
@@ -55,8 +60,8 @@ cudaError_t launch_dt(const RowStatsParams &p, cudaStream_t stream) {
   const long long units = p.stages / p.spr * ((p.spr + kUnit - 1) / kUnit);
   long long grid = device_sm_count();
   if (grid > units) grid = units;
-  row_stats_kernel<DT, kA><<<(unsigned)grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(row_stats_kernel<DT, kA>, dim3((unsigned)grid), dim3(kThreads), (size_t)smem,
+                    stream, p);
 }
 
 }  // namespace

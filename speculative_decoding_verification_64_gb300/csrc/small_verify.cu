@@ -88,6 +88,11 @@ __device__ __forceinline__ unsigned long long cta_exscan_u64(unsigned long long 
 template <int DT>
 __global__ void __launch_bounds__(kT, 1)
     small_verify_kernel(const LinearFinalizeParams p, const int kC, const bool qres) {
+  // launched programmatically dependent on the kernel before it: only the
+  // launch overlaps that kernel (wait for it first); a next call's kernels
+  // wait for this grid's completion themselves
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Head &h = *reinterpret_cast<Head *>(smem_raw);
   uint8_t *slices = smem_raw + kHeadBytes;
@@ -317,13 +322,15 @@ cudaError_t launch_dt(const LinearFinalizeParams &p, const Plan &pl, cudaStream_
   cfg.blockDim = dim3(kT);
   cfg.dynamicSmemBytes = (size_t)kHeadBytes + (size_t)rows * nst * kStageBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)pl.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, small_verify_kernel<DT>, p, pl.C, pl.qres);
 }
 
