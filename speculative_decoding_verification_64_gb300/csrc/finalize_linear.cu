@@ -391,7 +391,7 @@ using namespace drawc;
 constexpr int kUnitStages = 4;
 constexpr int kUnitBytes = kStage * kUnitStages;    // one bulk copy of logits (+ one of q)
 constexpr int kSlots = 6;
-constexpr int kWarps = 12;                          // consumer warps
+constexpr int kWarps = 15;                          // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;         // + the producer warp
 constexpr int kMaxReq = 8;                          // requests in one CTA's run
 static_assert(kWarps <= kSlots * kUnitStages, "no more consumer warps than ring stages");
