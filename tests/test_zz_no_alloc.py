@@ -5,7 +5,7 @@ for a workspace (a runtime that forbids allocation once it is running, or a
 plug-in interface whose calls carry only inputs and outputs): its scratch is a
 fixed array inside the library.  Its results must be those of
 specdec_verify_linear with a caller workspace -- the same kernels on the same
-data -- on two calls in a row, whatever the previous call left in the array.
+data -- on calls in a row, whatever the previous call left in the array.
 This file is collected last so that a run stopping at the first failure has
 run every other test before it.
 """
@@ -56,11 +56,22 @@ def _with_workspace(w):
 
 
 def test_static_entry_point_matches_the_workspace_one(lib):
+    from speculative_decoding_verification_64_gb300 import binding
     cases = [
-        W.make_workload("linear_b256_g8_v128256_bf16", B=48, V=30011),
-        W.make_workload("mixed_b512_g4_v152064_bf16", B=40, V=20000, seed_offset=7),
+        # the one-launch path of a small batch
+        (W.make_workload("linear_b1_g4_v32000_f32", B=2), binding.PATH_SMALL_ONE_LAUNCH),
+        # the two launches: the chunked draw (odd V), the bulk-copy draw
+        (W.make_workload("linear_b256_g8_v128256_bf16", B=48, V=30011), binding.PATH_TWO_LAUNCHES),
+        (W.make_workload("mixed_b512_g4_v152064_bf16", B=40, V=20000, seed_offset=7),
+         binding.PATH_TWO_LAUNCHES),
+        # the benchmark's batch, whose scratch (1.2 MB) sits well inside the array
+        (W.make_workload("linear_b256_g8_v128256_bf16"), binding.PATH_TWO_LAUNCHES),
     ]
-    for w in cases:                       # two calls in a row on the shared array
+    for w, path in cases:                 # calls in a row on the shared array
+        x = binding.linear_inputs_to_device(w)
+        assert binding.verify_linear_path(x[0], x[1]) == path, w.name
+        assert lib.specdec_workspace_size(w.B, w.gamma + 1, w.V,
+                                          binding.dtype_code(x[0])) <= (4 << 20)
         got = _static(lib, w)
         want = _with_workspace(w)
         for key in ("n_accepted", "out_tokens", "final_token", "is_bonus", "row_status"):
