@@ -107,6 +107,27 @@ def test_greedy_rows_with_ties(oracle_lib):
     assert np.array_equal(g["final_token"][greedy], o["final_token"][greedy])
 
 
+@pytest.mark.parametrize("pattern", ["all", "first_half", "last_half", "every_third", "invalid"])
+def test_requests_that_draw_nothing(oracle_lib, pattern):
+    """Greedy requests and requests with an invalid temperature draw nothing:
+    the bulk-copy draw (aligned bf16 rows, B = 300) streams no unit of theirs,
+    wherever they sit in the CTAs' runs, all of them included."""
+    w = W.make_linear("normal2_tq08", B=300, gamma=4, V=32000, dtype="bf16", seed=17)
+    B = w.B
+    idx = {"all": np.arange(B), "first_half": np.arange(B // 2),
+           "last_half": np.arange(B // 2, B), "every_third": np.arange(0, B, 3),
+           "invalid": np.arange(0, B, 7)}[pattern]
+    w.temperature[idx] = 0.0
+    if pattern == "invalid":
+        bad = np.arange(3, B, 11)
+        w.temperature[bad] = np.array([-1.0, np.nan, 2.0 ** 21])[np.arange(bad.size) % 3]
+    g, o, rep = run(w, oracle_lib)
+    greedy = w.temperature == 0
+    assert np.array_equal(g["final_token"][greedy], o["final_token"][greedy])
+    if pattern == "invalid":
+        assert (g["row_status"][bad] == 8).all()
+
+
 def test_all_accepted_when_q_equals_p(oracle_lib):
     w = W.make_linear("normal2_q05", B=32, gamma=6, V=5000, dtype="f32", seed=8)
     l = w.logits[:, :w.gamma].astype(np.float64)
