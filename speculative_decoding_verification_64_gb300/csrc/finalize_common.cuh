@@ -28,7 +28,10 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPerThread = 16;        // contiguous elements per thread in a tile
 constexpr int kTile = kThreads * kPerThread;
-constexpr int kBatch = 4;             // tiles whose loads are in flight together
+// tiles whose loads are in flight together: 4 of bf16 (64 registers of raw
+// data a thread), 2 of float32 (the same bytes), within the 128-register cap
+template <int DT>
+__host__ __device__ constexpr int batch_tiles() { return (DT == SPECDEC_F32) ? 2 : 4; }
 constexpr int kMaxTilesPerCta = ((SPECDEC_MAX_V + kG - 1) / kG + 15 + kTile - 1) / kTile;
 constexpr double kFixedUnit = 0x1p-40;  // value of one unit of the fixed-point sums
 
@@ -159,6 +162,7 @@ template <int DT>
 __device__ __forceinline__ void draw_sums(DrawSmem &ds, const DrawRow &r, int pass) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nt = slice_tiles(r);
+  constexpr int kBatch = batch_tiles<DT>();
   for (int tb = 0; tb < nt; tb += kBatch) {
     Raw16<DT> x[kBatch];
 #pragma unroll

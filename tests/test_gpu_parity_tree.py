@@ -24,10 +24,47 @@ def run(w, oracle_lib, **kw):
     return g, o, rep
 
 
-@pytest.mark.parametrize("dtype,V", [("bf16", 10007), ("f32", 4099)])
+# Small cases: unaligned and aligned rows; V = 8 and 12 leave seven of the
+# eight CTA slices empty; float32 rows take two tiles a load batch.
+@pytest.mark.parametrize("dtype,V", [("bf16", 10007), ("f32", 4099), ("bf16", 10008),
+                                     ("f32", 4100), ("bf16", 8), ("f32", 12)])
 def test_tree_parity_small(oracle_lib, dtype, V):
     w = W.make_tree(B=12, N=64, V=V, dtype=dtype, seed=3)
     g, o, rep = run(w, oracle_lib)
+
+
+def test_tree_many_nodes_large_vocabulary(oracle_lib):
+    # 1024 nodes over an 80000-token vocabulary: three tiles a CTA slice (one
+    # partial), deep walks
+    w = W.make_tree(B=3, N=1024, V=80000, dtype="bf16", seed=9, max_depth=12, branching=3)
+    run(w, oracle_lib)
+
+
+def test_tree_aligned_and_unaligned_rows_agree():
+    # one stats pass, then the walk twice on it: on the aligned rows (vector
+    # loads) and on copies of them one element off a 16-byte boundary
+    # (element loads): identical results
+    import torch
+    from parity import _offset_copy
+    from speculative_decoding_verification_64_gb300 import binding
+    w = W.make_tree(B=24, N=64, V=20000, dtype="bf16", seed=8)
+    logits, q, toks, par, temp, uni = binding.tree_inputs_to_device(w)
+    dt = binding.dtype_code(logits)
+    ws = binding.alloc_workspace(w.B, w.N, w.V, dt)
+    binding.row_stats(logits, temp, ws)
+    res = []
+    for lg, qq in ((logits, q), (_offset_copy(logits, 1), _offset_copy(q, 1))):
+        out = binding.TreeOut.empty(w.B, w.N, w.max_depth, "cuda")
+        binding.tree_finalize(lg, qq, toks, par, temp, uni, w.max_depth, out, ws)
+        mass = binding.final_mass(ws, w.B, w.N, w.V, dt)
+        torch.cuda.synchronize()
+        r = {k: v.cpu().numpy() for k, v in vars(out).items() if v is not None}
+        r["final_mass"] = mass.cpu().numpy()
+        res.append(r)
+    assert (res[0]["row_status"] == 0).all()
+    for key in ("n_accepted", "path_nodes", "out_tokens", "final_token", "is_bonus",
+                "row_status", "p_node", "final_mass"):
+        assert np.array_equal(res[0][key], res[1][key]), key
 
 
 def test_tree_full_size(oracle_lib):
