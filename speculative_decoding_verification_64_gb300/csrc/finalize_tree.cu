@@ -22,9 +22,10 @@
 // One 8-CTA cluster per request.  Every CTA validates the tree and gathers
 // l_parent(t_n), q_parent(t_n) for all nodes; the row statistics are merged
 // one eighth per CTA and copied between the CTAs through distributed shared
-// memory; the walk is replicated in every CTA (the decisions depend only on
-// those values and on exact fixed-point cluster sums, so all CTAs agree);
-// reductions over the vocabulary are split across the cluster.
+// memory; then one warp finds the depths while the others form p_parent(t_n).  The walk is replicated in
+// every CTA (the decisions depend only on those values and on exact
+// fixed-point cluster sums, so all CTAs agree); reductions over the
+// vocabulary are split across the cluster.
 #include "finalize_common.cuh"
 
 namespace specdec {
@@ -37,7 +38,6 @@ constexpr int kMaxN = SPECDEC_MAX_TREE_NODES;
 struct TreeSmem {
   DrawSmem ds;
   int par[kMaxN];
-  int anc[kMaxN];
   int dep[kMaxN];
   int kids[kMaxN];
   float lg[kMaxN];    // l_parent(t_n)
@@ -50,7 +50,8 @@ struct TreeSmem {
   int tok[kMaxN];     // t_n
   float uu[kMaxN];    // the request's uniforms (slot 0: final draw; slot n: test of node n)
   int path[SPECDEC_MAX_TREE_DEPTH + 1];
-  int status, nkids;
+  int wst[kWarps];  // status bits found by each warp
+  int nkids;
 };
 
 __device__ __forceinline__ unsigned lanemask_lt() {
@@ -72,10 +73,6 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
   constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
 
   const float T = __ldg(p.temperature + b);
-  const bool greedy = (T == 0.0f);
-  const float c = temperature_scale(T);
-  if (tid == 0) sm.status = temperature_valid(T) ? 0 : SPECDEC_ROW_BAD_TEMP;
-  __syncthreads();
 
   // ---- structure, the drafted tokens' logits and q values ---------------------
   int st = 0;
@@ -83,8 +80,6 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
     const int a = __ldg(p.parent + nodebase + n);
     sm.par[n] = a;
     if (n == 0 ? (a != -1) : (a < 0 || a >= n)) st |= SPECDEC_ROW_BAD_TREE;
-    sm.anc[n] = (n == 0) ? -1 : a;
-    sm.dep[n] = (n == 0) ? 0 : 1;
     sm.lg[n] = 0.0f;
     sm.qg[n] = 1.0f;
     sm.uu[n] = __ldg(p.uniforms + nodebase + n);  // the walk then needs no global load per test
@@ -103,6 +98,10 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
     sm.qg[n] = qt;
     sm.lg[n] = lt;
   }
+
+  const bool greedy = (T == 0.0f);
+  const float c = temperature_scale(T);
+  if (!temperature_valid(T)) st |= SPECDEC_ROW_BAD_TEMP;
   // ---- row statistics: row n merged by warp (n / kG) % kWarps of CTA n % kG,
   // then every CTA copies the other CTAs' rows (one remote round trip instead
   // of a warp merging N / kWarps rows one after another)
@@ -125,63 +124,69 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
       sm.rowA[n] = o->rowA[n];
       sm.rowF[n] = o->rowF[n];
     }
+    st |= sm.rowF[n];
   }
   cluster.sync();  // every copy done before any CTA goes on (or exits)
-  for (int n = tid; n < N; n += kThreads) st |= sm.rowF[n];
-  if (st) atomicOr(&sm.status, st);
+  st = __reduce_or_sync(0xffffffffu, st);
+  if (lane == 0) sm.wst[warp] = st;
   __syncthreads();
-  const bool tree_ok = !(sm.status & SPECDEC_ROW_BAD_TREE);
-  if (tree_ok) {
-    // depths by pointer jumping (parent[n] < n, so every chain ends at the
-    // root); a tree of depth d is done after ceil(log2 d) + 1 rounds, and the
-    // rounds stop as soon as no node has an ancestor left to jump over
-    for (int it = 0; it < 11; ++it) {
-      int na[kMaxN / kThreads], nd[kMaxN / kThreads];
-      bool more = false;
-#pragma unroll
-      for (int k = 0; k < kMaxN / kThreads; ++k) {
-        const int n = tid + k * kThreads;
-        if (n < N) {
-          const int a = sm.anc[n];
-          more |= (a > 0);
-          na[k] = (a > 0) ? sm.anc[a] : a;
-          nd[k] = (a > 0) ? sm.dep[n] + sm.dep[a] : sm.dep[n];
-        }
-      }
-      if (!__syncthreads_or(more)) break;  // uniform: nothing would change
-#pragma unroll
-      for (int k = 0; k < kMaxN / kThreads; ++k) {
-        const int n = tid + k * kThreads;
-        if (n < N) {
-          sm.anc[n] = na[k];
-          sm.dep[n] = nd[k];
-        }
-      }
-      __syncthreads();
-    }
-  }
 
-  // ---- depths and p_parent of every drafted token ----------------------------
-  st = 0;
-  for (int n = tid; n < N; n += kThreads) {
-    if (tree_ok && sm.dep[n] > p.max_depth) st |= SPECDEC_ROW_BAD_TREE;
-    sm.pg[n] = 0.0f;
-    if (n == 0) continue;
-    const int t = sm.tok[n];
-    const int a = sm.par[n];
-    if (t < 0 || t >= V || a < 0 || a >= n) continue;
-    if (greedy) {
-      sm.pg[n] = (t == sm.rowA[a]) ? 1.0f : 0.0f;
-    } else {
-      RowStat r;
-      r.M = sm.rowM[a];
-      r.S = sm.rowS[a];
-      sm.pg[n] = target_prob(sm.lg[n], r, c);
+  // ---- depths (warp 0) and p_parent of every drafted token (the others) -------
+  if (warp == 0) {
+    // parent[n] < n: the depths of 32 nodes at a time, from the final depths
+    // of earlier nodes and, for parents among the 32, by shuffles (a chain
+    // within 32 nodes resolves one link a step)
+    bool deep = false;
+    for (int base = 0; base < N; base += 32) {
+      const int n = base + lane;
+      int a = -1, d = 0;
+      bool done = true;
+      if (n < N && n > 0) {
+        a = sm.par[n];
+        if (a >= 0 && a < n) {  // (a malformed parent is reported already)
+          if (a < base) d = sm.dep[a] + 1;
+          else done = false;
+        }
+      }
+      for (int it = 0; it < 32; ++it) {
+        if (!__ballot_sync(0xffffffffu, !done)) break;
+        const int src = done ? lane : a - base;
+        const int dp = __shfl_sync(0xffffffffu, d, src);
+        const int pdone = __shfl_sync(0xffffffffu, (int)done, src);
+        if (!done && pdone) {
+          d = dp + 1;
+          done = true;
+        }
+      }
+      if (n < N) {
+        sm.dep[n] = d;
+        deep |= d > p.max_depth;
+      }
+      __syncwarp();
+    }
+    if (__any_sync(0xffffffffu, deep) && lane == 0) sm.wst[0] |= SPECDEC_ROW_BAD_TREE;
+  } else {
+    for (int n = tid - 32; n < N; n += kThreads - 32) {
+      sm.pg[n] = 0.0f;
+      if (n == 0) continue;
+      const int t = sm.tok[n];
+      const int a = sm.par[n];
+      if (t < 0 || t >= V || a < 0 || a >= n) continue;
+      if (greedy) {
+        sm.pg[n] = (t == sm.rowA[a]) ? 1.0f : 0.0f;
+      } else {
+        RowStat r;
+        r.M = sm.rowM[a];
+        r.S = sm.rowS[a];
+        sm.pg[n] = target_prob(sm.lg[n], r, c);
+      }
     }
   }
-  if (st) atomicOr(&sm.status, st);
   __syncthreads();
-  const int status = sm.status;
+  int status_bits = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) status_bits |= sm.wst[w];
+  const int status = status_bits;
 
   if (status) {
     if (rank == 0) {
