@@ -79,6 +79,22 @@ def test_unaligned_base_pointers(oracle_lib, offset, dtype):
     run(w, oracle_lib, offset_elems=offset)
 
 
+def test_unaligned_rows_of_many_requests(oracle_lib):
+    # odd V (rows off 16-byte boundaries) and runs of more than 8 requests per
+    # CTA: the chunked draw with shifted vector loads
+    w = W.make_linear("normal2_tq08", B=1200, gamma=4, V=20003, dtype="bf16", seed=31)
+    run(w, oracle_lib)
+
+
+@pytest.mark.parametrize("V,offset", [(128255, 0), (128256, 1), (32001, 7)])
+def test_unaligned_rows_benchmark_vocabulary(oracle_lib, V, offset):
+    # rows off 16-byte boundaries at the benchmark's vocabulary (odd V or an
+    # offset base): the stats pass's plain edge loads and the chunked draw's
+    # shifted vectors, the row's last vector partial when V is odd
+    w = W.make_linear("zipf_t07", B=24, gamma=8, V=V, dtype="bf16", seed=V + offset)
+    run(w, oracle_lib, offset_elems=offset)
+
+
 def test_batch_zero_is_a_noop():
     import torch
     from speculative_decoding_verification_64_gb300 import binding
