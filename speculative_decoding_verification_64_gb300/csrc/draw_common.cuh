@@ -31,20 +31,23 @@ __device__ __forceinline__ float4 load_partial(const float4 *pr, int j, int spr,
 // Merge of one row's partials by a 16-lane segment of a warp (L2 loads: the
 // partials may have been written by other CTAs of the running kernel) (both segments
 // of the warp take part in every shuffle; an idle segment merges nothing).
-// The first two partials of each lane are loaded before any arithmetic, so
-// that rows of up to 32 stages cost one memory round trip.
+// The first three partials of each lane are loaded before any arithmetic, so
+// that rows of up to 48 stages (bf16 rows up to 196608 elements) cost one
+// memory round trip.
 __device__ __forceinline__ RowStat segment_merge_row(const RowPartial *part, long long row,
                                                      bool active, int spr, float c, int sl) {
   const float4 *pr = reinterpret_cast<const float4 *>(part + row * (long long)spr);
   const float4 x0 = load_partial(pr, sl, spr, active);
   const float4 x1 = load_partial(pr, sl + kSeg, spr, active);
+  const float4 x2 = load_partial(pr, sl + 2 * kSeg, spr, active);
   float m = -INFINITY, s = 0.0f;
   int a = 0x7FFFFFFF;
-  int fl = __float_as_int(x0.w) | __float_as_int(x1.w);
+  int fl = __float_as_int(x0.w) | __float_as_int(x1.w) | __float_as_int(x2.w);
   merge2(m, s, a, x0.x, x0.y, __float_as_int(x0.z), c);
   merge2(m, s, a, x1.x, x1.y, __float_as_int(x1.z), c);
+  merge2(m, s, a, x2.x, x2.y, __float_as_int(x2.z), c);
   if (active) {
-    for (int j = sl + 2 * kSeg; j < spr; j += kSeg) {  // rows of more than 32 stages
+    for (int j = sl + 3 * kSeg; j < spr; j += kSeg) {  // rows of more than 48 stages
       const float4 x = __ldcg(pr + j);
       fl |= __float_as_int(x.w);
       merge2(m, s, a, x.x, x.y, __float_as_int(x.z), c);
@@ -327,13 +330,14 @@ __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const
   }
   bool use_q = d.k < gamma;
   const float U = __ldg(p.uniforms + b * R + gamma);
-  // rows of at most 64 stages keep their stage totals in registers (two per lane)
-  const bool cached = Tot::kRegCache && rq.nst <= 64;
-  unsigned long long c0 = 0, c1 = 0, Z = 0;
+  // rows of at most 128 stages keep their stage totals in registers (four per
+  // lane, loaded together: one round trip)
+  const bool cached = Tot::kRegCache && rq.nst <= 128;
+  unsigned long long c[4] = {0, 0, 0, 0}, Z = 0;
   if (cached) {
-    c0 = (lane < rq.nst) ? tot.get(lane) : 0ull;
-    c1 = (lane + 32 < rq.nst) ? tot.get(lane + 32) : 0ull;
-    Z = c0 + c1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = (lane + 32 * i < rq.nst) ? tot.get(lane + 32 * i) : 0ull;
+    Z = c[0] + c[1] + c[2] + c[3];
   } else {
     for (int s = lane; s < rq.nst; s += 32) Z += tot.get(s);
   }
@@ -354,8 +358,8 @@ __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const
     }
     __syncwarp();
     if (cached) {
-      c0 = (lane < rq.nst) ? tot.get(lane) : 0ull;
-      c1 = (lane + 32 < rq.nst) ? tot.get(lane + 32) : 0ull;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] = (lane + 32 * i < rq.nst) ? tot.get(lane + 32 * i) : 0ull;
     }
   }
   const unsigned long long target = uniform_target(U, Z);
@@ -364,7 +368,8 @@ __device__ __forceinline__ void search_warp(const LinearFinalizeParams &p, const
   unsigned long long base = 0;
   int st = -1;
   for (int s0 = 0; s0 < rq.nst && st < 0; s0 += 32) {
-    const unsigned long long v = cached ? (s0 == 0 ? c0 : c1)
+    const int i = s0 >> 5;
+    const unsigned long long v = cached ? (i == 0 ? c[0] : i == 1 ? c[1] : i == 2 ? c[2] : c[3])
                                         : ((s0 + lane < rq.nst) ? tot.get(s0 + lane) : 0ull);
     const unsigned long long incl = warp_incl_scan_u64(v, lane);
     const unsigned m = __ballot_sync(0xffffffffu, target < base + incl);
