@@ -45,23 +45,36 @@ def _headers():
     return sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def _up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+# Test builds: the same sources with a define that changes one behaviour, in a
+# library (and object folder) of their own.  "shortwait": consumers' waits on
+# copies give up at once, so that the give-up paths run (see common.cuh).
+VARIANTS = {"shortwait": ["-DSPECDEC_CONSUMER_WAIT_NS=0ull"]}
+
+
+def _up_to_date(lib_path: str) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(f) <= t for f in _sources() + _headers() + [__file__])
 
 
-def build(force: bool = False, extra_flags=None, verbose: bool = False) -> str:
-    """Compile every CUDA translation unit and link ``libspecdec.so``.  Returns its path."""
-    if not force and _up_to_date():
-        return LIB_PATH
+def build(force: bool = False, extra_flags=None, verbose: bool = False,
+          variant: str = None) -> str:
+    """Compile every CUDA translation unit and link ``libspecdec.so`` (or the
+    test variant's ``libspecdec_<variant>.so``).  Returns its path."""
+    lib_path, build_dir = LIB_PATH, BUILD_DIR
+    if variant is not None:
+        extra_flags = list(extra_flags or []) + VARIANTS[variant]
+        lib_path = os.path.join(HERE, f"libspecdec_{variant}.so")
+        build_dir = BUILD_DIR + "_" + variant
+    if not force and _up_to_date(lib_path):
+        return lib_path
     nvcc = nvcc_path()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     flags = ARCH_FLAGS + NVCC_FLAGS + list(extra_flags or [])
     jobs = []
     for src in _sources():
-        obj = os.path.join(BUILD_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(os.path.basename(src))[0] + ".o")
         jobs.append(([nvcc] + flags + ["-c", src, "-o", obj], obj))
 
     def run(cmd):
@@ -75,14 +88,14 @@ def build(force: bool = False, extra_flags=None, verbose: bool = False) -> str:
             sys.stderr.write(r.stdout + r.stderr)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     link = [nvcc] + ARCH_FLAGS + ["-shared", "-cudart", "static", "-o", tmp] + \
         [o for _, o in jobs]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + " ".join(link) + "\n" + r.stdout + r.stderr)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 def main(argv=None):

@@ -443,13 +443,24 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 
 // Bounded wait: gives up after ~2 s of wall time (returns false).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// The limit of a consumer's wait for a copy it is about to read.  A test
+// build sets it to 0 (SPECDEC_CONSUMER_WAIT_NS): those waits then give up
+// without looking, every time, so that the give-up paths run; the waits that
+// keep a CTA until its copies have landed (the producers' and the drains')
+// keep kWaitLimitNs.
+#ifndef SPECDEC_CONSUMER_WAIT_NS
+#define SPECDEC_CONSUMER_WAIT_NS 2000000000ull
+#endif
+constexpr unsigned long long kConsumerWaitNs = SPECDEC_CONSUMER_WAIT_NS;
 
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  unsigned long long limit = kWaitLimitNs) {
+  if (limit == 0) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit) return false;
   }
 }
 

@@ -524,8 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1) draw_bulk_kernel(const LinearFina
       // wait tells only two phases apart, and copies land in any order)
       const bool ok = __all_sync(0xffffffffu,  // one outcome for the whole warp
                                  !sm.abort_flag &&
-                                     (use == 0 || mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1)) &&
-                                     mbar_wait_bounded(&sm.full[slot], use & 1));
+                                     (use == 0 || mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1,
+                                                                    kConsumerWaitNs)) &&
+                                     mbar_wait_bounded(&sm.full[slot], use & 1, kConsumerWaitNs));
       if (!ok) sm.abort_flag = 1;
       uint4 lv[kVec], qv[kVec];
       const int sbytes = (ok && real) ? min(kStage, rowbytes - s * kStage) : 0;

@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kT, 1)
   // ---- stage statistics, as the stats pass computes them --------------------
   // one outcome for the whole CTA (the threads could see the wait give up
   // differently, and the stage reductions below are warp-synchronous)
-  const bool ok = __syncthreads_and(mbar_wait_bounded(&h.full, 0)) != 0;
+  const bool ok = __syncthreads_and(mbar_wait_bounded(&h.full, 0, kConsumerWaitNs)) != 0;
   if (!ok) h.abort_flag = 1;  // the partials carry SPECDEC_ROW_INTERNAL: no draw follows
   const float T = __ldg(p.temperature + b);
   const float c = temperature_scale(T);
@@ -211,7 +211,9 @@ __global__ void __launch_bounds__(kT, 1)
                         (uint32_t)stage_bytes(j0 + t), &h.full);
       }
       qk = reinterpret_cast<const uint4 *>(slot);
-      if (!mbar_wait_bounded(&h.full, 1)) {
+      // one outcome for the CTA: a thread that saw the wait give up while
+      // thread 0 did not must not let junk sums pass as a draw
+      if (!__syncthreads_and(mbar_wait_bounded(&h.full, 1, kConsumerWaitNs))) {
         // this CTA's share never landed: the request gets SPECDEC_ROW_INTERNAL
         // (told to every CTA with the first draw barrier); its sums are junk
         if (tid == 0) {

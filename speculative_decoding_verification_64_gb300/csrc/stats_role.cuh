@@ -146,8 +146,9 @@ __device__ __forceinline__ void stats_role(const RowStatsParams &p, StatsSmem &s
     // everything after it is warp-synchronous)
     const bool ok = __all_sync(0xffffffffu,
                                !sm.abort_flag &&
-                                   (use == 0 || mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1)) &&
-                                   mbar_wait_bounded(&sm.full[slot], use & 1));
+                                   (use == 0 || mbar_wait_bounded(&sm.empty[slot], (use - 1) & 1,
+                                                                  kConsumerWaitNs)) &&
+                                   mbar_wait_bounded(&sm.full[slot], use & 1, kConsumerWaitNs));
     if (!ok) sm.abort_flag = 1;
     const int sbytes = max(0, min(kStageBytes, u.bytes - t * kStageBytes));
     if (ok && real) load_lane<DT>(d, sm.stage[slot] + t * kStageBytes, sbytes / 16, lane);
