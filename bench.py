@@ -356,12 +356,40 @@ class Setup:
             raise RuntimeError(f"{fn.__name__}: {self.binding.status_string(rc)}")
 
 
+PAUSE_CYCLES = 200_000  # ~0.1 ms at 2 GHz
+# Warm-up: the requested steps (at least 3), and at least this much wall time
+# of steps.  A 20-step timed region after 3 warm-up steps measured 0.7 us a
+# step slower than after 400 (about 50 ms): the GPU needs that long under load
+# to settle (the SM clock read 2070 MHz throughout).
+WARM_SECONDS = 0.1
+
+
 def time_steps(torch, st, K, warmup, stream, dist, sampler=None):
-    """K verify calls back to back between two events (after `warmup` calls);
-    every call is the public C entry point, nothing else is issued in between."""
+    """K verify calls back to back between two events (after the warm-up
+    calls); every call is the public C entry point, nothing else is issued in
+    between.  Sets st.warmup_run to the number of warm-up calls made."""
     st.marshal(stream)
-    for s in range(max(warmup, 3)):
+    # the requested warm-up steps, timed; then, back to back with no wait in
+    # between, as many more as fill WARM_SECONDS at that rate
+    n0 = max(warmup, 3)
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
+    for s in range(n0):
         st.call(s)
+    w1.record(stream)
+    torch.cuda.synchronize()
+    per_step = max(w0.elapsed_time(w1) / 1e3 / n0, 1e-6)
+    n = max(n0, int(WARM_SECONDS / per_step))
+    for s in range(n0, n):
+        st.call(s)
+    torch.cuda.synchronize()
+    # and one untimed run of the timed region's own shape (K steps from a
+    # synchronised start): the first such run after the warm-up measured
+    # slower than the ones after it
+    for s in range(K):
+        st.call(s)
+    st.warmup_run = n + K
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -369,6 +397,13 @@ def time_steps(torch, st, K, warmup, stream, dist, sampler=None):
     torch.cuda.synchronize()
     if sampler:
         sampler.mark("begin")
+    # A device-side pause (torch's bounded sleep kernel, ~0.1 ms) ahead of the
+    # start event, so that the host has queued the first calls when the timed
+    # region starts: the host's latency in issuing the first call is not
+    # device time of a step (the e2e figure counts the host).
+    if hasattr(torch.cuda, "_sleep"):
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(PAUSE_CYCLES)
     t0.record(stream)
     for s in range(K):
         st.call(s)
@@ -556,6 +591,7 @@ def run_ours(args, dist):
         "n_gpus": dist.world,
         "steps": K,
         "warmup": max(args.warmup, 3),
+        "warmup_run": st.warmup_run,
         "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True,
         "scaling": "weak",
