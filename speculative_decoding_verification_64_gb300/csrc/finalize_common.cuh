@@ -150,9 +150,45 @@ struct DrawSmem {
   unsigned long long prefix, Z, base;
   float Zf;  // Z as a float, in units of the row maximum
   unsigned long long scan_warp[kWarps];
+  alignas(8) uint64_t xbar[2];         // the exchange's arrivals, by pass parity
   int tile;
   int found;
+  int lost;                            // an exchange wait of this CTA gave up
 };
+
+// Before the first exchange, by thread 0 of every CTA, ahead of a cluster
+// barrier (the other CTAs' stores complete on these barriers).
+__device__ __forceinline__ void exchange_init(DrawSmem &ds) {
+  mbar_init(&ds.xbar[0], 1);
+  mbar_init(&ds.xbar[1], 1);
+  ds.lost = 0;
+  fence_mbar_init();
+}
+
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+// 8 bytes into another CTA's shared memory, completing bytes on its barrier
+__device__ __forceinline__ void st_async_u64(uint32_t addr, unsigned long long v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u64 [%0], %1, [%2];" ::"r"(addr),
+               "l"(v), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
 __device__ __forceinline__ int slice_tiles(const DrawRow &r) { return (r.v1 - r.v0 + kTile - 1) / kTile; }
 
@@ -194,24 +230,35 @@ __device__ __forceinline__ void draw_sums(DrawSmem &ds, const DrawRow &r, int pa
   }
 }
 
-// Cluster-wide exclusive prefix of the CTA totals (all CTAs call it).  Each
-// CTA stores its total into slot [pass & 1][rank] of every CTA's shared memory
-// (remote stores, made visible by the cluster barrier), then reads its own
-// copy: no remote load on the path.  A slot is rewritten two passes later,
-// after every CTA has passed the cluster barrier of the pass in between, i.e.
-// after every reader of the old value has read it.
+// Cluster-wide exclusive prefix of the CTA totals (all CTAs call it).  Thread
+// 0 of each CTA stores its total into slot [pass & 1][rank] of every CTA's
+// shared memory with an asynchronous remote store that completes 8 bytes on
+// that CTA's barrier xbar[pass & 1]; it expects kG * 8 bytes on its own and
+// waits (bounded) for them, then reads its own copy: no cluster-wide barrier
+// and no remote load on the path.  A slot and its barrier are used again two
+// passes later: a CTA reaches that pass only after every CTA's store of the
+// pass in between, which each CTA makes only after reading this pass's slots.
+// A wait that gives up marks the CTA lost (its sums are not to be trusted).
 __device__ __forceinline__ void draw_exchange(DrawSmem &ds, cg::cluster_group &cluster,
                                               int pass) {
   if (threadIdx.x == 0) {
     const unsigned rank = cluster.block_rank();
+    uint64_t *bar = &ds.xbar[pass & 1];
+    mbar_arrive_expect_tx(bar, (uint32_t)(kG * sizeof(unsigned long long)));
+    const uint32_t slot = smem_addr(&ds.totals[pass & 1][rank]);
+    const uint32_t b = smem_addr(bar);
     const unsigned long long s = ds.cta_total;
 #pragma unroll
     for (unsigned r = 0; r < (unsigned)kG; ++r)
-      cluster.map_shared_rank(&ds, r)->totals[pass & 1][rank] = s;
-  }
-  cluster.sync();
-  if (threadIdx.x == 0) {
-    const unsigned rank = cluster.block_rank();
+      st_async_u64(cluster_addr(slot, r), s, cluster_addr(b, r));
+    const uint32_t parity = (uint32_t)((pass >> 1) & 1);
+    bool ok = mbar_try_wait_cluster(bar, parity);
+    if (!ok) {
+      const unsigned long long t0 = global_timer_ns();
+      while (!(ok = mbar_try_wait_cluster(bar, parity)) && global_timer_ns() - t0 <= kWaitLimitNs) {
+      }
+    }
+    if (!ok) ds.lost = 1;
     unsigned long long pre = 0, tot = 0;
 #pragma unroll
     for (unsigned r = 0; r < (unsigned)kG; ++r) {

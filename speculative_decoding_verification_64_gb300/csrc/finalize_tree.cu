@@ -73,6 +73,13 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
   constexpr int es = (DT == SPECDEC_F32) ? 4 : 2;
 
   const float T = __ldg(p.temperature + b);
+  if (tid == 0) {
+    exchange_init(sm.ds);  // ahead of the cluster barriers below
+    // the request's status starts clean: a CTA whose exchange wait gives up
+    // ORs SPECDEC_ROW_INTERNAL into it at the end (ordered after this store
+    // by the cluster barriers)
+    if (rank == 0) p.row_status[b] = 0;
+  }
 
   // ---- structure, the drafted tokens' logits and q values ---------------------
   int st = 0;
@@ -325,7 +332,6 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
     if (tid == 0) {
       p.n_accepted[b] = nacc;
       p.is_bonus[b] = (uint8_t)bonus;
-      p.row_status[b] = 0;
       if (greedy) {
         p.final_token[b] = fin_tok;
         p.out_tokens[b * D1 + nacc] = fin_tok;
@@ -333,8 +339,10 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
       }
     }
   }
-  // No shared memory of another CTA is touched after the last cluster barrier
-  // (the walk's exchanges store before their barrier), so CTAs leave freely.
+  if (tid == 0 && sm.ds.lost) atomicOr(&p.row_status[b], SPECDEC_ROW_INTERNAL);
+  // Every store into this CTA's shared memory has landed once its last
+  // exchange wait completed (each exchange waits for all kG stores), and no
+  // CTA stores after its last exchange, so CTAs leave freely.
 }
 
 }  // namespace
