@@ -178,6 +178,13 @@ __device__ __forceinline__ void st_async_u64(uint32_t addr, unsigned long long v
                : "memory");
 }
 
+// 4 bytes into another CTA's shared memory, completing bytes on its barrier
+__device__ __forceinline__ void st_async_u32(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+               "r"(v), "r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -230,6 +237,16 @@ __device__ __forceinline__ void draw_sums(DrawSmem &ds, const DrawRow &r, int pa
   }
 }
 
+// Bounded wait on a barrier that other CTAs' asynchronous stores complete.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // Cluster-wide exclusive prefix of the CTA totals (all CTAs call it).  Thread
 // 0 of each CTA stores its total into slot [pass & 1][rank] of every CTA's
 // shared memory with an asynchronous remote store that completes 8 bytes on
@@ -251,14 +268,7 @@ __device__ __forceinline__ void draw_exchange(DrawSmem &ds, cg::cluster_group &c
 #pragma unroll
     for (unsigned r = 0; r < (unsigned)kG; ++r)
       st_async_u64(cluster_addr(slot, r), s, cluster_addr(b, r));
-    const uint32_t parity = (uint32_t)((pass >> 1) & 1);
-    bool ok = mbar_try_wait_cluster(bar, parity);
-    if (!ok) {
-      const unsigned long long t0 = global_timer_ns();
-      while (!(ok = mbar_try_wait_cluster(bar, parity)) && global_timer_ns() - t0 <= kWaitLimitNs) {
-      }
-    }
-    if (!ok) ds.lost = 1;
+    if (!mbar_wait_cluster_bounded(bar, (uint32_t)((pass >> 1) & 1))) ds.lost = 1;
     unsigned long long pre = 0, tot = 0;
 #pragma unroll
     for (unsigned r = 0; r < (unsigned)kG; ++r) {

@@ -21,8 +21,9 @@
 //
 // One 8-CTA cluster per request.  Every CTA validates the tree and gathers
 // l_parent(t_n), q_parent(t_n) for all nodes; the row statistics are merged
-// one eighth per CTA and copied between the CTAs through distributed shared
-// memory; then one warp finds the depths while the others form p_parent(t_n).  The walk is replicated in
+// one eighth per CTA and pushed to the other CTAs' shared memory by
+// asynchronous remote stores; then one warp finds the depths while the others
+// form p_parent(t_n).  The walk is replicated in
 // every CTA (the decisions depend only on those values and on exact
 // fixed-point cluster sums, so all CTAs agree); reductions over the
 // vocabulary are split across the cluster.
@@ -52,6 +53,7 @@ struct TreeSmem {
   int path[SPECDEC_MAX_TREE_DEPTH + 1];
   int wst[kWarps];  // status bits found by each warp
   int nkids;
+  alignas(8) uint64_t rbar;  // the other CTAs' merged rows have arrived
 };
 
 __device__ __forceinline__ unsigned lanemask_lt() {
@@ -74,12 +76,18 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
 
   const float T = __ldg(p.temperature + b);
   if (tid == 0) {
-    exchange_init(sm.ds);  // ahead of the cluster barriers below
+    exchange_init(sm.ds);
+    mbar_init(&sm.rbar, 1);
+    fence_mbar_init();
     // the request's status starts clean: a CTA whose exchange wait gives up
     // ORs SPECDEC_ROW_INTERNAL into it at the end (ordered after this store
-    // by the cluster barriers)
+    // by the cluster barrier)
     if (rank == 0) p.row_status[b] = 0;
   }
+  // every CTA of the cluster is running, with its barriers initialised, before
+  // any other CTA stores into its shared memory (arrive now, wait before the
+  // first remote store)
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   // ---- structure, the drafted tokens' logits and q values ---------------------
   int st = 0;
@@ -110,8 +118,8 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
   const float c = temperature_scale(T);
   if (!temperature_valid(T)) st |= SPECDEC_ROW_BAD_TEMP;
   // ---- row statistics: row n merged by warp (n / kG) % kWarps of CTA n % kG,
-  // then every CTA copies the other CTAs' rows (one remote round trip instead
-  // of a warp merging N / kWarps rows one after another)
+  // then pushed to the other CTAs by asynchronous remote stores that complete
+  // on their barrier rbar (one round trip, no cluster-wide barrier)
   for (int n = rank + kG * warp; n < N; n += kG * kWarps) {
     const RowStat r = warp_merge_row(p.part, nodebase + n, p.spr, c, lane);
     if (lane == 0) {
@@ -121,19 +129,26 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
       sm.rowF[n] = r.flags | (row_usable(r) ? 0 : SPECDEC_ROW_NONFINITE);
     }
   }
-  cluster.sync();  // every owner's rows written
-  for (int n = tid; n < N; n += kThreads) {
-    const int owner = n % kG;
-    if (owner != rank) {
-      const TreeSmem *o = cluster.map_shared_rank(&sm, owner);
-      sm.rowM[n] = o->rowM[n];
-      sm.rowS[n] = o->rowS[n];
-      sm.rowA[n] = o->rowA[n];
-      sm.rowF[n] = o->rowF[n];
-    }
-    st |= sm.rowF[n];
+  const int own = (N - rank + kG - 1) / kG;  // rows n = rank + kG k of this CTA
+  if (tid == 0)  // 4 words of every other CTA's row, from the kG - 1 others
+    mbar_arrive_expect_tx(&sm.rbar, (uint32_t)((N - own) * 16));
+  __syncthreads();  // this CTA's rows are in shared memory
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  for (int i = tid; i < own * (kG - 1) * 4; i += kThreads) {
+    const int f = i & 3, rest = i >> 2;
+    const int k = rest / (kG - 1), d = rest - k * (kG - 1);
+    const uint32_t dst = (uint32_t)(d < rank ? d : d + 1);  // every rank but this one
+    const int n = rank + kG * k;
+    uint32_t *word = (f == 0) ? reinterpret_cast<uint32_t *>(&sm.rowM[n])
+                     : (f == 1) ? reinterpret_cast<uint32_t *>(&sm.rowS[n])
+                     : (f == 2) ? reinterpret_cast<uint32_t *>(&sm.rowA[n])
+                                : reinterpret_cast<uint32_t *>(&sm.rowF[n]);
+    st_async_u32(cluster_addr(smem_addr(word), dst), *word, cluster_addr(smem_addr(&sm.rbar), dst));
   }
-  cluster.sync();  // every copy done before any CTA goes on (or exits)
+  // the other CTAs' rows (one outcome for the CTA: a lost row would make
+  // this CTA's walk differ from the others')
+  if (!__syncthreads_and(mbar_wait_cluster_bounded(&sm.rbar, 0)) && tid == 0) sm.ds.lost = 1;
+  for (int n = tid; n < N; n += kThreads) st |= sm.rowF[n];
   st = __reduce_or_sync(0xffffffffu, st);
   if (lane == 0) sm.wst[warp] = st;
   __syncthreads();
