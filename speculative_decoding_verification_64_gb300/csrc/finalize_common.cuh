@@ -165,37 +165,6 @@ __device__ __forceinline__ void exchange_init(DrawSmem &ds) {
   fence_mbar_init();
 }
 
-__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-
-// 8 bytes into another CTA's shared memory, completing bytes on its barrier
-__device__ __forceinline__ void st_async_u64(uint32_t addr, unsigned long long v, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u64 [%0], %1, [%2];" ::"r"(addr),
-               "l"(v), "r"(bar)
-               : "memory");
-}
-
-// 4 bytes into another CTA's shared memory, completing bytes on its barrier
-__device__ __forceinline__ void st_async_u32(uint32_t addr, uint32_t v, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
-               "r"(v), "r"(bar)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
 __device__ __forceinline__ int slice_tiles(const DrawRow &r) { return (r.v1 - r.v0 + kTile - 1) / kTile; }
 
@@ -234,16 +203,6 @@ __device__ __forceinline__ void draw_sums(DrawSmem &ds, const DrawRow &r, int pa
     unsigned long long s = 0;
     for (int i = 0; i < nt; ++i) s += ds.tile_tot[i];
     ds.cta_total = s;
-  }
-}
-
-// Bounded wait on a barrier that other CTAs' asynchronous stores complete.
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_t parity) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 

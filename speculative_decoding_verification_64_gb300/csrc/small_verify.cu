@@ -26,11 +26,12 @@
 //   U * Z finds the token -- the vector-ordered CDF of the bulk draw, so the
 //   token is the two-kernel step's.
 //
-// Every CTA of a cluster runs the same sequence of cluster barriers (the
-// branches between them depend only on the decision, which all CTAs compute
-// alike); the waits on memory (the bulk copies) are bounded.  Remote shared
-// memory is only written (each slot once per launch) before a cluster barrier,
-// never read.
+// Every CTA of a cluster runs the same sequence of cluster barriers and
+// exchanges (the branches between them depend only on the decision, which all
+// CTAs compute alike); the waits on memory (the bulk copies, the exchanges)
+// are bounded.  Remote shared memory is only written, by asynchronous stores
+// that complete on the receiver's barrier (each slot once per launch), never
+// read.
 #include <cfloat>
 
 #include <cooperative_groups.h>
@@ -55,9 +56,13 @@ struct Head {
   lindec::DecisionSmem dec;
   unsigned long long red[kW];
   unsigned long long tot[2][kMaxC];        // every CTA's draw weight, stored by that CTA; by attempt
+  alignas(8) uint64_t xbar[2];             // the exchange's arrivals, by attempt
   int abort_flag;                          // 1 + the parity of the copy wait that gave up, or 0
-  int abort_any;                           // set in every CTA by a CTA whose q-row wait gave up
+  int abort_any;                           // some CTA's q-row wait (or an exchange wait) gave up
 };
+// A CTA total carrying this bit reports a q-row wait that gave up (totals stay
+// below it: at most 2^21 weights <= 1 with 40 fraction bits).
+constexpr unsigned long long kAbortBit = 1ull << 63;
 constexpr int kHeadBytes = (int)((sizeof(Head) + 127) / 128 * 128);
 
 __device__ __forceinline__ unsigned long long cta_exscan_u64(unsigned long long v,
@@ -114,8 +119,10 @@ __global__ void __launch_bounds__(kT, 1)
 
   if (tid == 0) {
     mbar_init(&h.full, 1);
+    mbar_init(&h.xbar[0], 1);  // initialised before the first cluster barrier,
+    mbar_init(&h.xbar[1], 1);  // so before any remote store completes on them
     h.abort_flag = 0;
-    h.abort_any = 0;  // before the first cluster barrier, so before any remote store
+    h.abort_any = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -215,11 +222,8 @@ __global__ void __launch_bounds__(kT, 1)
       // thread 0 did not must not let junk sums pass as a draw
       if (!__syncthreads_and(mbar_wait_bounded(&h.full, 1, kConsumerWaitNs))) {
         // this CTA's share never landed: the request gets SPECDEC_ROW_INTERNAL
-        // (told to every CTA with the first draw barrier); its sums are junk
-        if (tid == 0) {
-          h.abort_flag = 2;
-          for (int r = 0; r < kC; ++r) *cluster.map_shared_rank(&h.abort_any, r) = 1;
-        }
+        // (told to every CTA with the first exchange); its sums are junk
+        if (tid == 0) h.abort_flag = 2;
       }
     }
     const int per = (nvec + kT - 1) / kT;
@@ -231,12 +235,21 @@ __global__ void __launch_bounds__(kT, 1)
       for (int v = v0; v < v1; ++v) mine += to_fixed40(vec_sum<DT>(lk[v], use_q ? qk[v] : none, d, use_q));
       unsigned long long tot;
       pre = cta_exscan_u64(mine, h.red, tot);
-      // this CTA's total into slot [attempt][rank] of every CTA (remote stores,
-      // visible after the barrier; a slot is written once per launch)
-      if (tid == 0)
-        for (int r = 0; r < kC; ++r) cluster.map_shared_rank(&h, r)->tot[attempt][rank] = tot;
-      cluster.sync();
-      if (h.abort_any) break;  // uniform: every CTA was told before the barrier
+      // this CTA's total (with the abort bit if its q-row wait gave up) into
+      // slot [attempt][rank] of every CTA by asynchronous remote stores that
+      // complete on that CTA's barrier xbar[attempt]; then the kC totals here
+      if (tid == 0) {
+        uint64_t *bar = &h.xbar[attempt];
+        mbar_arrive_expect_tx(bar, (uint32_t)(kC * sizeof(unsigned long long)));
+        const uint32_t slot = smem_addr(&h.tot[attempt][rank]), ba = smem_addr(bar);
+        const unsigned long long v = tot | (h.abort_flag == 2 ? kAbortBit : 0ull);
+        for (int r = 0; r < kC; ++r) st_async_u64(cluster_addr(slot, (uint32_t)r), v, cluster_addr(ba, (uint32_t)r));
+        bool any = !mbar_wait_cluster_bounded(bar, 0);
+        for (int r = 0; r < kC; ++r) any |= (h.tot[attempt][r] & kAbortBit) != 0;
+        h.abort_any = any;
+      }
+      __syncthreads();
+      if (h.abort_any) break;  // uniform: every CTA sees every total's abort bit
       cta_pre = 0;
       Z = 0;
       for (int r = 0; r < kC; ++r) {
@@ -277,9 +290,9 @@ __global__ void __launch_bounds__(kT, 1)
       }
     }
   }
-  // No CTA touches another's shared memory after the draw's last cluster
-  // barrier (the totals are stored before it; none at all on the other
-  // paths), so a CTA may leave now.  Copies of a
+  // Every store into this CTA's shared memory has landed once its last
+  // exchange wait completed, and none follows (no remote store at all on the
+  // other paths), so a CTA may leave now.  Copies of a
   // CTA whose wait gave up are waited for (bounded) before it exits.
   if (h.abort_flag && tid == 0) mbar_wait_bounded(&h.full, (uint32_t)(h.abort_flag - 1));
 }
