@@ -512,6 +512,7 @@ def run_ours(args, dist):
         sampler.start()
         time.sleep(0.3)
     total_ms = time_steps(torch, st, K, args.warmup, stream, dist, sampler)
+    warmup_run = st.warmup_run
     clocks = sampler.stop() if sampler else None
     # outputs of the last timed step (its rejected requests set the q-row bytes)
     torch.cuda.synchronize()
@@ -591,7 +592,7 @@ def run_ours(args, dist):
         "n_gpus": dist.world,
         "steps": K,
         "warmup": max(args.warmup, 3),
-        "warmup_run": st.warmup_run,
+        "warmup_run": warmup_run,
         "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True,
         "scaling": "weak",
