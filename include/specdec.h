@@ -46,7 +46,9 @@
  *     (SPECDEC_ERR_*); data errors inside a request are reported per request
  *     through row_status[b] (SPECDEC_ROW_* bits) and never trap the device;
  *     a request with a nonzero status gets n_accepted = 0, is_bonus = 0 and
- *     -1 in every token output;
+ *     -1 in every token output (one exception: when a tree walk's exchange
+ *     between the CTAs of a request's cluster runs out of time, the status
+ *     gets SPECDEC_ROW_INTERNAL and the other outputs are not to be used);
  *   - B = 0 is a no-op that returns SPECDEC_OK.
  *
  * Numerics: target probabilities are computed in float32 with base-2
@@ -87,7 +89,8 @@ extern "C" {
 #define SPECDEC_ROW_NONFINITE 4  /* a target row holds NaN or +inf, no finite value, or a max > 2^100 */
 #define SPECDEC_ROW_BAD_TEMP 8   /* temperature not 0 and not in [2^-20, 2^20] */
 #define SPECDEC_ROW_BAD_TREE 16  /* parent[0] != -1, parent[n] not in [0, n), or depth > max_depth */
-#define SPECDEC_ROW_INTERNAL 32  /* a kernel's bounded wait for its own copy ran out */
+#define SPECDEC_ROW_INTERNAL 32  /* a kernel's bounded wait ran out: for a copy of its own, or (tree walk)
+                                    for another CTA of the request's cluster */
 
 /* Limits. */
 #define SPECDEC_MAX_GAMMA 32       /* linear: drafted positions per request */
