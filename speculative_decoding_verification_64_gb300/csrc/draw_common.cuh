@@ -23,23 +23,19 @@ constexpr int kVec = kStage / 16 / 32;              // 16-byte vectors per lane 
 
 constexpr int kSeg = 16;                     // lanes merging one row
 
-__device__ __forceinline__ float4 load_partial(const float4 *pr, int j, int spr, bool active) {
-  return (active && j < spr) ? __ldcg(pr + j)
-                             : make_float4(-INFINITY, 0.0f, __int_as_float(0x7FFFFFFF), 0.0f);
-}
 
-// Merge of one row's partials by a 16-lane segment of a warp (L2 loads: the
-// partials may have been written by other CTAs of the running kernel) (both segments
-// of the warp take part in every shuffle; an idle segment merges nothing).
-// The first three partials of each lane are loaded before any arithmetic, so
-// that rows of up to 48 stages (bf16 rows up to 196608 elements) cost one
-// memory round trip.
-__device__ __forceinline__ RowStat segment_merge_row(const RowPartial *part, long long row,
-                                                     bool active, int spr, float c, int sl) {
-  const float4 *pr = reinterpret_cast<const float4 *>(part + row * (long long)spr);
-  const float4 x0 = load_partial(pr, sl, spr, active);
-  const float4 x1 = load_partial(pr, sl + kSeg, spr, active);
-  const float4 x2 = load_partial(pr, sl + 2 * kSeg, spr, active);
+// Merge of one row's partials by a 16-lane segment of a warp (both segments of
+// the warp take part in every shuffle; an idle segment merges nothing).
+// part(j) gives partial j < spr of the row.  The first three partials of each
+// lane are loaded before any arithmetic, so that rows of up to 48 stages
+// (bf16 rows up to 196608 elements) cost one memory round trip.
+template <typename Part>
+__device__ __forceinline__ RowStat segment_merge(const Part &part, bool active, int spr, float c,
+                                                 int sl) {
+  const float4 none = make_float4(-INFINITY, 0.0f, __int_as_float(0x7FFFFFFF), 0.0f);
+  const float4 x0 = (active && sl < spr) ? part(sl) : none;
+  const float4 x1 = (active && sl + kSeg < spr) ? part(sl + kSeg) : none;
+  const float4 x2 = (active && sl + 2 * kSeg < spr) ? part(sl + 2 * kSeg) : none;
   float m = -INFINITY, s = 0.0f;
   int a = 0x7FFFFFFF;
   int fl = __float_as_int(x0.w) | __float_as_int(x1.w) | __float_as_int(x2.w);
@@ -48,7 +44,7 @@ __device__ __forceinline__ RowStat segment_merge_row(const RowPartial *part, lon
   merge2(m, s, a, x2.x, x2.y, __float_as_int(x2.z), c);
   if (active) {
     for (int j = sl + 3 * kSeg; j < spr; j += kSeg) {  // rows of more than 48 stages
-      const float4 x = __ldcg(pr + j);
+      const float4 x = part(j);
       fl |= __float_as_int(x.w);
       merge2(m, s, a, x.x, x.y, __float_as_int(x.z), c);
     }
@@ -67,6 +63,14 @@ __device__ __forceinline__ RowStat segment_merge_row(const RowPartial *part, lon
   r.arg = a;
   r.flags = fl;
   return r;
+}
+
+// The same from the workspace (L2 loads: the partials may have been written
+// by other CTAs of the running kernel).
+__device__ __forceinline__ RowStat segment_merge_row(const RowPartial *part, long long row,
+                                                     bool active, int spr, float c, int sl) {
+  const float4 *pr = reinterpret_cast<const float4 *>(part + row * (long long)spr);
+  return segment_merge([&](int j) { return __ldcg(pr + j); }, active, spr, c, sl);
 }
 
 // Inputs of one lane's accept test: draft x~_i, its uniform, and the logit
@@ -98,11 +102,6 @@ __device__ __forceinline__ void load_draft_gather(const LinearFinalizeParams &p,
   if (lane < p.gamma) in.g = __ldcg(p.ws.gather + b * (p.gamma + 1) + lane);  // valid x only
 }
 
-__device__ __forceinline__ DraftIn load_draft(const LinearFinalizeParams &p, long long b, int lane) {
-  DraftIn in = load_draft_inputs(p, b, lane);
-  load_draft_gather(p, b, lane, in);
-  return in;
-}
 
 // The accept test of request b by warp 0 from the merged rows rs[0, R):
 // lane i < gamma tests draft i, a ballot gives the first rejection.  Lane

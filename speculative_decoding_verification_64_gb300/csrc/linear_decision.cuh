@@ -17,23 +17,40 @@ struct DecisionSmem {
   LinearDecision dec;
 };
 
+// Where a decision reads the stats pass's results (stage partials, gathered
+// logit and q of the drafted tokens): the workspace.
+struct WorkspaceSrc {
+  const LinearFinalizeParams &p;
+  __device__ __forceinline__ float4 partial(long long row, int j) const {
+    return __ldcg(reinterpret_cast<const float4 *>(p.part + row * (long long)p.spr) + j);
+  }
+  __device__ __forceinline__ float2 gather(long long b, int i) const {
+    return __ldcg(p.ws.gather + b * (p.gamma + 1) + i);
+  }
+};
+
 // The accept test of request b by a whole CTA of kT threads (rows merged by
 // 16-lane segments, the test in warp 0); the owner of chunk 0 also writes
 // every output but a drawn token.  Two barriers; the result is CTA-uniform.
-// S holds RowStat rs[SPECDEC_MAX_GAMMA + 1] and LinearDecision dec.
-template <int DT, int kT, typename S>
-__device__ __forceinline__ LinearDecision request_decision(const LinearFinalizeParams &p,
-                                                           long long b, bool owns_chunk0, S &sm) {
+// S holds RowStat rs[SPECDEC_MAX_GAMMA + 1] and LinearDecision dec; src gives
+// the stats pass's results (WorkspaceSrc, or a copy of them).
+template <int DT, int kT, typename S, typename Src>
+__device__ __forceinline__ LinearDecision request_decision_from(const LinearFinalizeParams &p,
+                                                                long long b, bool owns_chunk0,
+                                                                S &sm, const Src &src) {
   constexpr int kRowsPerRound = kT / kSeg;
   const int tid = threadIdx.x;
   const int gamma = p.gamma, R = gamma + 1;
   const float T = __ldg(p.temperature + b);
-  const DraftIn din = load_draft(p, b, tid);
+  DraftIn din = load_draft_inputs(p, b, tid);
+  if (tid < gamma) din.g = src.gather(b, tid);  // (read for valid tokens only)
   const float c = temperature_scale(T);
   for (int r0 = 0; r0 < R; r0 += kRowsPerRound) {
     const int r = r0 + tid / kSeg;
     if (r0 + (tid / 32) * (32 / kSeg) >= R) continue;  // both segments of this warp idle
-    const RowStat st = segment_merge_row(p.part, b * R + r, r < R, p.spr, c, tid % kSeg);
+    const long long row = b * R + r;
+    const RowStat st =
+        segment_merge([&](int j) { return src.partial(row, j); }, r < R, p.spr, c, tid % kSeg);
     if (r < R && tid % kSeg == 0) sm.rs[r] = st;
   }
   __syncthreads();
@@ -65,6 +82,12 @@ __device__ __forceinline__ LinearDecision request_decision(const LinearFinalizeP
     }
   }
   return d;
+}
+
+template <int DT, int kT, typename S>
+__device__ __forceinline__ LinearDecision request_decision(const LinearFinalizeParams &p,
+                                                           long long b, bool owns_chunk0, S &sm) {
+  return request_decision_from<DT, kT>(p, b, owns_chunk0, sm, WorkspaceSrc{p});
 }
 
 }  // namespace lindec

@@ -15,8 +15,10 @@
 //   workspace are the stats pass's, bit for bit; rank 0 also writes the
 //   gathered (logit, q) of the drafted tokens and zeroes the request's ticket,
 //   so the workspace ends as the two-kernel step leaves it;
-// * after a cluster barrier every CTA merges the partials and runs the accept
-//   test with the draw kernels' own routine (same merge order, same decision);
+// * the partials (and rank 0's gathered logit and q values) also go to every
+//   CTA's shared memory by asynchronous remote stores on an mbarrier; every
+//   CTA then merges them and runs the accept test with the draw kernels' own
+//   routine (same merge order, same decision);
 // * when the q rows are not resident and draft k was rejected, each CTA copies
 //   its share of q row k into the slot of the bonus row, which is no longer
 //   needed (k < gamma);
@@ -50,9 +52,15 @@ constexpr int kT = 512;                    // threads per CTA (a warp per stage 
 constexpr int kW = kT / 32;
 constexpr int kVecPerStage = kStageBytes / 16;
 constexpr int kMaxDynSmem = 200 * 1024;    // row slices plus the header
+// stage partials of a request: (gamma + 1) * ceil(spr / C) stage slots fit in
+// kMaxDynSmem, so R * spr <= 25 C
+constexpr int kMaxPart = (kMaxDynSmem / kStageBytes) * kMaxC;
 
 struct Head {
   alignas(8) uint64_t full;                // completes when this CTA's slices have landed
+  alignas(8) uint64_t pbar;                // every CTA's stage partials and rank 0's gathers have arrived
+  alignas(16) RowPartial part[kMaxPart];   // the request's stage partials [R][spr], pushed by their CTAs
+  float2 gath[SPECDEC_MAX_GAMMA];          // the drafted tokens' (logit, q), pushed by rank 0
   lindec::DecisionSmem dec;
   unsigned long long red[kW];
   unsigned long long tot[2][kMaxC];        // every CTA's draw weight, stored by that CTA; by attempt
@@ -88,6 +96,26 @@ __device__ __forceinline__ unsigned long long cta_exscan_u64(unsigned long long 
   return pre + inc - v;
 }
 
+// 16 bytes into another CTA's shared memory, completing bytes on its barrier
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+                   "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+               : "memory");
+}
+
+// The stats results of the request as the decision reads them: the copies
+// pushed into this CTA's shared memory.
+struct CopySrc {
+  const RowPartial *part;  // [R][spr]
+  const float2 *gath;
+  int spr, R;
+  long long b;
+  __device__ __forceinline__ float4 partial(long long row, int j) const {
+    return *reinterpret_cast<const float4 *>(part + (row - b * R) * spr + j);
+  }
+  __device__ __forceinline__ float2 gather(long long, int i) const { return gath[i]; }
+};
+
 // kC: CTAs per request (the launch's cluster size); qres: the q rows are
 // resident too, else q row k is copied in after the decision.
 template <int DT>
@@ -119,13 +147,18 @@ __global__ void __launch_bounds__(kT, 1)
 
   if (tid == 0) {
     mbar_init(&h.full, 1);
-    mbar_init(&h.xbar[0], 1);  // initialised before the first cluster barrier,
-    mbar_init(&h.xbar[1], 1);  // so before any remote store completes on them
+    mbar_init(&h.pbar, 1);     // initialised before the cluster arrival below,
+    mbar_init(&h.xbar[0], 1);  // so before any remote store completes on them
+    mbar_init(&h.xbar[1], 1);
     h.abort_flag = 0;
     h.abort_any = 0;
     fence_mbar_init();
+    mbar_arrive_expect_tx(&h.pbar, (uint32_t)(R * spr * sizeof(RowPartial) + gamma * sizeof(float2)));
   }
   __syncthreads();
+  // every CTA of the cluster is running with its barriers initialised before
+  // any stores into its shared memory (arrive now, wait before the first)
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   // ---- this CTA's slices of the request's rows, one bulk copy per stage ----
   if (tid == 0) {
     const int qrows = qres ? gamma : 0;
@@ -145,12 +178,14 @@ __global__ void __launch_bounds__(kT, 1)
                       (uint32_t)stage_bytes(j0 + t), &h.full);
   }
   // ---- the gathered (logit, q) of the drafted tokens, and the ticket ----------
+  float2 gx = make_float2(0.0f, 1.0f);  // (pushed to every CTA below; unused for a bad token)
   if (rank == 0 && tid < gamma) {
     const int x = __ldg(p.tokens + b * gamma + tid);
     if (x >= 0 && x < V) {
       const float lx = load_elem(p.logits, DT, (b * R + tid) * (long long)V + x);
       const float qx = load_elem(p.q, DT, (b * gamma + tid) * (long long)V + x);
-      p.ws.gather[b * R + tid] = make_float2(lx, qx);
+      gx = make_float2(lx, qx);
+      p.ws.gather[b * R + tid] = gx;
     }
   }
   if (rank == 0 && tid == 0) p.ws.draw_cnt[b] = 0u;
@@ -159,6 +194,19 @@ __global__ void __launch_bounds__(kT, 1)
   // differently, and the stage reductions below are warp-synchronous)
   const bool ok = __syncthreads_and(mbar_wait_bounded(&h.full, 0, kConsumerWaitNs)) != 0;
   if (!ok) h.abort_flag = 1;  // the partials carry SPECDEC_ROW_INTERNAL: no draw follows
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  // the request's partials and gathers go to every CTA of the cluster by
+  // asynchronous remote stores completing on its barrier pbar (the decision
+  // then reads them from shared memory: no cluster barrier, no L2 round trip)
+  const uint32_t pbar_a = smem_addr(&h.pbar);
+  if (rank == 0 && tid < gamma) {
+    // (x in the low word, y in the high: the float2's bytes)
+    const unsigned long long g =
+        ((unsigned long long)__float_as_uint(gx.y) << 32) | __float_as_uint(gx.x);
+    for (int r = 0; r < kC; ++r)
+      st_async_u64(cluster_addr(smem_addr(&h.gath[tid]), (uint32_t)r), g,
+                   cluster_addr(pbar_a, (uint32_t)r));
+  }
   const float T = __ldg(p.temperature + b);
   const float c = temperature_scale(T);
   for (int item = warp; item < R * nj; item += kW) {
@@ -188,14 +236,34 @@ __global__ void __launch_bounds__(kT, 1)
     }
     // the workspace's partials (read-only for the draw kernels, written here)
     if (lane == 0) const_cast<RowPartial *>(p.part)[(b * R + r) * (long long)spr + j] = part;
+    if (lane < kC)  // and every CTA's copy, lane r storing into CTA r
+      st_async_v4(cluster_addr(smem_addr(&h.part[r * spr + j]), (uint32_t)lane),
+                  make_uint4(__float_as_uint(part.m), __float_as_uint(part.s), (uint32_t)part.arg,
+                             (uint32_t)part.flags),
+                  cluster_addr(pbar_a, (uint32_t)lane));
   }
-  // A cluster barrier with release (arrive) and acquire (wait) semantics at
-  // cluster scope orders global memory as well: the partials and gathers
-  // written above are visible to every CTA of the cluster after it, with no
-  // GPU-scope fence.
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+  // every CTA's partials and the gathers here (one outcome for the CTA)
+  const bool got = __syncthreads_and(mbar_wait_cluster_bounded(&h.pbar, 0)) != 0;
   // ---- the accept test: every CTA alike, rank 0 writes the outputs ----------
-  const LinearDecision d = lindec::request_decision<DT, kT>(p, b, rank == 0, h.dec);
+  LinearDecision d;
+  if (got) {
+    d = lindec::request_decision_from<DT, kT>(p, b, rank == 0, h.dec, CopySrc{h.part, h.gath, spr, R, b});
+  } else {
+    // another CTA's results never arrived: the request gets SPECDEC_ROW_INTERNAL
+    d.status = SPECDEC_ROW_INTERNAL;
+    d.greedy = false;
+    if (rank == 0) {
+      if (tid < R) p.out_tokens[b * R + tid] = -1;
+      if (tid < gamma && p.p_draft) p.p_draft[b * gamma + tid] = __int_as_float(0x7fc00000);
+      if (tid == 0) {
+        p.n_accepted[b] = 0;
+        p.is_bonus[b] = 0;
+        p.row_status[b] = SPECDEC_ROW_INTERNAL;
+        p.final_token[b] = -1;
+        p.ws.mass[b] = kNoMass;
+      }
+    }
+  }
   if (!(d.status || d.greedy)) {
     // ---- the draw over row k: this CTA's vectors, in index order -------------
     const int k = d.k;
@@ -204,8 +272,9 @@ __global__ void __launch_bounds__(kT, 1)
     const uint4 *lk = reinterpret_cast<const uint4 *>(lsl + (size_t)k * nst * kStageBytes);
     const uint4 *qk = reinterpret_cast<const uint4 *>(qsl + (size_t)(use_q ? k : 0) * nst * kStageBytes);
     if (!qres && use_q) {
-      // q row k into the bonus row's slot (k < gamma; every read of that slot
-      // was before the cluster barrier above), second phase of the barrier
+      // q row k into the bonus row's slot (k < gamma; every read of that slot,
+      // by the stage statistics, was before the CTA barriers above), second
+      // phase of the copy barrier
       uint8_t *slot = lsl + (size_t)gamma * nst * kStageBytes;
       if (tid == 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -313,6 +382,7 @@ bool plan_for(int B, int gamma, int V, int dtype, const void *logits, const void
   while (C >= 2 && (long long)B * C > sms) C /= 2;
   if (C < 2) return false;
   const int spr = stages_per_row(V, es);
+  if ((long long)(gamma + 1) * spr > kMaxPart) return false;  // (implied by the fit below)
   const long long slot = (long long)((spr + C - 1) / C) * kStageBytes;  // one row's share
   pl.C = C;
   if ((long long)(2 * gamma + 1) * slot <= kMaxDynSmem) {
