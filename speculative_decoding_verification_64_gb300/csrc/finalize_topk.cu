@@ -130,14 +130,52 @@ struct Vec {
   static constexpr int kN = (DT == SPECDEC_F32) ? 4 : 8;  // elements per 16 bytes
 };
 
-// The 16 bytes of vector vi of a row (element loads for a vector that is
-// ragged, unaligned or past V; the missing elements read as zero bits and are
-// masked by the caller).
+// The 16 bytes at row + 16 vi of a row whose start is not 16-byte aligned
+// (vi * kN < V): the aligned vector holding the first byte, and the next one
+// when it holds a byte of the row, then whole-word and half-word shifts.
+// Every vector read holds a byte of the row (an aligned 16-byte vector never
+// straddles a page), so no read leaves the caller's buffer.  Elements at or
+// past V read as zero bits.
+template <int DT>
+__device__ __forceinline__ uint4 load_vec_shifted(const uint8_t *row, int vi, int V) {
+  constexpr int kN = Vec<DT>::kN;
+  constexpr int es = 16 / kN;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(row) + (uintptr_t)vi * 16u;
+  const uintptr_t end = reinterpret_cast<uintptr_t>(row) + (uintptr_t)V * es;
+  const unsigned mis = (unsigned)(a & 15u);
+  const uint4 *c = reinterpret_cast<const uint4 *>(a - mis);
+  const uint4 x0 = __ldg(c);
+  const uint4 x1 = (a - mis + 16u < end) ? __ldg(c + 1) : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  const unsigned ws = mis >> 2, hs = (mis & 2u) ? 16u : 0u;
+  uint32_t d[5];
+#pragma unroll
+  for (int j = 0; j < 5; ++j) d[j] = ws == 0 ? w[j] : ws == 1 ? w[j + 1] : ws == 2 ? w[j + 2] : w[j + 3];
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) o[j] = __funnelshift_r(d[j], d[j + 1], hs);
+  const int n = V - vi * kN;  // elements of the row in this vector (>= 1)
+  if (n < kN) {
+#pragma unroll
+    for (int e = 0; e < kN; ++e) {
+      if (e < n) continue;
+      if (DT == SPECDEC_F32) o[e] = 0u;
+      else o[e >> 1] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The 16 bytes of vector vi of a row (shifted aligned vectors on a row that
+// is not 16-byte aligned; element loads for the ragged last vector of an
+// aligned row; the missing elements read as zero bits and are masked by the
+// caller).
 template <int DT>
 __device__ __forceinline__ uint4 load_vec(const uint8_t *row, bool aligned, int vi, int V, bool valid) {
   constexpr int kN = Vec<DT>::kN;
   const int v0 = vi * kN;
   if (valid && aligned && v0 + kN <= V) return __ldg(reinterpret_cast<const uint4 *>(row) + vi);
+  if (valid && !aligned && v0 < V) return load_vec_shifted<DT>(row, vi, V);
   uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
   for (int e = 0; e < kN; ++e) {

@@ -59,3 +59,68 @@ def test_shifted_groups_are_the_bytes_at_every_offset():
 
 def test_the_model_detects_a_wrong_half_word_shift():
     assert _check(8) > 0
+
+
+# --- the top-k draw's single-vector form --------------------------------------
+# On a row that is not 16-byte aligned the top-k draw reads vector vi (16
+# bytes at row + 16 vi, element vi * kN < V) through the aligned vector that
+# holds its first byte and, only when it still holds a byte of the row, the
+# next one; the words are moved into place the same way, and the elements at
+# or past V are cleared.
+
+
+def shifted_vec(buf, row, vi, V, es, half_shift=16):
+    kN = 16 // es
+    a = row + 16 * vi
+    end = row + V * es
+    mis = a & 15
+    base = a - mis
+    reads = [(base, base + 16)]
+    w = [int.from_bytes(bytes(buf[base + 4 * j: base + 4 * j + 4]), "little") for j in range(4)]
+    if base + 16 < end:
+        reads.append((base + 16, base + 32))
+        w += [int.from_bytes(bytes(buf[base + 16 + 4 * j: base + 20 + 4 * j]), "little")
+              for j in range(4)]
+    else:
+        w += [0] * 4
+    ws, hs = mis >> 2, (half_shift if mis & 2 else 0)
+    d = [w[j + ws] for j in range(5)]
+    o = [funnel_r(d[j], d[j + 1], hs) for j in range(4)]
+    n = V - vi * kN
+    for e in range(n, kN):
+        if es == 4:
+            o[e] = 0
+        else:
+            o[e >> 1] &= 0x0000FFFF if e & 1 else 0xFFFF0000
+    return o, reads
+
+
+def _check_vec(half_shift):
+    rng = np.random.default_rng(11)
+    buf = rng.integers(0, 256, size=4096, dtype=np.uint8)
+    wrong = 0
+    for es in (2, 4):
+        kN = 16 // es
+        for mis in range(es, 16, es):              # every unaligned row start
+            for V in (1, 2, 3, 7, 8, 9, 15, 16, 17, 31, 40):
+                row = 1024 + mis
+                end = row + V * es
+                for vi in range(-(-V // kN)):
+                    got, reads = shifted_vec(buf, row, vi, V, es, half_shift)
+                    a = row + 16 * vi
+                    want = bytearray(buf[a: a + 16])
+                    for e in range(V - vi * kN, kN):    # elements past V read as zero
+                        want[e * es: e * es + es] = bytes(es)
+                    want = [int.from_bytes(bytes(want[4 * j: 4 * j + 4]), "little") for j in range(4)]
+                    wrong += got != want
+                    for lo, hi in reads:                 # every read holds a byte of the row
+                        assert lo < end and hi > row, (es, mis, V, vi, lo, hi)
+    return wrong
+
+
+def test_topk_shifted_vectors_are_the_row_bytes():
+    assert _check_vec(16) == 0
+
+
+def test_topk_vector_model_detects_a_wrong_half_word_shift():
+    assert _check_vec(8) > 0
