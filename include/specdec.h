@@ -159,8 +159,9 @@ int specdec_final_mass(const void *workspace, size_t workspace_bytes, int B,
 /*
  * Which path specdec_verify_linear takes for these arguments (host only):
  *   SPECDEC_PATH_SMALL_ONE_LAUNCH  a small batch: one cluster of C CTAs per
- *       request (C the largest of 8, 4, 2 with B * C no more than the GPU's
- *       SMs) holding its rows in shared memory; needs rows, logits and q
+ *       request (C the largest of 16, 8, 4, 2 of which the device holds B
+ *       clusters at once, one CTA per SM) holding its rows in shared memory;
+ *       needs rows, logits and q
  *       16-byte aligned and each CTA's 1/C share of the request's gamma + 1
  *       target rows (plus the gamma q rows, or else of one q row) fitting its
  *       shared memory;

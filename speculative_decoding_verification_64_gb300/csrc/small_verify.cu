@@ -5,7 +5,8 @@
 // The two-kernel step (stats pass, then the draw) pays two launches and
 // several dependent memory round trips in each; with few requests the data is
 // small enough to stay on chip instead.  One cluster of C CTAs per request
-// (C = 8, 4 or 2: the largest with B * C CTAs on the GPU at once):
+// (C = 16, 8, 4 or 2: the largest of which the device holds all B clusters at
+// once, one CTA per SM):
 //
 // * CTA r bulk-copies its share of every target row of the request -- stages
 //   r*n .. r*n + n - 1 (8 KB each) of the gamma+1 rows -- into shared memory,
@@ -47,7 +48,12 @@ namespace {
 namespace cg = cooperative_groups;
 using namespace drawc;
 
-constexpr int kMaxC = 8;                   // CTAs per request at most: a portable cluster
+// CTAs per request at most: 16, a cluster size beyond the portable 8 that
+// the kernel opts into (taken only where the device can hold such a cluster)
+#ifndef SPECDEC_SMALL_MAX_C
+#define SPECDEC_SMALL_MAX_C 16
+#endif
+constexpr int kMaxC = SPECDEC_SMALL_MAX_C;
 constexpr int kT = 512;                    // threads per CTA (a warp per stage at B = 1)
 constexpr int kW = kT / 32;
 constexpr int kVecPerStage = kStageBytes / 16;
@@ -372,14 +378,62 @@ struct Plan {
   bool qres;
 };
 
+// How many clusters of C CTAs (C = 16, 8, 4 or 2) the device holds at once
+// with one CTA of this kernel per SM, once per device and size: the count
+// depends on how the SMs fall into GPCs, so it can be below SMs / C, and a
+// batch of more clusters runs in two waves.  16 needs the non-portable
+// cluster size opt-in.  -1 when the query is not answered (no device).
+constexpr int kSizes = 4;  // C = 16 >> i
+std::atomic<int> g_capacity[kMaxCachedDevices][kSizes]{};  // count + 2; 0: not asked yet
+
+int cluster_capacity(int C) {
+  const int i = (C == 16) ? 0 : (C == 8) ? 1 : (C == 4) ? 2 : 3;
+  int dev = 0;
+  if (C > kMaxC || cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+  int c = (dev < kMaxCachedDevices) ? g_capacity[dev][i].load(std::memory_order_relaxed) : 0;
+  if (c != 0) return c - 2;
+  int n = -1;
+  const int smem = kHeadBytes + kMaxDynSmem;
+  auto kernel = small_verify_kernel<SPECDEC_BF16>;
+  bool ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
+  if (ok && C > 8)
+    ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+         cudaFuncSetAttribute(small_verify_kernel<SPECDEC_F32>,
+                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  if (ok) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C);
+    cfg.blockDim = dim3(kT);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = (unsigned)C;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int m = 0;
+    if (cudaOccupancyMaxActiveClusters(&m, kernel, &cfg) == cudaSuccess) n = m;
+  }
+  (void)cudaGetLastError();  // a refused query leaves no error behind
+  if (dev < kMaxCachedDevices) g_capacity[dev][i].store(n + 2, std::memory_order_relaxed);
+  return n;
+}
+
 bool plan_for(int B, int gamma, int V, int dtype, const void *logits, const void *q, Plan &pl) {
   const int es = (dtype == SPECDEC_F32) ? 4 : 2;
   const long long rowbytes = (long long)V * es;
   if (B < 1 || rowbytes % 16 != 0) return false;
   if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(q)) & 15) return false;
+  // the largest cluster size whose B clusters the device holds at once (one
+  // CTA per SM); without an answer from the device, B C no more than its SMs
+  // and at most 8
   const long long sms = device_sm_count();
-  int C = kMaxC;  // the largest cluster with every CTA on the GPU at once (one CTA per SM)
-  while (C >= 2 && (long long)B * C > sms) C /= 2;
+  int C = kMaxC;
+  for (; C >= 2; C /= 2) {
+    const int cap = cluster_capacity(C);
+    if (cap >= 0 ? B <= cap : (C <= 8 && (long long)B * C <= sms)) break;
+  }
   if (C < 2) return false;
   const int spr = stages_per_row(V, es);
   if ((long long)(gamma + 1) * spr > kMaxPart) return false;  // (implied by the fit below)

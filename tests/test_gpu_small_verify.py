@@ -1,11 +1,12 @@
 """The one-launch path of specdec_verify_linear for small batches (one cluster
-of 8, 4 or 2 CTAs per request, rows held in shared memory; the q rows too when
-they fit, else q row k copied in after the decision) against the two-kernel
-path (specdec_row_stats, then specdec_linear_finalize) and the oracle:
-outputs, p_draft and the workspace's stage partials bit for bit.
+of 16, 8, 4 or 2 CTAs per request, rows held in shared memory; the q rows too
+when they fit, else q row k copied in after the decision) against the
+two-kernel path (specdec_row_stats, then specdec_linear_finalize) and the
+oracle: outputs, p_draft and the workspace's stage partials bit for bit.
 
-With 152 SMs the cases below take: B <= 19 clusters of 8, B = 24 clusters of
-4, B = 40 .. 64 clusters of 2; the q rows are resident except in the cases
+The cluster size is the largest of which the device holds all B clusters at
+once: on a GB300 the smallest batches below take clusters of 16, the others
+clusters of 8, 4 or 2 as B grows; the q rows are resident except in the cases
 marked "q row k after the decision"."""
 import numpy as np
 import pytest
@@ -54,6 +55,7 @@ def both_paths(w):
 
 @pytest.mark.parametrize("name,B,V,gamma", [
     ("linear_b1_g4_v32000_f32", 1, None, None),       # the B = 1 workload itself
+    ("linear_b256_g8_v128256_bf16", 1, None, None),   # one request of the benchmark's rows
     ("linear_b1_g4_v32000_f32", 8, 20000, None),
     ("linear_b64_g5_v32000_bf16", 19, None, None),    # the largest batch of one wave
     ("linear_b64_g5_v32000_bf16", 3, 4104, None),     # a last stage of 16 bytes
