@@ -161,10 +161,9 @@ int specdec_final_mass(const void *workspace, size_t workspace_bytes, int B,
  *   SPECDEC_PATH_SMALL_ONE_LAUNCH  a small batch: one cluster of C CTAs per
  *       request (C the largest of 16, 8, 4, 2 of which the device holds B
  *       clusters at once, one CTA per SM) holding its rows in shared memory;
- *       needs rows, logits and q
- *       16-byte aligned and each CTA's 1/C share of the request's gamma + 1
- *       target rows (plus the gamma q rows, or else of one q row) fitting its
- *       shared memory;
+ *       needs rows, logits and q 16-byte aligned and each CTA's 1/C share of
+ *       the request's gamma + 1 target rows (plus the gamma q rows, or else
+ *       of one q row) fitting its shared memory;
  *   SPECDEC_PATH_TWO_LAUNCHES      the stats pass, then the draw.
  * Every path gives the same outputs and leaves the same workspace.
  * SPECDEC_PATH_NONE for B = 0, -1 for invalid sizes.
