@@ -56,7 +56,8 @@ LINEAR = [
     (lambda: W.make_workload("linear_b256_g8_v128256_bf16", B=64), "two launches, bulk-copy draw"),
     (lambda: W.make_linear("normal2_tq08", B=16, gamma=4, V=20003, dtype="bf16", seed=3),
      "two launches, chunked draw"),
-    (lambda: W.make_workload("linear_b1_g4_v32000_f32", B=2), "one launch, clusters of 8"),
+    (lambda: W.make_workload("linear_b1_g4_v32000_f32", B=2), "one launch, clusters of 16"),
+    (lambda: W.make_workload("linear_b1_g4_v32000_f32", B=12), "one launch, clusters of 8"),
     (lambda: W.make_workload("linear_b64_g5_v32000_bf16"), "one launch, clusters of 2"),
 ]
 

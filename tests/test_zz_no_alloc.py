@@ -58,7 +58,7 @@ def _with_workspace(w):
 def test_static_entry_point_matches_the_workspace_one(lib):
     from speculative_decoding_verification_64_gb300 import binding
     cases = [
-        # the one-launch path of small batches (clusters of 8 and of 2 CTAs)
+        # the one-launch path of small batches (clusters of 16 and of 2 CTAs)
         (W.make_workload("linear_b1_g4_v32000_f32", B=2), binding.PATH_SMALL_ONE_LAUNCH),
         (W.make_workload("mixed_b512_g4_v152064_bf16", B=40, V=20000, seed_offset=7),
          binding.PATH_SMALL_ONE_LAUNCH),
