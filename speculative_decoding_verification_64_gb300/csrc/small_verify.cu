@@ -414,8 +414,9 @@ int cluster_capacity(int C) {
     cfg.numAttrs = 1;
     int m = 0;
     if (cudaOccupancyMaxActiveClusters(&m, kernel, &cfg) == cudaSuccess) n = m;
+    else ok = false;
   }
-  (void)cudaGetLastError();  // a refused query leaves no error behind
+  if (!ok) (void)cudaGetLastError();  // a refused query leaves no error behind
   if (dev < kMaxCachedDevices) g_capacity[dev][i].store(n + 2, std::memory_order_relaxed);
   return n;
 }
