@@ -56,6 +56,31 @@ struct TreeSmem {
   alignas(8) uint64_t rbar;  // the other CTAs' merged rows have arrived
 };
 
+// warp_merge_row of a row of at most 32 stages whose partial x this lane
+// holds (has: lane < the row's stage count): the same merges in the same
+// order, so the result is bit-identical.
+__device__ __forceinline__ RowStat warp_merge_one(const float4 x, bool has, float c) {
+  float m = -INFINITY, s = 0.0f;
+  int a = 0x7FFFFFFF, fl = 0;
+  if (has) {
+    fl |= __float_as_int(x.w);
+    merge2(m, s, a, x.x, x.y, __float_as_int(x.z), c);
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, d);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, d);
+    const int a2 = __shfl_xor_sync(0xffffffffu, a, d);
+    merge2(m, s, a, m2, s2, a2, c);
+  }
+  RowStat r;
+  r.M = m;
+  r.S = s;
+  r.arg = a;
+  r.flags = __reduce_or_sync(0xffffffffu, fl);
+  return r;
+}
+
 __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -89,6 +114,14 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
   // first remote store)
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
+  // The stage partials of the first row this warp merges (rows of at most 32
+  // stages: one partial a lane), loaded now so that their round trip overlaps
+  // the structure loads below rather than following them.
+  const int n_first = rank + kG * warp;
+  const bool hoisted = p.spr <= 32;
+  float4 x_first = make_float4(-INFINITY, 0.0f, __int_as_float(0x7FFFFFFF), 0.0f);
+  if (hoisted && n_first < N && lane < p.spr)
+    x_first = reinterpret_cast<const float4 *>(p.part + (nodebase + n_first) * (long long)p.spr)[lane];
   // ---- structure, the drafted tokens' logits and q values ---------------------
   int st = 0;
   for (int n = tid; n < N; n += kThreads) {
@@ -121,7 +154,8 @@ __global__ void __cluster_dims__(kG, 1, 1) __launch_bounds__(kThreads, 2)
   // then pushed to the other CTAs by asynchronous remote stores that complete
   // on their barrier rbar (one round trip, no cluster-wide barrier)
   for (int n = rank + kG * warp; n < N; n += kG * kWarps) {
-    const RowStat r = warp_merge_row(p.part, nodebase + n, p.spr, c, lane);
+    const RowStat r = (hoisted && n == n_first) ? warp_merge_one(x_first, lane < p.spr, c)
+                                                : warp_merge_row(p.part, nodebase + n, p.spr, c, lane);
     if (lane == 0) {
       sm.rowM[n] = r.M;
       sm.rowS[n] = r.S;
